@@ -1,0 +1,443 @@
+"""Benchmark of the DLRM embedding + dot-interaction hot path on GB300.
+
+One step = one pass of the whole path over one batch of 65,536 samples:
+    dlrm_emb_fwd -> dlrm_interact_fwd -> dlrm_interact_bwd -> dlrm_emb_bwd_sgd
+on the DLRM-default shapes (26 single-hot tables with log-uniform row counts in
+[10, 4e6], D = 128, 13 lognormal dense features through the 13-512-256-128
+bottom MLP, 480 interaction columns), FP32 master tables, Zipf(1.2) indices,
+upstream gradient N(0, 1e-2), SGD lr 0.1.  The forward alone at the same batch
+with fp16 tables and Zipf(1.05) indices is reported under "fwd".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  With N > 1 (torchrun) every rank runs its own
+replica on its own GPU (weak scaling; the path needs no exchange between GPUs).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DLRM emb+interaction samples/s at batch 64K (fwd, fwd+bwd); % of HBM peak"
+BATCH = 65536
+ALPHA_TRAIN = 1.2
+ALPHA_FWD = 1.05
+LR = 0.1
+L2_BYTES = 129 * 2**20
+WORKLOAD = ("dlrm-default 64K training step: 26 single-hot fp32 tables (rows log-uniform 10..4e6), "
+            "D=128, Zipf 1.2, 480 interaction columns, SGD lr 0.1")
+
+
+# ---------------------------------------------------------------- utilities
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when there is one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dlrm_clocks_{os.getpid()}.csv")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def lib_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "dlrm_embeddings_dot_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, digest: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_digest") != digest:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ oracle (CPU)
+def cpu_oracle_step(w, samples: np.ndarray) -> float:
+    """Time the CPU oracle on the step for a sample of the batch; returns seconds."""
+    import oracle
+    from dlrm_embeddings_dot_gb300.inputs import Compact
+    c = Compact(w, samples)
+    t0 = time.perf_counter()
+    pooled, _ = oracle.emb_fwd(c.tables, c.row_base, c.F, c.D, c.B, c.indices, c.offsets)
+    oracle.interact_fwd(c.dense, pooled, w.out_cols)
+    _, gp = oracle.interact_bwd(c.grad_out, c.dense, pooled)
+    oracle.emb_bwd_sgd(c.tables, c.row_base, c.F, c.D, c.B, c.indices, c.offsets, gp, w.lr)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, n_samples: int) -> dict:
+    samples = np.arange(n_samples)
+    dt = cpu_oracle_step(w, samples)
+    return {"value": n_samples / dt, "unit": "samples/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n_samples} of the {w.B} samples of the same batch (tables compacted to the "
+                      f"rows they touch); single-threaded C oracle, double accumulation; {dt:.2f} s"}
+
+
+# ------------------------------------------------------------- GPU benchmark
+def kernels_per_step(total_rows: int) -> int:
+    nbits = int(total_rows).bit_length()
+    npasses = (nbits + 7) // 8
+    # emb_fwd, interact_fwd, interact_bwd, then keys + 3 per radix pass + segment + fixup
+    return 3 + 1 + 3 * npasses + 2
+
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import dlrm_embeddings_dot_gb300 as dl
+    from dlrm_embeddings_dot_gb300 import inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dl.load()
+    stream = torch.cuda.Stream(device=dev)
+    B = args.batch
+
+    # ---- inputs (rank-specific seed: each replica trains on its own batch)
+    w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, seed=rank, train=True)
+    F, D, P = w.F, w.D, w.out_cols
+    with torch.cuda.stream(stream):
+        tables = torch.empty(w.total_rows, D, dtype=torch.float32, device=dev)
+        dl.dlrm_synth_fill_uniform(tables, w.table_seed, 0, stream=stream)
+        row_base = torch.from_numpy(w.row_base).to(dev)
+        idx = torch.from_numpy(w.indices).to(dev)
+        off = torch.from_numpy(w.offsets).to(dev)
+        dense = torch.from_numpy(w.dense).to(dev)
+        grad_out = torch.from_numpy(w.grad_out).to(dev)
+        pooled = torch.empty(B, F, D, device=dev)
+        out = torch.empty(B, P, device=dev)
+        gd = torch.empty(B, D, device=dev)
+        gp = torch.empty(B, F, D, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
+                         device=dev)
+    torch.cuda.synchronize()
+    nnz = w.nnz
+
+    ev = {k: [] for k in ("emb_fwd", "interact_fwd", "interact_bwd", "emb_bwd_sgd")}
+
+    def step(record=False):
+        marks = []
+        if record:
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            marks[0].record(stream)
+        dl.dlrm_emb_fwd(tables, row_base, F, D, B, idx, off, pooled, status=status, stream=stream)
+        if record:
+            marks[1].record(stream)
+        dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)
+        if record:
+            marks[2].record(stream)
+        dl.dlrm_interact_bwd(grad_out, dense, pooled, F, D, B, P, gd, gp, stream=stream)
+        if record:
+            marks[3].record(stream)
+        dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status,
+                            stream=stream)
+        if record:
+            marks[4].record(stream)
+            for k, (a, b) in zip(ev, zip(marks[:-1], marks[1:])):
+                ev[k].append((a, b))
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- per-op durations (events on the launching stream), separate from the timed loop
+    for _ in range(max(5, min(args.steps, 50))):
+        step(record=True)
+    torch.cuda.synchronize()
+    op_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+
+    # ---- timed region (inputs > L2: the 4.1 GB tables and 0.9 GB pooled/grad tensors)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = reduce_max(t0.elapsed_time(t1), world, dev)
+    st = int(status.item())
+    value = B * world * args.steps / (ms / 1e3)
+
+    # ---- forward only, configs' fp16 DLRM-default: Zipf 1.05, tensor-core interaction
+    wf = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, seed=rank)
+    with torch.cuda.stream(stream):
+        tab16 = torch.empty(wf.total_rows, D, dtype=torch.float16, device=dev)
+        dl.dlrm_synth_fill_uniform(tab16, wf.table_seed, 0, stream=stream)
+        rb16 = torch.from_numpy(wf.row_base).to(dev)
+        idx16 = torch.from_numpy(wf.indices).to(dev)
+        off16 = torch.from_numpy(wf.offsets).to(dev)
+        dense16 = torch.from_numpy(wf.dense.astype(np.float16)).to(dev)
+        pooled16 = torch.empty(B, F, D, dtype=torch.float16, device=dev)
+        out16 = torch.empty(B, P, dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+
+    def fstep():
+        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, idx16, off16, pooled16, status=status, stream=stream)
+        dl.dlrm_interact_fwd(dense16, pooled16, F, D, B, out16, P, status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        fstep()
+    fev = []
+    for _ in range(max(5, min(args.steps, 50))):
+        m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        m[0].record(stream)
+        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, idx16, off16, pooled16, status=status, stream=stream)
+        m[1].record(stream)
+        dl.dlrm_interact_fwd(dense16, pooled16, F, D, B, out16, P, status=status, stream=stream)
+        m[2].record(stream)
+        fev.append(m)
+    torch.cuda.synchronize()
+    f_emb = statistics.mean(m[0].elapsed_time(m[1]) for m in fev)
+    f_int = statistics.mean(m[1].elapsed_time(m[2]) for m in fev)
+    barrier(world)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        fstep()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fms = reduce_max(f0.elapsed_time(f1), world, dev)
+    del tab16, pooled16, out16
+
+    # ---- end to end through the public API from pinned host buffers
+    h_dense = torch.from_numpy(w.dense).pin_memory()
+    h_idx = torch.from_numpy(w.indices).pin_memory()
+    h_off = torch.from_numpy(w.offsets).pin_memory()
+    h_go = torch.from_numpy(w.grad_out).pin_memory()
+    h_out = torch.empty(B, P).pin_memory()
+    h_gd = torch.empty(B, D).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_dense, h_idx, h_off, h_go))
+    d2h = h_out.numel() * 4 + h_gd.numel() * 4
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dense.copy_(h_dense, non_blocking=True)
+            idx.copy_(h_idx, non_blocking=True)
+            off.copy_(h_off, non_blocking=True)
+            grad_out.copy_(h_go, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_gd.copy_(gd, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, args.steps // 4)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = reduce_max(e0.elapsed_time(e1), world, dev)
+
+    # ---- roofline of the dominant kernel (algorithmic bytes per launch / event time)
+    peaks = measured_peaks()
+    unique_rows = None
+    keys = ws[: 4 * nnz].view(torch.int32)
+    k = keys[keys != -1]
+    if k.numel():
+        unique_rows = int(torch.unique_consecutive(k).numel())
+    s = 4  # fp32
+    alg = {
+        "emb_fwd": B * F * (4 + 4 + D * s) + B * F * D * s,
+        "interact_fwd": B * (D * s + F * D * s + P * s),
+        "interact_bwd": B * (P * 4 + D * s + F * D * s + D * 4 + F * D * 4),
+        "emb_bwd_sgd": nnz * (4 + 4 + D * 4) + (unique_rows or 0) * 2 * D * 4,
+    }
+    dom = max(op_ms, key=op_ms.get)
+    kernel_names = {"emb_fwd": "emb_fwd_single_kernel", "interact_fwd": "interact_fwd_ffma_kernel",
+                    "interact_bwd": "interact_bwd_kernel", "emb_bwd_sgd": "emb_bwd_sgd (12 kernels)"}
+    achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": ncu_traffic(kernel_names[dom], lib_digest()),
+            "algorithmic_bytes_per_launch": alg[dom], "launch_ms": round(op_ms[dom], 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; Criteo Terabyte not available)",
+        "config": {"workload": WORKLOAD, "global_batch": B * world, "per_gpu_batch": B, "tables": F,
+                   "embedding_dim": D, "total_rows": w.total_rows, "nnz": nnz, "out_cols": P,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (4.1 GB tables, 0.87 GB pooled/grad tensors per step)"},
+        "ops_ms": {k: round(v, 4) for k, v in op_ms.items()},
+        "fwd": {"value": round(B * world * args.steps / (fms / 1e3), 1), "unit": "samples/s",
+                "ms_per_step": round(fms / args.steps, 4), "dtype": "f16 storage, f32 accumulate",
+                "workload": "dlrm-default 64K forward: 26 single-hot fp16 tables, Zipf 1.05, 480 columns",
+                "ops_ms": {"emb_fwd": round(f_emb, 4), "interact_fwd_tcgen05": round(f_int, 4)},
+                "alg_GBps": {"emb_fwd": round(B * F * (8 + 2 * D * 2) / (f_emb / 1e3) / 1e9, 1),
+                             "interact_fwd": round(B * (D * 2 + F * D * 2 + P * 2) / (f_int / 1e3) / 1e9, 1)}},
+        "e2e": {"value": round(B * world * e_steps / (ems / 1e3), 1), "unit": "samples/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels_per_step(w.total_rows) * args.steps,
+        "clocks": clk,
+        "roofline": roof,
+        "device_status": st,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_samples)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args) -> None:
+    """The CPU oracle, timed as it stands, on bounded samples of the same workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from dlrm_embeddings_dot_gb300 import inputs
+    w = inputs.dlrm_default(B=BATCH, dtype=inputs.F32, alpha=ALPHA_TRAIN, seed=0, train=True)
+    n = args.ref_samples
+    for i in range(args.warmup):
+        cpu_oracle_step(w, np.arange(n) + (i * n) % (w.B - n))
+    total = 0.0
+    for i in range(args.steps):
+        total += cpu_oracle_step(w, np.arange(n) + ((i + args.warmup) * n) % (w.B - n))
+    value = n * args.steps / total
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "samples/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps * (BATCH / n), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": BATCH, "per_gpu_batch": BATCH},
+        "cpu_baseline": {"value": round(value, 1), "unit": "samples/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} samples of the 65,536-sample batch per step"},
+        "e2e": {"value": round(value, 1), "unit": "samples/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=BATCH)
+    ap.add_argument("--cpu-samples", type=int, default=32768,
+                    help="samples of the batch the CPU-oracle baseline runs on (about 10 s of CPU)")
+    ap.add_argument("--ref-samples", type=int, default=512,
+                    help="samples per step of the --impl reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

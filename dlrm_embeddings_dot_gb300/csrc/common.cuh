@@ -1,0 +1,104 @@
+// common.cuh -- shared host/device helpers of the CUDA library (not the oracle).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+
+#include "dlrm.h"
+
+namespace dlrm {
+
+// ---------------------------------------------------------------- host side
+void set_error(const char* fmt, ...);
+void clear_error();
+
+inline dlrm_status fail(dlrm_status code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    set_error("%s", buf);
+    return code;
+}
+
+inline dlrm_status check_launch(const char* what)
+{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return DLRM_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int dtype_size(dlrm_dtype dt) { return dt == DLRM_F16 ? 2 : 4; }
+inline bool dtype_ok(dlrm_dtype dt) { return dt == DLRM_F32 || dt == DLRM_F16; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int num_sms();   // SM count of the current device (cached per device)
+
+// -------------------------------------------------------------- device side
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit)
+{
+    if (status) atomicOr(status, bit);
+}
+
+// 16-byte read-only load that does not allocate in L1 (rows are streamed).
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte streaming store (evict-first: outputs are not re-read by this kernel).
+__device__ __forceinline__ void stg_cs_v4(void* p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 u4_as_f4(uint4 v)
+{
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                       __uint_as_float(v.w));
+}
+
+__device__ __forceinline__ uint4 f4_as_u4(float4 v)
+{
+    return make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                      __float_as_uint(v.w));
+}
+
+// 8 halves packed in a uint4 -> 8 floats (exact widening).
+__device__ __forceinline__ void h8_to_f8(uint4 v, float* f)
+{
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// 8 floats -> 8 halves (round to nearest even) packed in a uint4.
+__device__ __forceinline__ uint4 f8_to_h8(const float* f)
+{
+    uint4 v;
+    __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+}  // namespace dlrm

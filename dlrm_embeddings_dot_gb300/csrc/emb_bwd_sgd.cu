@@ -1,0 +1,528 @@
+// emb_bwd_sgd.cu -- sparse embedding gradient fused with the SGD row update.
+//
+// The gradient of the sum pooling ("DLRM For PyTorch", §Model architecture)
+// sends grad_pooled[b][t] to every row of bag (t, b); the tables are FP32
+// (§Training process) and only touched rows change (--embedding_type
+// joint_sparse).  No dense gradient table is formed:
+//
+//  1. keys: position p of bag (t, b) -> (key = global row, val = b*F + t);
+//     skipped indices get key 0xFFFFFFFF.
+//  2. stable LSD radix sort of (key, val) over the bits that can be set,
+//     8 bits per pass, reduce-then-scan (no inter-block waiting):
+//     per-tile digit histograms -> per-digit scan over tiles -> stable
+//     scatter with warp-level ranking (match.any) in position order.
+//  3. segments: the sorted array is cut into chunks of 32 positions; a warp
+//     sums, in ascending position order, the grad rows of each run of equal
+//     keys inside its chunk.  A run wholly inside the chunk updates its row
+//     at once (w = fmaf(-lr, g, w)); a run crossing a chunk edge leaves one
+//     partial sum per chunk it touches.
+//  4. fixup: one block per run that crossed a chunk edge adds its partial
+//     sums in a fixed order and updates the row.
+// Every order of summation is fixed by the data, so results are bitwise
+// reproducible.  Workspace layout (256-byte aligned pieces):
+//   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
+//   partials[2 * nchunks][D] | split_list[nchunks] | counter
+// The sort ends in keysA/valsA, which the caller may read after the call.
+#include "common.cuh"
+
+namespace dlrm {
+namespace {
+
+constexpr uint32_t kSkipKey = 0xFFFFFFFFu;
+constexpr int kSortThreads = 256;
+constexpr int kItems = 8;
+constexpr int kTile = kSortThreads * kItems;   // 2048 keys per tile
+constexpr int kChunk = 32;                     // positions per segment chunk
+constexpr int kFixThreads = 256;
+
+struct Ws {
+    uint32_t *keys[2], *vals[2];
+    uint32_t* hist;
+    uint32_t* totals;
+    float* partials;
+    uint32_t* split_list;
+    uint32_t* split_count;
+    size_t bytes;
+};
+
+Ws carve(void* base, int64_t nnz, int D)
+{
+    Ws w;
+    const int64_t ntiles = (nnz + kTile - 1) / kTile;
+    const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* q = p ? p + off : nullptr;
+        off += dlrm_ws_align(bytes);
+        return q;
+    };
+    w.keys[0] = (uint32_t*)take(4 * (size_t)nnz);
+    w.vals[0] = (uint32_t*)take(4 * (size_t)nnz);
+    w.keys[1] = (uint32_t*)take(4 * (size_t)nnz);
+    w.vals[1] = (uint32_t*)take(4 * (size_t)nnz);
+    w.hist = (uint32_t*)take(4 * 256 * (size_t)ntiles);
+    w.totals = (uint32_t*)take(4 * 256);
+    w.partials = (float*)take(4 * 2 * (size_t)nchunks * D);
+    w.split_list = (uint32_t*)take(4 * (size_t)nchunks);
+    w.split_count = (uint32_t*)take(4);
+    w.bytes = off;
+    return w;
+}
+
+// ------------------------------------------------------------------ 1. keys
+template <int G>
+__global__ void __launch_bounds__(256)
+keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* __restrict__ indices,
+            const int32_t* __restrict__ offsets, bool hash, uint32_t* status, uint32_t* __restrict__ keys,
+            uint32_t* __restrict__ vals, int64_t nbags)
+{
+    const int lane = threadIdx.x % G;
+    const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
+    for (int64_t g = group; g < nbags; g += ngroups) {   // g = t*B + b (feature-major, like offsets)
+        const int t = (int)(g / B);
+        const int b = (int)(g - (int64_t)t * B);
+        const int64_t base = row_base[t], n = row_base[t + 1] - base;
+        const uint32_t val = (uint32_t)((int64_t)b * F + t);
+        const int64_t s = offsets[g], e = offsets[g + 1];
+        for (int64_t p = s + lane; p < e; p += G) {
+            int64_t i = indices[p];
+            uint32_t key = kSkipKey;
+            if (hash) {
+                if (n > 0) {
+                    i %= n;
+                    if (i < 0) i += n;
+                    key = (uint32_t)(base + i);
+                } else {
+                    set_status(status, DLRM_STATUS_OOB_INDEX);
+                }
+            } else if (i >= 0 && i < n) {
+                key = (uint32_t)(base + i);
+            } else {
+                set_status(status, DLRM_STATUS_OOB_INDEX);
+            }
+            keys[p] = key;
+            vals[p] = val;
+        }
+    }
+}
+
+// ------------------------------------------------------- block scan helper
+// Exclusive scan of one value per thread over a block of kSortThreads threads.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total)
+{
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == kWarp - 1) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < kSortThreads / kWarp ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kSortThreads / kWarp) warp_sums[lane] = w;   // inclusive
+    }
+    __syncthreads();
+    const uint32_t before = warp > 0 ? warp_sums[warp - 1] : 0;
+    if (total) *total = warp_sums[kSortThreads / kWarp - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+// ------------------------------------------------------------ 2. radix sort
+__global__ void __launch_bounds__(kSortThreads)
+radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t mask, uint32_t* __restrict__ hist,
+              int64_t ntiles)
+{
+    __shared__ uint32_t h[256];
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kTile;
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t p = base + r * kSortThreads + threadIdx.x;
+        if (p < n) atomicAdd(&h[(keys[p] >> shift) & mask], 1u);
+    }
+    __syncthreads();
+    hist[(int64_t)threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
+}
+
+// One block per digit: exclusive scan of hist[d][0..ntiles) in place, total to totals[d].
+__global__ void __launch_bounds__(kSortThreads)
+radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ totals)
+{
+    __shared__ uint32_t warp_sums[kSortThreads / kWarp];
+    __shared__ uint32_t chunk_total;
+    uint32_t* row = hist + (int64_t)blockIdx.x * ntiles;
+    uint32_t carry = 0;
+    for (int64_t c0 = 0; c0 < ntiles; c0 += kTile) {
+        uint32_t v[kItems];
+        uint32_t s = 0;
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int64_t i = c0 + (int64_t)threadIdx.x * kItems + r;
+            v[r] = i < ntiles ? row[i] : 0;
+            s += v[r];
+        }
+        uint32_t ex = block_excl_scan(s, warp_sums, &chunk_total);
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int64_t i = c0 + (int64_t)threadIdx.x * kItems + r;
+            if (i < ntiles) row[i] = carry + ex;
+            ex += v[r];
+        }
+        carry += chunk_total;
+    }
+    if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+}
+
+__global__ void __launch_bounds__(kSortThreads)
+radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
+                uint32_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out, int64_t n, int shift,
+                uint32_t mask, const uint32_t* __restrict__ hist, const uint32_t* __restrict__ totals,
+                int64_t ntiles)
+{
+    constexpr int kW = kSortThreads / kWarp;
+    __shared__ uint32_t wcnt[kW][256];
+    __shared__ uint32_t dbase[256];
+    __shared__ uint32_t warp_sums[kW];
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    const uint32_t lt = (1u << lane) - 1u;
+
+    // global start of each digit in this tile
+    const uint32_t ex = block_excl_scan(totals[threadIdx.x], warp_sums, nullptr);
+    dbase[threadIdx.x] = ex + hist[(int64_t)threadIdx.x * ntiles + blockIdx.x];
+#pragma unroll
+    for (int w = 0; w < kW; ++w) wcnt[w][threadIdx.x] = 0;
+    __syncthreads();
+
+    uint32_t key[kItems], val[kItems], local[kItems];
+    const int64_t wbase = (int64_t)blockIdx.x * kTile + (int64_t)warp * kWarp * kItems;
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t p = wbase + r * kWarp + lane;
+        const bool valid = p < n;
+        key[r] = valid ? keys_in[p] : 0;
+        val[r] = valid ? vals_in[p] : 0;
+        const uint32_t d = (key[r] >> shift) & mask;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 0x100u);
+        const uint32_t prior = valid ? wcnt[warp][d] : 0;
+        __syncwarp();
+        if (valid && (peers & lt) == 0) wcnt[warp][d] = prior + __popc(peers);
+        __syncwarp();
+        local[r] = prior + __popc(peers & lt);
+    }
+    __syncthreads();
+    {   // exclusive scan over warps, per digit
+        uint32_t s = 0;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+            const uint32_t c = wcnt[w][threadIdx.x];
+            wcnt[w][threadIdx.x] = s;
+            s += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t p = wbase + r * kWarp + lane;
+        if (p < n) {
+            const uint32_t d = (key[r] >> shift) & mask;
+            const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
+            keys_out[pos] = key[r];
+            vals_out[pos] = val[r];
+        }
+    }
+}
+
+// --------------------------------------------------------- 3. segment sums
+template <int MC>
+__global__ void __launch_bounds__(256)
+segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
+               const float* __restrict__ grad, int D, float* __restrict__ tables, float lr,
+               float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
+               int64_t nchunks)
+{
+    const int lane = threadIdx.x % kWarp;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
+    const int c4 = D / 4;   // float4 columns per row
+    for (int64_t c = warp_id; c < nchunks; c += nwarps) {
+        const int64_t p0 = c * kChunk;
+        const int64_t p = p0 + lane;
+        const uint32_t key = p < n ? keys[p] : kSkipKey;
+        const uint32_t val = p < n ? vals[p] : 0;
+        uint32_t prev = __shfl_up_sync(0xffffffffu, key, 1);
+        if (lane == 0) prev = p0 > 0 ? keys[p0 - 1] : ~key;
+        const uint32_t after = (p0 + kChunk < n) ? keys[p0 + kChunk] : kSkipKey;
+        const bool valid = key != kSkipKey;
+        const uint32_t heads = __ballot_sync(0xffffffffu, valid && prev != key);
+        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+        if (vmask == 0) continue;
+        const int nvalid = 32 - __clz(vmask);             // valid lanes are a prefix
+        uint32_t starts = heads | 1u;                     // lane 0 starts a run piece
+        while (starts) {
+            const int s = __ffs(starts) - 1;
+            starts &= starts - 1;
+            if (s >= nvalid) break;
+            const int e = starts ? min(__ffs(starts) - 1, nvalid) : nvalid;
+            const uint32_t skey = __shfl_sync(0xffffffffu, key, s);
+            float4 acc[MC];
+#pragma unroll
+            for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = s; q < e; q += 4) {
+                float4 v[4][MC];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t row = __shfl_sync(0xffffffffu, val, (q + u) & 31);
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        const int col = lane + m * kWarp;
+                        v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (q + u < e && col < c4)
+                            v[u][m] = u4_as_f4(ldg_nc_v4(grad + (int64_t)row * D + 4 * col));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (q + u < e)
+#pragma unroll
+                        for (int m = 0; m < MC; ++m) {
+                            acc[m].x += v[u][m].x;
+                            acc[m].y += v[u][m].y;
+                            acc[m].z += v[u][m].z;
+                            acc[m].w += v[u][m].w;
+                        }
+            }
+            const bool starts_here = (heads >> s) & 1u;
+            const bool ends_here = e < 32 || after != skey;
+            if (starts_here && ends_here) {
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    const int col = lane + m * kWarp;
+                    if (col < c4) {
+                        float4* w = reinterpret_cast<float4*>(tables + (int64_t)skey * D + 4 * col);
+                        float4 x = *w;
+                        x.x = fmaf(-lr, acc[m].x, x.x);
+                        x.y = fmaf(-lr, acc[m].y, x.y);
+                        x.z = fmaf(-lr, acc[m].z, x.z);
+                        x.w = fmaf(-lr, acc[m].w, x.w);
+                        *w = x;
+                    }
+                }
+            } else {
+                const int64_t slot = 2 * c + (starts_here ? 1 : 0);
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    const int col = lane + m * kWarp;
+                    if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
+                }
+                if (starts_here && lane == 0) split_list[atomicAdd(split_count, 1u)] = (uint32_t)c;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- 4. fixup
+template <int MC>
+__global__ void __launch_bounds__(kFixThreads)
+fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
+             const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ split_count, int D,
+             float* __restrict__ tables, float lr)
+{
+    constexpr int kW = kFixThreads / kWarp;
+    extern __shared__ __align__(16) float red[];   // [kW][D]
+    __shared__ int64_t s_end;
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    const int c4 = D / 4;
+    const uint32_t count = *split_count;
+    for (uint32_t i = blockIdx.x; i < count; i += gridDim.x) {
+        const int64_t c0 = split_list[i];
+        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
+        if (threadIdx.x == 0) {   // first position after the run: keys are sorted
+            int64_t lo = c0 * kChunk + kChunk, hi = n;
+            while (lo < hi) {
+                const int64_t mid = lo + (hi - lo) / 2;
+                if (keys[mid] == K) lo = mid + 1;
+                else hi = mid;
+            }
+            s_end = lo;
+        }
+        __syncthreads();
+        const int64_t c_end = (s_end - 1) / kChunk;
+        const int64_t pieces = c_end - c0 + 1;
+        float4 acc[MC];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t j = warp; j < pieces; j += kW) {
+            const int64_t slot = j == 0 ? 2 * c0 + 1 : 2 * (c0 + j);
+#pragma unroll
+            for (int m = 0; m < MC; ++m) {
+                const int col = lane + m * kWarp;
+                if (col < c4) {
+                    const float4 v = reinterpret_cast<const float4*>(partials + slot * D)[col];
+                    acc[m].x += v.x;
+                    acc[m].y += v.y;
+                    acc[m].z += v.z;
+                    acc[m].w += v.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+            const int col = lane + m * kWarp;
+            if (col < c4) reinterpret_cast<float4*>(red + warp * D)[col] = acc[m];
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int m = 0; m < MC; ++m) {
+                const int col = lane + m * kWarp;
+                if (col < c4) {
+                    float4 g = reinterpret_cast<const float4*>(red)[col];
+                    for (int w = 1; w < kW; ++w) {
+                        const float4 v = reinterpret_cast<const float4*>(red + w * D)[col];
+                        g.x += v.x;
+                        g.y += v.y;
+                        g.z += v.z;
+                        g.w += v.w;
+                    }
+                    float4* wp = reinterpret_cast<float4*>(tables + (int64_t)K * D + 4 * col);
+                    float4 x = *wp;
+                    x.x = fmaf(-lr, g.x, x.x);
+                    x.y = fmaf(-lr, g.y, x.y);
+                    x.z = fmaf(-lr, g.z, x.z);
+                    x.w = fmaf(-lr, g.w, x.w);
+                    *wp = x;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+int key_bits(int64_t total_rows)
+{
+    int b = 0;
+    while (b < 32 && ((uint64_t)1 << b) <= (uint64_t)total_rows) ++b;   // 2^b > total_rows
+    return b;
+}
+
+template <int MC>
+dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, float* tables, float lr,
+                            cudaStream_t st)
+{
+    const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
+    int64_t blocks = (nchunks * kWarp + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    segment_kernel<MC><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, lr, w.partials,
+                                                    w.split_list, w.split_count, nchunks);
+    dlrm_status s = check_launch("segment_kernel");
+    if (s != DLRM_OK) return s;
+    int64_t fblocks = nchunks < (int64_t)num_sms() * 4 ? nchunks : (int64_t)num_sms() * 4;
+    const size_t smem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fixup_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
+    }
+    fixup_kernel<MC><<<(int)fblocks, kFixThreads, smem, st>>>(w.keys[0], nnz, w.partials, w.split_list,
+                                                              w.split_count, D, tables, lr);
+    return check_launch("fixup_kernel");
+}
+
+}  // namespace
+}  // namespace dlrm
+
+using namespace dlrm;
+
+extern "C" size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows)
+{
+    if (nnz < 0 || nnz >= ((int64_t)1 << 31) || D < 1 || D % 4 != 0 || D > 1024 || total_rows < 1 ||
+        total_rows >= 0xFFFFFFFFll)
+        return 0;
+    return carve(nullptr, nnz, D).bytes;
+}
+
+extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t total_rows, int F,
+                                        int D, int B, const int32_t* d_indices, const int32_t* d_offsets,
+                                        int64_t nnz, const float* d_grad_pooled, float lr, void* d_workspace,
+                                        size_t workspace_bytes, unsigned flags, uint32_t* d_status, void* stream)
+{
+    clear_error();
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: need F >= 1, D >= 1, B >= 0");
+    if (nnz < 0 || nnz >= ((int64_t)1 << 31))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: nnz must be in [0, 2^31)");
+    if ((int64_t)F * B >= ((int64_t)1 << 31))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: F*B must be below 2^31");
+    if (total_rows < 1 || total_rows >= 0xFFFFFFFFll)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: total_rows must be in [1, 2^32 - 1)");
+    if (!d_tables || !d_row_base || !d_offsets || !d_grad_pooled || (nnz > 0 && (!d_indices || !d_workspace)))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: null device pointer");
+    if (flags & ~DLRM_FLAG_HASH_INDICES)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: unknown flag bits 0x%x", flags);
+    if (D % 4 != 0 || D > 1024)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: D must be a multiple of 4, at most 1024");
+    if (!aligned16(d_tables) || !aligned16(d_grad_pooled))
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: tables and grad_pooled must be 16-byte aligned");
+    if (nnz > 0 && (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: workspace must be 256-byte aligned");
+    const size_t need = dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows);
+    if (nnz > 0 && workspace_bytes < need)
+        return fail(DLRM_ERR_WORKSPACE, "dlrm_emb_bwd_sgd: workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (nnz == 0 || B == 0) return DLRM_OK;
+
+    cudaStream_t st = as_stream(stream);
+    Ws w = carve(d_workspace, nnz, D);
+    const int nbits = key_bits(total_rows);
+    const int npasses = (nbits + 7) / 8;
+    int cur = npasses & 1;   // the last pass lands in buffer 0
+    cudaError_t ce = cudaMemsetAsync(w.split_count, 0, sizeof(uint32_t), st);
+    if (ce != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(ce));
+
+    const int64_t nbags = (int64_t)F * B;
+    const bool multi = nnz > 2 * nbags;
+    const bool hash = (flags & DLRM_FLAG_HASH_INDICES) != 0;
+    {
+        const int G = multi ? 32 : 1;
+        int64_t blocks = (nbags * G + 255) / 256;
+        const int64_t cap = (int64_t)num_sms() * 8;
+        if (blocks > cap) blocks = cap;
+        if (multi)
+            keys_kernel<32><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
+                                                         w.keys[cur], w.vals[cur], nbags);
+        else
+            keys_kernel<1><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
+                                                        w.keys[cur], w.vals[cur], nbags);
+        dlrm_status s = check_launch("keys_kernel");
+        if (s != DLRM_OK) return s;
+    }
+    const int64_t ntiles = (nnz + kTile - 1) / kTile;
+    for (int pass = 0; pass < npasses; ++pass) {
+        const int shift = 8 * pass;
+        const int bits = nbits - shift < 8 ? nbits - shift : 8;
+        const uint32_t mask = (1u << bits) - 1u;
+        radix_upsweep<<<(int)ntiles, kSortThreads, 0, st>>>(w.keys[cur], nnz, shift, mask, w.hist, ntiles);
+        radix_scan<<<256, kSortThreads, 0, st>>>(w.hist, ntiles, w.totals);
+        radix_downsweep<<<(int)ntiles, kSortThreads, 0, st>>>(w.keys[cur], w.vals[cur], w.keys[cur ^ 1],
+                                                              w.vals[cur ^ 1], nnz, shift, mask, w.hist, w.totals,
+                                                              ntiles);
+        dlrm_status s = check_launch("radix sort pass");
+        if (s != DLRM_OK) return s;
+        cur ^= 1;
+    }
+    const float* grad = d_grad_pooled;
+    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, lr, st);
+    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, lr, st);
+    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, lr, st);
+    return launch_segments<8>(w, nnz, grad, D, d_tables, lr, st);
+}

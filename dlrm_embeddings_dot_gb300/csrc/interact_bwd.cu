@@ -1,0 +1,160 @@
+// interact_bwd.cu -- gradient of the dot interaction ("DLRM For PyTorch",
+// §Model architecture: interaction output = dense vector followed by the
+// pairwise dot products).  With G the upstream gradient row and M the
+// symmetric (F+1)x(F+1) matrix holding G's triangle (zero diagonal),
+//   dZ = M Z,  grad_dense = G[0..D) + dZ_0,  grad_pooled[t] = dZ_{t+1}.
+//
+// One warp per sample.  M is expanded into shared memory (row stride padded
+// to a multiple of 4 so a row is read with broadcast float4 loads); lane l
+// owns columns l + 32m of Z, held in registers for all F+1 rows, so each
+// output element is an in-register fp32 FMA chain over j (fixed order).
+// Columns are processed 64 at a time; every global access is a coalesced
+// 128-byte row segment.
+#include "common.cuh"
+
+namespace dlrm {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMC = 2;   // columns per lane per pass (64-column passes)
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p)
+{
+    if constexpr (sizeof(T) == 4)
+        return __ldg(reinterpret_cast<const float*>(p));
+    else
+        return __half2float(*p);
+}
+
+template <typename T, int RMAX>
+__global__ void __launch_bounds__(kWarps * kWarp)
+interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ dense,
+                    const T* __restrict__ pooled, int F, int D, int B, int P,
+                    float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
+{
+    constexpr int RS = RMAX;                     // smem row stride of M (multiple of 4)
+    __shared__ __align__(16) float msh[kWarps][RMAX * RS];
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int R = F + 1;
+    float* M = msh[warp];
+    const int warps_total = gridDim.x * kWarps;
+
+    for (int b = blockIdx.x * kWarps + warp; b < B; b += warps_total) {
+        const float* G = grad_out + (int64_t)b * P;
+        __syncwarp();
+        for (int x = lane; x < RMAX * RS; x += kWarp) {
+            const int i = x / RS, j = x % RS;
+            float v = 0.f;
+            if (i < R && j < R && i != j) {
+                const int hi = i > j ? i : j, lo = i > j ? j : i;
+                v = __ldg(G + D + hi * (hi - 1) / 2 + lo);
+            }
+            M[x] = v;
+        }
+        __syncwarp();
+        for (int c0 = 0; c0 < D; c0 += kMC * kWarp) {
+            float z[RMAX][kMC];
+#pragma unroll
+            for (int j = 0; j < RMAX; ++j)
+#pragma unroll
+                for (int m = 0; m < kMC; ++m) {
+                    const int k = c0 + lane + m * kWarp;
+                    z[j][m] = 0.f;
+                    if (j < R && k < D) {
+                        const T* src = (j == 0) ? dense + (int64_t)b * D + k
+                                                : pooled + ((int64_t)b * F + (j - 1)) * D + k;
+                        z[j][m] = ld_elem(src);
+                    }
+                }
+            for (int i = 0; i < R; ++i) {
+                float acc[kMC];
+#pragma unroll
+                for (int m = 0; m < kMC; ++m) acc[m] = 0.f;
+                const float4* mrow = reinterpret_cast<const float4*>(M + i * RS);
+#pragma unroll
+                for (int j4 = 0; j4 < RMAX / 4; ++j4) {
+                    const float4 c = mrow[j4];
+#pragma unroll
+                    for (int m = 0; m < kMC; ++m) {
+                        acc[m] = fmaf(c.x, z[4 * j4 + 0][m], acc[m]);
+                        acc[m] = fmaf(c.y, z[4 * j4 + 1][m], acc[m]);
+                        acc[m] = fmaf(c.z, z[4 * j4 + 2][m], acc[m]);
+                        acc[m] = fmaf(c.w, z[4 * j4 + 3][m], acc[m]);
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < kMC; ++m) {
+                    const int k = c0 + lane + m * kWarp;
+                    if (k < D) {
+                        if (i == 0)
+                            grad_dense[(int64_t)b * D + k] = __ldg(G + k) + acc[m];
+                        else
+                            grad_pooled[((int64_t)b * F + (i - 1)) * D + k] = acc[m];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int RMAX>
+dlrm_status launch(const float* grad_out, const void* dense, const void* pooled, int F, int D, int B, int P,
+                   float* gd, float* gp, cudaStream_t stream)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_bwd_kernel<T, RMAX>, kWarps * kWarp, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    if (blocks > cap) blocks = cap;
+    interact_bwd_kernel<T, RMAX><<<(int)blocks, kWarps * kWarp, 0, stream>>>(
+        grad_out, (const T*)dense, (const T*)pooled, F, D, B, P, gd, gp);
+    return check_launch("interact_bwd_kernel");
+}
+
+template <typename T>
+dlrm_status dispatch(const float* grad_out, const void* dense, const void* pooled, int F, int D, int B, int P,
+                     float* gd, float* gp, cudaStream_t stream)
+{
+    const int R = F + 1;
+    if (R <= 8) return launch<T, 8>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
+    if (R <= 16) return launch<T, 16>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
+    if (R <= 32) return launch<T, 32>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
+    return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: F > 31 is not implemented");
+}
+
+}  // namespace
+}  // namespace dlrm
+
+using namespace dlrm;
+
+extern "C" dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_dense, const void* d_pooled,
+                                         dlrm_dtype dtype, int F, int D, int B, int out_cols,
+                                         float* d_grad_dense, float* d_grad_pooled, void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd: bad dtype");
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd: need F >= 1, D >= 1, B >= 0");
+    const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
+    if (out_cols < W)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd: out_cols %d < D + F(F+1)/2 = %lld", out_cols,
+                    (long long)W);
+    if (!d_grad_out || !d_dense || !d_pooled || !d_grad_dense || !d_grad_pooled)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd: null device pointer");
+    if (((int64_t)D * dtype_size(dtype)) % 16 != 0)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: D*%d bytes must be a multiple of 16",
+                    dtype_size(dtype));
+    if (!aligned16(d_grad_out) || !aligned16(d_dense) || !aligned16(d_pooled) || !aligned16(d_grad_dense) ||
+        !aligned16(d_grad_pooled))
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: pointers must be 16-byte aligned");
+    if (B == 0) return DLRM_OK;
+    cudaStream_t st = as_stream(stream);
+    if (dtype == DLRM_F32)
+        return dispatch<float>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);
+    return dispatch<__half>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);
+}

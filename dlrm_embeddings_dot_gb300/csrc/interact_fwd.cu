@@ -1,0 +1,219 @@
+// interact_fwd.cu -- dot interaction ("DLRM For PyTorch", §Model
+// architecture; --interaction_op cuda_dot): pairwise dot products among the
+// bottom-MLP output and the F pooled embeddings, strict lower triangle in
+// row-major order, concatenated after the dense vector, zero padded.
+//
+// This file holds the CUDA-core (FFMA) kernel, used for fp32 (tensor-core
+// TF32 cannot meet fp32 accuracy) and for fp16 shapes the tensor-core kernel
+// does not take, plus the entry point that picks between the two.
+//
+// FFMA kernel: one warp per sample.  Z = [dense; pooled rows] is staged in
+// shared memory as fp32, rows padded to a multiple of 4 and to 128-byte
+// strides, with the 16-byte chunk index XOR-swizzled by (row / 4) so that the
+// float4 reads of up to 8 row-blocks in one instruction hit distinct banks.
+// Lane l owns 4x4 blocks (I, J), J <= I, of the lower block triangle of Z Z^T
+// and walks k in steps of 4: 8 LDS.128 feed 64 FFMA.  Entries with i > j are
+// staged into a shared output row, which the warp then writes coalesced.
+#include "common.cuh"
+#include "interact_tc.cuh"
+
+namespace dlrm {
+namespace {
+
+constexpr int kMaxWarpsPerBlock = 4;
+
+__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+struct FfmaGeom {
+    int R;        // F + 1 vectors
+    int R4;       // rounded up to 4
+    int ld;       // floats per smem row (multiple of 32)
+    int P;        // out_cols
+    int z_floats; // R4 * ld
+    int warp_floats;
+};
+
+__host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
+{
+    FfmaGeom g;
+    g.R = F + 1;
+    g.R4 = round_up(g.R, 4);
+    g.ld = round_up(D, 32);
+    g.P = P;
+    g.z_floats = g.R4 * g.ld;
+    g.warp_floats = g.z_floats + round_up(P, 4);
+    return g;
+}
+
+// float offset of 16-byte chunk c of row i (XOR swizzle within 128-byte segments)
+__device__ __forceinline__ int zoff(int i, int c, int ld)
+{
+    return i * ld + (((c & ~7) | ((c ^ (i >> 2)) & 7)) << 2);
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_row(float* zs, int i, int ld, const T* src, int D, int lane)
+{
+    if constexpr (sizeof(T) == 4) {
+        for (int c = lane; c < D / 4; c += kWarp) {
+            float4 v = u4_as_f4(ldg_nc_v4(src + 4 * c));
+            *reinterpret_cast<float4*>(zs + zoff(i, c, ld)) = v;
+        }
+    } else {
+        for (int c8 = lane; c8 < D / 8; c8 += kWarp) {
+            float f[8];
+            h8_to_f8(ldg_nc_v4(src + 8 * c8), f);
+            *reinterpret_cast<float4*>(zs + zoff(i, 2 * c8, ld)) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4*>(zs + zoff(i, 2 * c8 + 1, ld)) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ T to_out(float v)
+{
+    if constexpr (sizeof(T) == 4)
+        return v;
+    else
+        return __float2half_rn(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMaxWarpsPerBlock * kWarp)
+interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D,
+                         int B, T* __restrict__ out, int P)
+{
+    extern __shared__ __align__(16) float smem[];
+    const FfmaGeom geo = ffma_geom(F, D, P);
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    float* zs = smem + warp * geo.warp_floats;
+    float* os = zs + geo.z_floats;
+    const int nb = geo.R4 / 4;
+    const int nblocks = nb * (nb + 1) / 2;
+    const int W = D + F * (F + 1) / 2;
+
+    // rows >= R stay zero for the whole kernel
+    for (int x = lane; x < (geo.R4 - geo.R) * geo.ld; x += kWarp) zs[geo.R * geo.ld + x] = 0.f;
+    for (int x = W + lane; x < P; x += kWarp) os[x] = 0.f;
+
+    const int warps_total = gridDim.x * (blockDim.x / kWarp);
+    for (int b = blockIdx.x * (blockDim.x / kWarp) + warp; b < B; b += warps_total) {
+        __syncwarp();
+        stage_row(zs, 0, geo.ld, dense + (int64_t)b * D, D, lane);
+        for (int t = 0; t < F; ++t) stage_row(zs, t + 1, geo.ld, pooled + ((int64_t)b * F + t) * D, D, lane);
+        __syncwarp();
+        // dense block of the output: exact copy of z_0
+        for (int k = lane; k < D; k += kWarp) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];
+        for (int blk = lane; blk < nblocks; blk += kWarp) {
+            int I = 0;
+            while ((I + 1) * (I + 2) / 2 <= blk) ++I;
+            const int J = blk - I * (I + 1) / 2;
+            float acc[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+            for (int c = 0; c < D / 4; ++c) {
+                float4 a[4], bq[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(zs + zoff(4 * I + r, c, geo.ld));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) bq[q] = *reinterpret_cast<const float4*>(zs + zoff(4 * J + q, c, geo.ld));
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[r][q] = fmaf(a[r].x, bq[q].x, acc[r][q]);
+                        acc[r][q] = fmaf(a[r].y, bq[q].y, acc[r][q]);
+                        acc[r][q] = fmaf(a[r].z, bq[q].z, acc[r][q]);
+                        acc[r][q] = fmaf(a[r].w, bq[q].w, acc[r][q]);
+                    }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int i = 4 * I + r, j = 4 * J + q;
+                    if (i < geo.R && j < i) os[D + i * (i - 1) / 2 + j] = acc[r][q];
+                }
+        }
+        __syncwarp();
+        T* orow = out + (int64_t)b * P;
+        for (int x = lane; x < P; x += kWarp) orow[x] = to_out<T>(os[x]);
+    }
+}
+
+template <typename T>
+dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
+                        cudaStream_t stream)
+{
+    const FfmaGeom g = ffma_geom(F, D, P);
+    const size_t per_warp = (size_t)g.warp_floats * sizeof(float);
+    if (per_warp > 200 * 1024)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: (F+1) x D too large for the CUDA-core kernel");
+    int wpb = (int)((200 * 1024) / per_warp);
+    if (wpb > kMaxWarpsPerBlock) wpb = kMaxWarpsPerBlock;
+    const size_t smem = per_warp * wpb;
+    cudaError_t e = cudaFuncSetAttribute(interact_fwd_ffma_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: %s", cudaGetErrorString(e));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_fwd_ffma_kernel<T>, wpb * kWarp, smem);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    int64_t blocks = ((int64_t)B + wpb - 1) / wpb;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    if (blocks > cap) blocks = cap;
+    interact_fwd_ffma_kernel<T><<<(int)blocks, wpb * kWarp, smem, stream>>>(
+        (const T*)dense, (const T*)pooled, F, D, B, (T*)out, P);
+    return check_launch("interact_fwd_ffma_kernel");
+}
+
+}  // namespace
+}  // namespace dlrm
+
+using namespace dlrm;
+
+extern "C" dlrm_status dlrm_interact_fwd(const void* d_dense, const void* d_pooled, dlrm_dtype dtype,
+                                         int F, int D, int B, void* d_out, int out_cols,
+                                         uint32_t* d_status, void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd: bad dtype");
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd: need F >= 1, D >= 1, B >= 0");
+    const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
+    if (out_cols < W)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd: out_cols %d < D + F(F+1)/2 = %lld",
+                    out_cols, (long long)W);
+    if (!d_dense || !d_pooled || !d_out)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd: null device pointer");
+    const int s = dtype_size(dtype);
+    if (((int64_t)D * s) % 16 != 0)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: D*%d bytes must be a multiple of 16", s);
+    if (!aligned16(d_dense) || !aligned16(d_pooled))
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: dense and pooled must be 16-byte aligned");
+    if (B == 0) return DLRM_OK;
+    cudaStream_t st = as_stream(stream);
+    if (dtype == DLRM_F16 && tc_interact_supported(F, D, out_cols, d_dense, d_pooled, d_out))
+        return tc_interact_fwd(d_dense, d_pooled, F, D, B, d_out, out_cols, d_status, st);
+    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+}
+
+// CUDA-core path for any shape, exposed for tests of the tensor-core kernel.
+extern "C" dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const void* d_pooled,
+                                                   dlrm_dtype dtype, int F, int D, int B,
+                                                   void* d_out, int out_cols, void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype) || F < 1 || D < 1 || B < 0 || !d_dense || !d_pooled || !d_out ||
+        out_cols < (int64_t)D + (int64_t)F * (F + 1) / 2)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd_cuda_core: bad arguments");
+    if (((int64_t)D * dtype_size(dtype)) % 16 != 0 || !aligned16(d_dense) || !aligned16(d_pooled))
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd_cuda_core: alignment");
+    if (B == 0) return DLRM_OK;
+    cudaStream_t st = as_stream(stream);
+    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+}

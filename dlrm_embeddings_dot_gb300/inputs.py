@@ -341,3 +341,47 @@ def large_tables_rows(seed: int = 0) -> np.ndarray:
     rows = np.concatenate([np.full(3, 40_000_000, dtype=np.int64),
                            log_uniform_rows(rng, 23, 10, 4e6)])
     return rows
+
+
+class Compact:
+    """The bags of samples ``samples`` of workload ``w`` over a compacted table.
+
+    Compaction only renames rows: the rows the sample touches are regenerated
+    from the seeded generator on the host (never copied from a device) and the
+    sample's indices are renumbered into that smaller table, order preserved
+    within each table, so sums, sort order and updates are unchanged.
+    """
+
+    def __init__(self, w: Workload, samples: np.ndarray, dtype: int | None = None):
+        dt = w.dtype if dtype is None else dtype
+        samples = np.asarray(samples, dtype=np.int64)
+        F, B = w.F, w.B
+        self.samples = samples
+        self.F, self.D, self.B = F, w.D, samples.size
+        rows_per_t, idx_per_bag, counts = [], [], []
+        for t in range(F):
+            bags = t * B + samples
+            s, e = w.offsets[bags], w.offsets[bags + 1]
+            per = [w.indices[a:b].astype(np.int64) for a, b in zip(s, e)]
+            idx_per_bag.append(per)
+            counts.append(e - s)
+            allidx = np.concatenate(per) if per else np.zeros(0, np.int64)
+            rows_per_t.append(np.unique(allidx))
+        self.uniq = rows_per_t                                    # table-local rows, sorted
+        self.rows = np.array([max(len(u), 1) for u in rows_per_t], dtype=np.int64)
+        self.row_base = np.concatenate([[0], np.cumsum(self.rows)]).astype(np.int64)
+        glob_rows = []
+        for t in range(F):
+            u = rows_per_t[t]
+            glob_rows.append(w.row_base[t] + (u if u.size else np.zeros(1, np.int64)))
+        self.global_rows = np.concatenate(glob_rows)
+        self.tables = table_rows(w.table_seed, self.global_rows, w.D, dt)
+        cnt = np.concatenate(counts)                              # feature-major bag sizes
+        self.offsets = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        parts = []
+        for t in range(F):
+            for per in idx_per_bag[t]:
+                parts.append(np.searchsorted(rows_per_t[t], per))
+        self.indices = (np.concatenate(parts) if parts else np.zeros(0, np.int64)).astype(np.int32)
+        self.dense = (w.dense.astype(np.float16) if dt == F16 else w.dense.astype(np.float32))[samples]
+        self.grad_out = None if w.grad_out is None else w.grad_out[samples]

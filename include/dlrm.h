@@ -1,0 +1,188 @@
+/*
+ * dlrm.h -- C ABI of the GB300 (sm_103a) DLRM embedding + dot-interaction
+ * hot path: embedding lookup with sum pooling, dot interaction, interaction
+ * backward, and the sparse embedding gradient fused with the SGD row update.
+ *
+ * The model is the one of the page "DLRM For PyTorch", §Model architecture:
+ * one embedding table per categorical feature; the bottom-MLP output and the
+ * embedding vectors enter the "dot interaction", whose output is concatenated
+ * with the bottom-MLP output and fed to the top MLP.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Names: F = number of tables (categorical features), D = embedding dim
+ *    (= bottom-MLP output width), B = batch, nnz = total number of indices,
+ *    W = D + F(F+1)/2 = meaningful interaction columns, s = element size.
+ *  - Pointers named d_* are DEVICE pointers; h_* are host pointers.  The
+ *    caller allocates and owns every buffer; the library allocates nothing,
+ *    neither device nor pinned memory.  Scratch space is caller-provided.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream).  DLRM_OK means the work was enqueued; there is no
+ *    implicit synchronisation and no host<->device copy.
+ *  - Errors detectable on the host (null pointers, bad sizes, misalignment,
+ *    workspace too small) are returned BEFORE anything is enqueued; nothing is
+ *    written.  The message is in dlrm_last_error() (thread-local).
+ *  - Errors found on the device are reported as bits OR-ed into *d_status
+ *    (a device uint32, may be NULL), read by the caller after synchronising.
+ *    No kernel traps; no kernel reads or writes out of bounds.
+ *  - Inputs must not alias outputs.  Results are bitwise reproducible for
+ *    identical inputs and arguments.
+ *  - Tables are one joint row-major buffer [total_rows][D] (the joint layout of
+ *    --embedding_type joint*); table t owns rows [row_base[t], row_base[t+1]).
+ *  - Index lists are CSR and feature-major: bag (t, b) = indices
+ *    [offsets[t*B + b], offsets[t*B + b + 1]).  offsets has F*B + 1 entries,
+ *    offsets[0] = 0, non-decreasing, offsets[F*B] = nnz (int32).  Monotonicity
+ *    is the caller's contract (checking it would need a device round trip).
+ */
+#ifndef DLRM_GB300_H
+#define DLRM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DLRM_OK = 0,
+    DLRM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, out_cols < W, ... */
+    DLRM_ERR_UNSUPPORTED = 2,   /* a legal request this library does not implement */
+    DLRM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message says which) */
+    DLRM_ERR_WORKSPACE = 4      /* workspace smaller than the size query returned */
+} dlrm_status;
+
+typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
+
+/* flags */
+#define DLRM_FLAG_HASH_INDICES 1u  /* fold every index into its table: idx := ((idx % N_t) + N_t) % N_t
+                                      ("DLRM For PyTorch", §Command-line options, --hash_indices) */
+
+/* bits OR-ed into *d_status by kernels */
+#define DLRM_STATUS_OOB_INDEX 1u   /* an index outside [0, N_t) with hashing off: it was skipped */
+#define DLRM_STATUS_TIMEOUT   2u   /* a bounded on-chip wait gave up; the output is incomplete */
+
+/*
+ * dlrm_emb_fwd -- embedding lookup with sum pooling.
+ * ("DLRM For PyTorch", §Model architecture: one table per categorical feature
+ *  turns each value into a dense vector; §Command-line options:
+ *  --embedding_type joint*, --embedding_dim, --hash_indices.)
+ *
+ *   pooled[b][t][:] = sum_{p in bag(t,b)} tables[row_base[t] + idx'(p)][:]
+ *
+ * with idx'(p) = indices[p] folded by DLRM_FLAG_HASH_INDICES, or, with hashing
+ * off, entries outside [0, N_t) skipped and DLRM_STATUS_OOB_INDEX set.  An
+ * empty bag pools to zero.  Sums are accumulated in fp32 in bag order and
+ * rounded once to `dtype`; a single-index bag is an exact copy of the row.
+ *
+ *   d_tables   [total_rows][D] of dtype, 16-byte aligned
+ *   d_row_base int64 [F+1], row_base[0] = 0, non-decreasing
+ *   d_indices  int32 [nnz];  d_offsets int32 [F*B+1]
+ *   d_pooled   [B][F][D] of dtype, 16-byte aligned (output)
+ * Requires F >= 1, D >= 1, B >= 0, 0 <= nnz < 2^31, D*s % 16 == 0.
+ */
+dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                         int F, int D, int B, const int32_t* d_indices,
+                         const int32_t* d_offsets, int64_t nnz, void* d_pooled,
+                         unsigned flags, uint32_t* d_status, void* stream);
+
+/*
+ * dlrm_interact_fwd -- dot interaction.
+ * ("DLRM For PyTorch", §Model architecture: the bottom-MLP output and the
+ *  embedding vectors enter the dot interaction, whose output is concatenated
+ *  with the bottom-MLP output; --interaction_op cuda_dot.)
+ *
+ * For each sample b, Z = [dense[b]; pooled[b][0]; ...; pooled[b][F-1]]
+ * ((F+1) x D) and
+ *   out[b] = [ dense[b] (D) | z_i . z_j for i = 1..F, j = 0..i-1 (row-major)
+ *              | zeros up to out_cols ]
+ * Dot products accumulate in fp32 and are rounded once to `dtype`.  For fp16
+ * with D % 64 == 0, D <= 256, F <= 32 and 16-byte-aligned rows the products
+ * run on the tcgen05 tensor cores; other shapes use CUDA cores.
+ *
+ *   d_dense  [B][D] of dtype;  d_pooled [B][F][D] of dtype (both 16-byte aligned)
+ *   d_out    [B][out_cols] of dtype (output), out_cols >= W
+ *   d_status may be NULL; gets DLRM_STATUS_TIMEOUT if a bounded wait gave up.
+ * Requires F >= 1, D >= 1, B >= 0, D*s % 16 == 0.
+ */
+dlrm_status dlrm_interact_fwd(const void* d_dense, const void* d_pooled, dlrm_dtype dtype,
+                              int F, int D, int B, void* d_out, int out_cols,
+                              uint32_t* d_status, void* stream);
+
+/*
+ * dlrm_interact_fwd_cuda_core -- the same operation as dlrm_interact_fwd, always
+ * on the CUDA-core (FFMA) kernel, for any shape dlrm_interact_fwd accepts.  It
+ * exists to cross-check and time the tensor-core kernel; d_status is not taken
+ * because this kernel has no waits.
+ */
+dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const void* d_pooled, dlrm_dtype dtype,
+                                        int F, int D, int B, void* d_out, int out_cols,
+                                        void* stream);
+
+/*
+ * dlrm_interact_bwd -- gradient of dlrm_interact_fwd.
+ * With G = grad_out[b][0..W) (pad columns ignored) and M the symmetric
+ * (F+1)x(F+1) matrix M_ij = M_ji = G[D + i(i-1)/2 + j] (i > j), M_ii = 0:
+ *   dZ = M Z;  grad_dense[b] = G[0..D) + dZ_0;  grad_pooled[b][t] = dZ_{t+1}
+ * All arithmetic in fp32 (fp16 inputs are widened exactly).
+ *
+ *   d_grad_out    fp32 [B][out_cols];  d_dense, d_pooled as in the forward
+ *   d_grad_dense  fp32 [B][D] (output);  d_grad_pooled fp32 [B][F][D] (output)
+ * All pointers 16-byte aligned.  Requires out_cols >= W, D*s % 16 == 0.
+ */
+dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_dense,
+                              const void* d_pooled, dlrm_dtype dtype, int F, int D, int B,
+                              int out_cols, float* d_grad_dense, float* d_grad_pooled,
+                              void* stream);
+
+/*
+ * Workspace bytes dlrm_emb_bwd_sgd needs for nnz indices of width D over
+ * total_rows rows.  Returns 0 for invalid sizes.
+ */
+size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
+
+/*
+ * dlrm_emb_bwd_sgd -- sparse embedding gradient fused with the SGD update.
+ * (The gradient of the sum pooling of dlrm_emb_fwd flows unchanged to every
+ *  row of a bag; the tables are FP32 as in "DLRM For PyTorch", §Training
+ *  process; the sparse-gradient joint table is --embedding_type joint_sparse.)
+ *
+ * For every global row r touched by the batch:
+ *   g_r = sum over positions p with row(p) = r of grad_pooled[b(p)][t(p)][:]
+ *   tables[r] := fmaf(-lr, g_r, tables[r])
+ * Rows not touched are left bit-for-bit unchanged; no dense gradient table is
+ * formed.  Deterministic: pairs (row, b*F + t) are stably radix-sorted by
+ * row, then each row's gradients are summed in ascending position order in
+ * fixed chunks of 32 positions whose partial sums are combined in a fixed
+ * order.  Skipped indices (see dlrm_emb_fwd) contribute nothing.
+ *
+ *   d_tables       fp32 [total_rows][D], updated in place, 16-byte aligned
+ *   d_row_base     int64 [F+1] with row_base[F] = total_rows
+ *   total_rows     rows in the joint table, 1 <= total_rows < 2^32 - 1
+ *   d_grad_pooled  fp32 [B][F][D] (from dlrm_interact_bwd), 16-byte aligned
+ *   d_workspace    >= dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows)
+ *                  bytes, 256-byte aligned.  After the stream completes, its
+ *                  first nnz uint32 are the sorted row keys (0xFFFFFFFF for
+ *                  skipped indices, which sort last) and the nnz uint32 that
+ *                  start at byte offset dlrm_ws_align(4*nnz) are the matching
+ *                  grad_pooled row numbers b*F + t.
+ * Requires D % 4 == 0.
+ */
+dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
+                             int F, int D, int B, const int32_t* d_indices,
+                             const int32_t* d_offsets, int64_t nnz,
+                             const float* d_grad_pooled, float lr, void* d_workspace,
+                             size_t workspace_bytes, unsigned flags, uint32_t* d_status,
+                             void* stream);
+
+/* Round a byte count up to the workspace sub-buffer alignment (256 bytes). */
+size_t dlrm_ws_align(size_t bytes);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+const char* dlrm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLRM_GB300_H */

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+declared in include/*.h, and rejects bad arguments before touching the GPU.
+
+No call here reaches a kernel launch: every call either fails validation or
+has nothing to do (empty batch), both of which return before any CUDA call.
+"""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import dlrm_embeddings_dot_gb300 as dl
+from dlrm_embeddings_dot_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAKE = 0x10000          # a 16-byte aligned non-null "device pointer" (never dereferenced)
+FAKE_MIS = 0x10004      # misaligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    libbuild.build()
+    return dl.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(dlrm_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_bwd", "dlrm_emb_bwd_sgd",
+            "dlrm_emb_bwd_sgd_workspace_size", "dlrm_last_error"} <= names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared but not exported"
+
+
+def _err(L):
+    return L.dlrm_last_error().decode()
+
+
+def test_emb_fwd_validation(L):
+    f = L.dlrm_emb_fwd
+    assert f(None, 0, FAKE, 1, 4, 2, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert "null" in _err(L)
+    assert f(FAKE, 0, FAKE, 0, 4, 2, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 1, 4, -1, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 1, 4, 2, FAKE, FAKE, -5, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 1, 4, 2, FAKE, FAKE, 2**31, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 7, FAKE, 1, 4, 2, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 1, 4, 2, FAKE, FAKE, 2, FAKE, 8, None, None) == dl.DLRM_ERR_INVALID_ARG
+    # 3 fp32 = 12 bytes per row: not a multiple of 16
+    assert f(FAKE, 0, FAKE, 1, 3, 2, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE_MIS, 0, FAKE, 1, 4, 2, FAKE, FAKE, 2, FAKE, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 1, 4, 2, FAKE, FAKE, 2, FAKE_MIS, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    # empty batch: nothing to do, returns before any CUDA call
+    assert f(FAKE, 0, FAKE, 3, 4, 0, None, FAKE, 0, FAKE, 0, None, None) == dl.DLRM_OK
+
+
+def test_interact_validation(L):
+    f = L.dlrm_interact_fwd
+    # F=2, D=4: W = 4 + 3 = 7
+    assert f(FAKE, FAKE, 0, 2, 4, 8, FAKE, 6, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert "out_cols" in _err(L)
+    assert f(None, FAKE, 0, 2, 4, 8, FAKE, 7, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 0, 0, 4, 8, FAKE, 7, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 4, 8, FAKE, 7, None, None) == dl.DLRM_ERR_UNSUPPORTED   # 4 halves = 8 B
+    assert f(FAKE_MIS, FAKE, 0, 2, 4, 8, FAKE, 7, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, 0, 2, 4, 0, FAKE, 7, None, None) == dl.DLRM_OK
+    g = L.dlrm_interact_bwd
+    assert g(FAKE, FAKE, FAKE, 0, 2, 4, 8, 6, FAKE, FAKE, None) == dl.DLRM_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, FAKE, 0, 2, 4, 8, 7, None, FAKE, None) == dl.DLRM_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, FAKE, 0, 2, 4, 8, 7, FAKE, FAKE_MIS, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert g(FAKE, FAKE, FAKE, 0, 2, 4, 0, 7, FAKE, FAKE, None) == dl.DLRM_OK
+    h = L.dlrm_interact_fwd_cuda_core
+    assert h(FAKE, FAKE, 0, 2, 4, 8, FAKE, 6, None) == dl.DLRM_ERR_INVALID_ARG
+
+
+def test_sgd_workspace_and_validation(L):
+    ws = L.dlrm_emb_bwd_sgd_workspace_size
+    assert ws(-1, 128, 10) == 0 and ws(10, 3, 10) == 0 and ws(10, 128, 0) == 0
+    assert ws(10, 128, 2**32) == 0
+    a, b = ws(1000, 128, 5000), ws(100000, 128, 5000)
+    assert 0 < a < b and a % 256 == 0
+    assert L.dlrm_ws_align(1) == 256 and L.dlrm_ws_align(256) == 256 and L.dlrm_ws_align(0) == 0
+    f = L.dlrm_emb_bwd_sgd
+    need = ws(100, 16, 50)
+    args = [FAKE, FAKE, 50, 2, 16, 50, FAKE, FAKE, 100, FAKE, ctypes.c_float(0.1), FAKE, need, 0, None, None]
+    bad = list(args); bad[12] = need - 1
+    assert f(*bad) == dl.DLRM_ERR_WORKSPACE
+    assert "workspace" in _err(L)
+    bad = list(args); bad[2] = 0
+    assert f(*bad) == dl.DLRM_ERR_INVALID_ARG
+    bad = list(args); bad[11] = FAKE + 16                 # workspace not 256-byte aligned
+    assert f(*bad) == dl.DLRM_ERR_UNSUPPORTED
+    bad = list(args); bad[4] = 6                          # D % 4 != 0
+    assert f(*bad) == dl.DLRM_ERR_UNSUPPORTED
+    bad = list(args); bad[13] = 4                         # unknown flag
+    assert f(*bad) == dl.DLRM_ERR_INVALID_ARG
+    ok = list(args); ok[8] = 0; ok[6] = None              # nnz = 0: nothing to do
+    assert f(*ok) == dl.DLRM_OK
+
+
+def test_synth_validation(L):
+    f = L.dlrm_synth_fill_uniform
+    assert f(None, 0, 1, 0, 10, -0.05, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, 1, 0, -1, -0.05, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, 1, 0, 0, -0.05, 0.05, None) == dl.DLRM_OK
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        dl.load(str(tmp_path / "nope.so"))
