@@ -237,8 +237,10 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
         if (p < n) {
             const uint32_t d = (key[r] >> shift) & mask;
             const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
-            keys_out[pos] = key[r];
-            vals_out[pos] = val[r];
+            if (pos < n) {   // always true for consistent histograms; guards the write
+                keys_out[pos] = key[r];
+                vals_out[pos] = val[r];
+            }
         }
     }
 }
@@ -247,7 +249,7 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
 template <int MC>
 __global__ void __launch_bounds__(256)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
-               const float* __restrict__ grad, int D, float* __restrict__ tables, float lr,
+               const float* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
                float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
                int64_t nchunks)
 {
@@ -305,6 +307,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
             const bool starts_here = (heads >> s) & 1u;
             const bool ends_here = e < 32 || after != skey;
             if (starts_here && ends_here) {
+                if ((int64_t)skey >= total_rows) continue;   // cannot happen for keys made above
 #pragma unroll
                 for (int m = 0; m < MC; ++m) {
                     const int col = lane + m * kWarp;
@@ -336,7 +339,7 @@ template <int MC>
 __global__ void __launch_bounds__(kFixThreads)
 fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
              const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ split_count, int D,
-             float* __restrict__ tables, float lr)
+             float* __restrict__ tables, int64_t total_rows, float lr)
 {
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
@@ -382,7 +385,7 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
             if (col < c4) reinterpret_cast<float4*>(red + warp * D)[col] = acc[m];
         }
         __syncthreads();
-        if (warp == 0) {
+        if (warp == 0 && (int64_t)K < total_rows) {
 #pragma unroll
             for (int m = 0; m < MC; ++m) {
                 const int col = lane + m * kWarp;
@@ -417,14 +420,15 @@ int key_bits(int64_t total_rows)
 }
 
 template <int MC>
-dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, float* tables, float lr,
-                            cudaStream_t st)
+dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, float* tables,
+                            int64_t total_rows, float lr, cudaStream_t st)
 {
     const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
     int64_t blocks = (nchunks * kWarp + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    segment_kernel<MC><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, lr, w.partials,
+    segment_kernel<MC><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
+                                                    w.partials,
                                                     w.split_list, w.split_count, nchunks);
     dlrm_status s = check_launch("segment_kernel");
     if (s != DLRM_OK) return s;
@@ -435,7 +439,7 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, 
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
     }
     fixup_kernel<MC><<<(int)fblocks, kFixThreads, smem, st>>>(w.keys[0], nnz, w.partials, w.split_list,
-                                                              w.split_count, D, tables, lr);
+                                                              w.split_count, D, tables, total_rows, lr);
     return check_launch("fixup_kernel");
 }
 
@@ -521,8 +525,8 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         cur ^= 1;
     }
     const float* grad = d_grad_pooled;
-    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, lr, st);
-    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, lr, st);
-    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, lr, st);
-    return launch_segments<8>(w, nnz, grad, D, d_tables, lr, st);
+    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, st);
+    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, st);
+    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, st);
+    return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, st);
 }

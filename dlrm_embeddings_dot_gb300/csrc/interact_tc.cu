@@ -322,6 +322,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             const int buf = it & 1;
             const uint32_t bph = (uint32_t)(it >> 1) & 1u;
             if (!mbar_wait(&tfull[buf], bph, abort_flag)) break;
+            __syncwarp();
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(kSlot * q) << 16) + (uint32_t)(buf * kAccStride);
             uint32_t v[32];
@@ -358,6 +359,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
