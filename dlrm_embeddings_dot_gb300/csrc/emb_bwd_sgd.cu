@@ -75,7 +75,7 @@ template <int G>
 __global__ void __launch_bounds__(256)
 keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* __restrict__ indices,
             const int32_t* __restrict__ offsets, bool hash, uint32_t* status, uint32_t* __restrict__ keys,
-            uint32_t* __restrict__ vals, int64_t nbags)
+            uint32_t* __restrict__ vals, int64_t nbags, int64_t nnz)
 {
     const int lane = threadIdx.x % G;
     const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
@@ -85,7 +85,12 @@ keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* _
         const int b = (int)(g - (int64_t)t * B);
         const int64_t base = row_base[t], n = row_base[t + 1] - base;
         const uint32_t val = (uint32_t)((int64_t)b * F + t);
-        const int64_t s = offsets[g], e = offsets[g + 1];
+        int64_t s = offsets[g], e = offsets[g + 1];
+        if (s < 0 || e < s || e > nnz) {   // malformed CSR: clamp, flag, stay in bounds
+            set_status(status, DLRM_STATUS_BAD_OFFSETS);
+            s = s < 0 ? 0 : (s > nnz ? nnz : s);
+            e = e < s ? s : (e > nnz ? nnz : e);
+        }
         for (int64_t p = s + lane; p < e; p += G) {
             int64_t i = indices[p];
             uint32_t key = kSkipKey;
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(256)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
                const float* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
                float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
-               int64_t nchunks)
+               int64_t nchunks, int64_t nbags)
 {
     const int lane = threadIdx.x % kWarp;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
@@ -289,7 +294,8 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                     for (int m = 0; m < MC; ++m) {
                         const int col = lane + m * kWarp;
                         v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (q + u < e && col < c4)
+                        // row < nbags holds for pairs made from well-formed offsets
+                        if (q + u < e && col < c4 && (int64_t)row < nbags)
                             v[u][m] = u4_as_f4(ldg_nc_v4(grad + (int64_t)row * D + 4 * col));
                     }
                 }
@@ -421,15 +427,14 @@ int key_bits(int64_t total_rows)
 
 template <int MC>
 dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, float* tables,
-                            int64_t total_rows, float lr, cudaStream_t st)
+                            int64_t total_rows, float lr, int64_t nbags, cudaStream_t st)
 {
     const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
     int64_t blocks = (nchunks * kWarp + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     segment_kernel<MC><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
-                                                    w.partials,
-                                                    w.split_list, w.split_count, nchunks);
+                                                    w.partials, w.split_list, w.split_count, nchunks, nbags);
     dlrm_status s = check_launch("segment_kernel");
     if (s != DLRM_OK) return s;
     int64_t fblocks = nchunks < (int64_t)num_sms() * 4 ? nchunks : (int64_t)num_sms() * 4;
@@ -503,10 +508,10 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         if (blocks > cap) blocks = cap;
         if (multi)
             keys_kernel<32><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
-                                                         w.keys[cur], w.vals[cur], nbags);
+                                                         w.keys[cur], w.vals[cur], nbags, nnz);
         else
             keys_kernel<1><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
-                                                        w.keys[cur], w.vals[cur], nbags);
+                                                        w.keys[cur], w.vals[cur], nbags, nnz);
         dlrm_status s = check_launch("keys_kernel");
         if (s != DLRM_OK) return s;
     }
@@ -525,8 +530,8 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         cur ^= 1;
     }
     const float* grad = d_grad_pooled;
-    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, st);
-    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, st);
-    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, st);
-    return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, st);
+    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+    return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
 }

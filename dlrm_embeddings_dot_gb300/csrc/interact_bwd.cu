@@ -4,8 +4,9 @@
 // symmetric (F+1)x(F+1) matrix holding G's triangle (zero diagonal),
 //   dZ = M Z,  grad_dense = G[0..D) + dZ_0,  grad_pooled[t] = dZ_{t+1}.
 //
-// One warp per sample.  M is expanded into shared memory (row stride padded
-// to a multiple of 4 so a row is read with broadcast float4 loads); lane l
+// One warp per sample.  G's triangle is fetched with all loads in flight and
+// M is expanded from it into shared memory (row stride padded to a multiple
+// of 4 so a row is read with broadcast float4 loads); lane l
 // owns columns l + 32m of Z, held in registers for all F+1 rows, so each
 // output element is an in-register fp32 FMA chain over j (fixed order).
 // Columns are processed 64 at a time; every global access is a coalesced
@@ -34,22 +35,33 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
     constexpr int RS = RMAX;                     // smem row stride of M (multiple of 4)
+    constexpr int NT = RMAX * (RMAX - 1) / 2;    // largest triangle
     __shared__ __align__(16) float msh[kWarps][RMAX * RS];
+    __shared__ float tsh[kWarps][NT];
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int R = F + 1;
     float* M = msh[warp];
+    float* T_ = tsh[warp];
+    const int ntri = F * (F + 1) / 2;
     const int warps_total = gridDim.x * kWarps;
 
     for (int b = blockIdx.x * kWarps + warp; b < B; b += warps_total) {
         const float* G = grad_out + (int64_t)b * P;
+        __syncwarp();
+        // the upstream triangle, all loads in flight together
+#pragma unroll
+        for (int u = 0; u < (NT + kWarp - 1) / kWarp; ++u) {
+            const int x = u * kWarp + lane;
+            if (x < ntri) T_[x] = __ldg(G + D + x);
+        }
         __syncwarp();
         for (int x = lane; x < RMAX * RS; x += kWarp) {
             const int i = x / RS, j = x % RS;
             float v = 0.f;
             if (i < R && j < R && i != j) {
                 const int hi = i > j ? i : j, lo = i > j ? j : i;
-                v = __ldg(G + D + hi * (hi - 1) / 2 + lo);
+                v = T_[hi * (hi - 1) / 2 + lo];
             }
             M[x] = v;
         }

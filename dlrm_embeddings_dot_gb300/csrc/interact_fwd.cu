@@ -8,9 +8,10 @@
 // does not take, plus the entry point that picks between the two.
 //
 // FFMA kernel: one warp per sample.  Z = [dense; pooled rows] is staged in
-// shared memory as fp32, rows padded to a multiple of 4 and to 128-byte
-// strides, with the 16-byte chunk index XOR-swizzled by (row / 4) so that the
-// float4 reads of up to 8 row-blocks in one instruction hit distinct banks.
+// shared memory as fp32 (all 16-byte chunks of a sample in flight at once),
+// rows padded to a multiple of 4 and to 128-byte strides, with the 16-byte
+// chunk index XOR-swizzled by (row / 4) so that the float4 reads of up to 8
+// row-blocks in one instruction hit distinct banks.
 // Lane l owns 4x4 blocks (I, J), J <= I, of the lower block triangle of Z Z^T
 // and walks k in steps of 4: 8 LDS.128 feed 64 FFMA.  Entries with i > j are
 // staged into a shared output row, which the warp then writes coalesced.
@@ -51,20 +52,59 @@ __device__ __forceinline__ int zoff(int i, int c, int ld)
     return i * ld + (((c & ~7) | ((c ^ (i >> 2)) & 7)) << 2);
 }
 
-template <typename T>
-__device__ __forceinline__ void stage_row(float* zs, int i, int ld, const T* src, int D, int lane)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
 {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Stage Z of sample b (row 0 = dense[b], rows 1..F = pooled[b]) into zs.
+// fp32: every 16-byte chunk is an independent cp.async, so the whole sample is
+// one memory latency.  fp16: chunks are loaded 8 at a time into registers,
+// widened and stored.
+template <typename T>
+__device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restrict__ dense,
+                                             const T* __restrict__ pooled, int64_t b, int F, int D, int lane)
+{
+    constexpr int V = 16 / sizeof(T);          // elements per 16-byte chunk
+    const int cpr = D / V;                      // chunks per row
+    const int total = (F + 1) * cpr;
+    const T* prow = pooled + b * F * D;
     if constexpr (sizeof(T) == 4) {
-        for (int c = lane; c < D / 4; c += kWarp) {
-            float4 v = u4_as_f4(ldg_nc_v4(src + 4 * c));
-            *reinterpret_cast<float4*>(zs + zoff(i, c, ld)) = v;
+        for (int x = lane; x < total; x += kWarp) {
+            const int i = x / cpr, c = x - i * cpr;
+            const float* src = i == 0 ? dense + b * D + 4 * c : prow + (int64_t)(i - 1) * D + 4 * c;
+            cp_async16(zs + zoff(i, c, ld), src);
         }
+        cp_async_wait_all();
     } else {
-        for (int c8 = lane; c8 < D / 8; c8 += kWarp) {
-            float f[8];
-            h8_to_f8(ldg_nc_v4(src + 8 * c8), f);
-            *reinterpret_cast<float4*>(zs + zoff(i, 2 * c8, ld)) = make_float4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<float4*>(zs + zoff(i, 2 * c8 + 1, ld)) = make_float4(f[4], f[5], f[6], f[7]);
+        for (int x0 = 0; x0 < total; x0 += 8 * kWarp) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + u * kWarp + lane;
+                if (x < total) {
+                    const int i = x / cpr, c = x - i * cpr;
+                    const __half* src = i == 0 ? dense + b * D + 8 * c : prow + (int64_t)(i - 1) * D + 8 * c;
+                    v[u] = ldg_nc_v4(src);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + u * kWarp + lane;
+                if (x < total) {
+                    const int i = x / cpr, c = x - i * cpr;
+                    float f[8];
+                    h8_to_f8(v[u], f);
+                    *reinterpret_cast<float4*>(zs + zoff(i, 2 * c, ld)) = make_float4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<float4*>(zs + zoff(i, 2 * c + 1, ld)) = make_float4(f[4], f[5], f[6], f[7]);
+                }
+            }
         }
     }
 }
@@ -100,8 +140,7 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
     const int warps_total = gridDim.x * (blockDim.x / kWarp);
     for (int b = blockIdx.x * (blockDim.x / kWarp) + warp; b < B; b += warps_total) {
         __syncwarp();
-        stage_row(zs, 0, geo.ld, dense + (int64_t)b * D, D, lane);
-        for (int t = 0; t < F; ++t) stage_row(zs, t + 1, geo.ld, pooled + ((int64_t)b * F + t) * D, D, lane);
+        stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, lane);
         __syncwarp();
         // dense block of the output: exact copy of z_0
         for (int k = lane; k < D; k += kWarp) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];

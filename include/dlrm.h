@@ -31,8 +31,11 @@
  *    --embedding_type joint*); table t owns rows [row_base[t], row_base[t+1]).
  *  - Index lists are CSR and feature-major: bag (t, b) = indices
  *    [offsets[t*B + b], offsets[t*B + b + 1]).  offsets has F*B + 1 entries,
- *    offsets[0] = 0, non-decreasing, offsets[F*B] = nnz (int32).  Monotonicity
- *    is the caller's contract (checking it would need a device round trip).
+ *    offsets[0] = 0, non-decreasing, offsets[F*B] = nnz (int32).  This is the
+ *    caller's contract (checking it on the host would need a device round
+ *    trip); kernels clamp every bag into [0, nnz] and flag
+ *    DLRM_STATUS_BAD_OFFSETS, so malformed offsets never cause an access
+ *    outside the buffers.
  */
 #ifndef DLRM_GB300_H
 #define DLRM_GB300_H
@@ -61,6 +64,9 @@ typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
 /* bits OR-ed into *d_status by kernels */
 #define DLRM_STATUS_OOB_INDEX 1u   /* an index outside [0, N_t) with hashing off: it was skipped */
 #define DLRM_STATUS_TIMEOUT   2u   /* a bounded on-chip wait gave up; the output is incomplete */
+#define DLRM_STATUS_BAD_OFFSETS 4u /* an offset outside [0, nnz] or decreasing: the bag was clamped
+                                      into [0, nnz] (results for malformed CSR are unspecified,
+                                      but no access leaves the buffers) */
 
 /*
  * dlrm_emb_fwd -- embedding lookup with sum pooling.

@@ -18,6 +18,8 @@ pytestmark = pytest.mark.gpu
 
 
 def run_lookup(dl, tables, row_base, F, D, B, indices, offsets, flags=0):
+    # only well-formed CSR goes to the device
+    assert offsets[0] == 0 and offsets[-1] == indices.size and (np.diff(offsets) >= 0).all()
     pooled = torch.full((B, F, D), float("nan"), dtype=tables.dtype, device=dev())
     status = torch.zeros(1, dtype=torch.int32, device=dev())
     dl.dlrm_emb_fwd(tables, to_dev(row_base), F, D, B, to_dev(indices.astype(np.int32)),
@@ -108,8 +110,9 @@ def test_hashing_and_out_of_range(cuda_lib):
     assert status == rs == oracle.STATUS_OOB and np.array_equal(got, ref)
     # multi-hot path with some bad entries
     off2 = np.concatenate([[0], np.cumsum(np.full(F * 8, 16))])
-    got, status = run_lookup(cuda_lib, to_dev(tables), row_base, F, D, 8, idx[: off2[-1]], off2)
-    ref, rs = oracle.emb_fwd(tables, row_base, F, D, 8, idx[: off2[-1]], off2)
+    idx2 = rng.integers(-40, 40, size=off2[-1]).astype(np.int32)
+    got, status = run_lookup(cuda_lib, to_dev(tables), row_base, F, D, 8, idx2, off2)
+    ref, rs = oracle.emb_fwd(tables, row_base, F, D, 8, idx2, off2)
     assert status == rs == oracle.STATUS_OOB
     np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5)
 
@@ -120,3 +123,19 @@ def test_empty_index_list(cuda_lib):
     got, status = run_lookup(cuda_lib, tables, np.array([0, 1, 3, 5]), F, D, B, np.zeros(0, np.int32),
                              np.zeros(F * B + 1, np.int64))
     assert status == 0 and not got.any()
+
+
+def test_malformed_offsets_are_clamped_and_flagged(cuda_lib):
+    """Offsets past nnz, negative or decreasing: the kernels clamp every bag
+    into [0, nnz] (no access leaves the index list) and set the status bit."""
+    F, B, D = 2, 4, 16
+    tables = to_dev(np.arange(5 * D, dtype=np.float32).reshape(5, D))
+    row_base = to_dev(np.array([0, 3, 5], dtype=np.int64))
+    idx = to_dev(np.array([0, 1, 2, 0, 1, 1], dtype=np.int32))
+    bad = to_dev(np.array([0, 2, 9, -3, 4, 3, 6, 100, 6], dtype=np.int32))
+    pooled = torch.zeros(B, F, D, device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    cuda_lib.dlrm_emb_fwd(tables, row_base, F, D, B, idx, bad, pooled, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & cuda_lib.DLRM_STATUS_BAD_OFFSETS
+    assert torch.isfinite(pooled).all()

@@ -20,6 +20,8 @@ pytestmark = pytest.mark.gpu
 def run_sgd(dl, tables_np_or_dev, row_base, F, D, B, indices, offsets, grad_pooled, lr, flags=0):
     tab = tables_np_or_dev if isinstance(tables_np_or_dev, torch.Tensor) else to_dev(tables_np_or_dev)
     nnz = indices.size
+    # only well-formed CSR goes to the device
+    assert offsets[0] == 0 and offsets[-1] == nnz and (np.diff(offsets) >= 0).all()
     total_rows = int(row_base[-1])
     wsb = dl.dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev())
@@ -163,3 +165,20 @@ def test_empty(cuda_lib):
     _, status, _, _ = run_sgd(cuda_lib, tab, np.array([0, 4]), 1, 8, 5, np.zeros(0, np.int32),
                               np.zeros(6, np.int64), np.zeros((5, 1, 8), np.float32), 0.1)
     assert status == 0 and torch.equal(tab, torch.ones(4, 8, device=dev()))
+
+
+def test_malformed_offsets_are_clamped_and_flagged(cuda_lib):
+    """Malformed CSR reaches the sparse update: keys are clamped into [0, nnz],
+    grad rows and table rows are range-checked, and the status bit is set."""
+    F, B, D = 2, 4, 16
+    tab = torch.zeros(5, D, device=dev())
+    idx = to_dev(np.array([0, 1, 2, 0, 1, 1], dtype=np.int32))
+    bad = to_dev(np.array([0, 2, 9, -3, 4, 3, 6, 100, 6], dtype=np.int32))
+    ws = torch.zeros(cuda_lib.dlrm_emb_bwd_sgd_workspace_size(6, D, 5), dtype=torch.uint8, device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    gp = torch.ones(B, F, D, device=dev())
+    cuda_lib.dlrm_emb_bwd_sgd(tab, to_dev(np.array([0, 3, 5], dtype=np.int64)), 5, F, D, B, idx, bad, gp, 0.1,
+                              ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & cuda_lib.DLRM_STATUS_BAD_OFFSETS
+    assert torch.isfinite(tab).all()
