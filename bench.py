@@ -391,6 +391,65 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+def run_op(args) -> None:
+    """Run one entry point repeatedly on the DLRM-default shapes (for ncu captures)."""
+    import torch
+
+    import dlrm_embeddings_dot_gb300 as dl
+    from dlrm_embeddings_dot_gb300 import inputs
+
+    dl.load()
+    dev = torch.device("cuda", 0)
+    B, F, D, P = args.batch, 26, 128, 480
+    g = torch.Generator(device=dev).manual_seed(0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.op in ("interact_fwd", "interact_fwd16", "interact_bwd"):
+        dt = torch.float16 if args.op == "interact_fwd16" else torch.float32
+        dense = torch.rand(B, D, generator=g, device=dev).to(dt)
+        pooled = ((torch.rand(B, F, D, generator=g, device=dev) - 0.5) * 0.1).to(dt)
+        out = torch.empty(B, P, dtype=dt, device=dev)
+        go = torch.randn(B, P, generator=g, device=dev) * 1e-2
+        gd = torch.empty(B, D, device=dev)
+        gp = torch.empty(B, F, D, device=dev)
+
+        def once():
+            if args.op == "interact_bwd":
+                dl.dlrm_interact_bwd(go, dense, pooled, F, D, B, P, gd, gp)
+            else:
+                dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status)
+    else:
+        dt = inputs.F16 if args.op == "emb_fwd16" else inputs.F32
+        w = inputs.dlrm_default(B=B, dtype=dt, alpha=ALPHA_FWD if dt == inputs.F16 else ALPHA_TRAIN,
+                                train=True)
+        tt = torch.float16 if dt == inputs.F16 else torch.float32
+        tables = torch.empty(w.total_rows, D, dtype=tt, device=dev)
+        dl.dlrm_synth_fill_uniform(tables, w.table_seed, 0)
+        rb = torch.from_numpy(w.row_base).to(dev)
+        idx = torch.from_numpy(w.indices).to(dev)
+        off = torch.from_numpy(w.offsets).to(dev)
+        pooled = torch.empty(B, F, D, dtype=tt, device=dev)
+        gp = torch.randn(B, F, D, generator=g, device=dev) * 1e-2
+        ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
+                         device=dev)
+
+        def once():
+            if args.op == "emb_bwd_sgd":
+                dl.dlrm_emb_bwd_sgd(tables, rb, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status)
+            else:
+                dl.dlrm_emb_fwd(tables, rb, F, D, B, idx, off, pooled, status=status)
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        once()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"op": args.op, "batch": B, "ms_per_launch": t0.elapsed_time(t1) / args.steps,
+                      "status": int(status.item())}), flush=True)
+
+
 def run_reference(args) -> None:
     """The CPU oracle, timed as it stands, on bounded samples of the same workload."""
     rank, world, _ = dist_env()
@@ -430,10 +489,15 @@ def main(argv=None) -> None:
     ap.add_argument("--ref-samples", type=int, default=512,
                     help="samples per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
+                                     "emb_bwd_sgd"],
+                    help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.op:
+        run_op(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -16,8 +16,9 @@
 //     keys inside its chunk.  A run wholly inside the chunk updates its row
 //     at once (w = fmaf(-lr, g, w)); a run crossing a chunk edge leaves one
 //     partial sum per chunk it touches.
-//  4. fixup: one block per run that crossed a chunk edge adds its partial
-//     sums in a fixed order and updates the row.
+//  4. fixup: one block per run that crossed a chunk edge finds the run's last
+//     chunk (32 chunks per probe), adds its partial sums in a fixed order and
+//     updates the row.
 // Every order of summation is fixed by the data, so results are bitwise
 // reproducible.  Workspace layout (256-byte aligned pieces):
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
@@ -349,24 +350,30 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
 {
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
-    __shared__ int64_t s_end;
+    __shared__ int64_t s_cend;
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const int c4 = D / 4;
     const uint32_t count = *split_count;
     for (uint32_t i = blockIdx.x; i < count; i += gridDim.x) {
         const int64_t c0 = split_list[i];
         const uint32_t K = keys[c0 * kChunk + kChunk - 1];
-        if (threadIdx.x == 0) {   // first position after the run: keys are sorted
-            int64_t lo = c0 * kChunk + kChunk, hi = n;
-            while (lo < hi) {
-                const int64_t mid = lo + (hi - lo) / 2;
-                if (keys[mid] == K) lo = mid + 1;
-                else hi = mid;
+        if (warp == 0) {
+            // Last chunk the run touches: chunks c0+1, c0+2, ... are checked 32 at a
+            // time (keys are sorted, so the run touches chunk c iff its first key is K).
+            int64_t base = c0 + 1;
+            for (;;) {
+                const int64_t c = base + lane;
+                const bool touches = c * kChunk < n && keys[c * kChunk] == K;
+                const uint32_t m = __ballot_sync(0xffffffffu, touches);
+                if (m != 0xffffffffu) {
+                    if (lane == 0) s_cend = base + (__ffs(~m) - 1) - 1;
+                    break;
+                }
+                base += kWarp;
             }
-            s_end = lo;
         }
         __syncthreads();
-        const int64_t c_end = (s_end - 1) / kChunk;
+        const int64_t c_end = s_cend;
         const int64_t pieces = c_end - c0 + 1;
         float4 acc[MC];
 #pragma unroll

@@ -2,15 +2,14 @@
 // §Model architecture: one table per categorical feature; joint table layout
 // of --embedding_type joint*; --hash_indices folds indices into the table).
 //
-// Design: a group of G lanes owns one bag at a time; each lane moves 16-byte
-// chunks of a row (D*s/16 chunks per row), so a row is read with fully
-// coalesced 16-byte loads.  Bags are walked in [b][t] order so that
-// consecutive groups write consecutive pooled rows.
-//  * single-hot kernel (about one index per bag): a group keeps NB = 4 bags in
-//    flight and is software pipelined: the offsets and indices of the next NB
-//    bags are fetched while the current rows are in flight.  A bag of one
-//    valid index is a bit copy of the row (the fp32 round trip of one term is
-//    exact, so this equals the general sum); other bags take the general path.
+// Design: a group of G lanes moves one row; each lane moves 16-byte chunks of
+// it (D*s/16 chunks per row), so a row is read and written with fully
+// coalesced 16-byte accesses.
+//  * single-hot kernel (about one index per bag): a warp resolves 32 bags with
+//    coalesced metadata loads, then keeps 8 row loads per lane in flight.  A
+//    bag of one valid index is a bit copy of the row (the fp32 round trip of
+//    one term is exact, so this equals the general sum); other bags take the
+//    general path.
 //  * multi-hot kernel: one bag per group, U = 4 positions in flight, fp32
 //    accumulation in bag order, one rounding to the table type.
 // Bag bounds are clamped into [0, nnz]; malformed offsets set
@@ -139,33 +138,14 @@ emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ r
     }
 }
 
-// Metadata of one bag for the single-hot kernel: source row (or null) and its
-// index count (-1 = no bag).
-template <typename T>
-__device__ __forceinline__ void single_meta(const T* __restrict__ tables, const int64_t* __restrict__ row_base,
-                                            const int32_t* __restrict__ indices,
-                                            const int32_t* __restrict__ offsets, int F, int D, int B,
-                                            int64_t g, int64_t nbags, int64_t nnz, int lane, bool hash,
-                                            uint32_t* status, const T*& src, int& len)
-{
-    constexpr int V = Vec<T>::n;
-    src = nullptr;
-    len = -1;
-    if (g < nbags) {
-        const int b = (int)(g / F);
-        const int t = (int)(g - (int64_t)b * F);
-        int64_t s, e;
-        bag_bounds(offsets, (int64_t)t * B + b, nnz, status, s, e);
-        len = (int)(e - s);
-        if (len == 1) {
-            const int64_t base = row_base[t];
-            const int64_t r = resolve_row(indices[s], base, row_base[t + 1] - base, hash, status);
-            if (r >= 0) src = tables + r * D + (int64_t)lane * V;
-        }
-    }
-}
-
-template <typename T, int G, int NB>
+// Single-hot kernel.  A warp takes 32 consecutive bags in CSR order (bag
+// g = t*B + b, so the offsets and indices of the 32 bags are read with one
+// coalesced load each), resolves their rows, then moves the rows with
+// RPI = 32/G rows per load instruction and U such instructions in flight per
+// lane.  Writes go to pooled row b*F + t, a full row per group of lanes.
+// Bags that do not hold exactly one index are summed afterwards by the
+// whole warp.
+template <typename T, int G>
 __global__ void __launch_bounds__(kThreads)
 emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ row_base, int F,
                       int D, int B, const int32_t* __restrict__ indices,
@@ -173,48 +153,73 @@ emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ 
                       uint32_t* status, int64_t nbags, int64_t nnz)
 {
     constexpr int V = Vec<T>::n;
-    const int chunks = D / V;       // <= G for this kernel
-    const int lane = threadIdx.x % G;
-    const bool active = lane < chunks;
-    const int64_t group = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / G;
-    const int64_t ngroups = (int64_t)gridDim.x * kThreads / G;
-    const int64_t stride = (int64_t)NB * ngroups;
+    constexpr int RPI = kWarp / G;                // rows per load instruction
+    constexpr int U = 8;                          // load instructions in flight per lane
+    const int chunks = D / V;                     // <= G for this kernel
+    const int lane = threadIdx.x % kWarp;
+    const int sub = lane / G, cl = lane % G;
+    const bool active = cl < chunks;
+    const int64_t warp_id = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kWarp;
+    const int64_t nwarps = (int64_t)gridDim.x * kThreads / kWarp;
 
-    const T* src[NB];
-    int len[NB];
-#pragma unroll
-    for (int k = 0; k < NB; ++k)
-        single_meta(tables, row_base, indices, offsets, F, D, B, group + (int64_t)k * ngroups, nbags, nnz,
-                    lane, hash, status, src[k], len[k]);
-    for (int64_t g0 = group; g0 < nbags; g0 += stride) {
-        uint4 v[NB];
-#pragma unroll
-        for (int k = 0; k < NB; ++k)
-            v[k] = (src[k] && active) ? ldg_nc_v4(src[k]) : make_uint4(0, 0, 0, 0);
-        // next bags' metadata while the rows are in flight
-        const T* nsrc[NB];
-        int nlen[NB];
-#pragma unroll
-        for (int k = 0; k < NB; ++k)
-            single_meta(tables, row_base, indices, offsets, F, D, B, g0 + stride + (int64_t)k * ngroups, nbags,
-                        nnz, lane, hash, status, nsrc[k], nlen[k]);
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            const int64_t g = g0 + (int64_t)k * ngroups;
-            if (len[k] >= 0 && active) {
-                if (len[k] != 1) {                    // empty or multi-index bag: general sum
-                    const int b = (int)(g / F);
-                    const int t = (int)(g - (int64_t)b * F);
-                    int64_t s, e;
-                    bag_bounds(offsets, (int64_t)t * B + b, nnz, status, s, e);
-                    const int64_t base = row_base[t];
-                    v[k] = pool_bag<T, 4>(tables, indices, s, e, base, row_base[t + 1] - base, D, lane, hash,
-                                          status);
-                }
-                *reinterpret_cast<uint4*>(pooled + g * D + (int64_t)lane * V) = v[k];
+    for (int64_t g0 = warp_id * kWarp; g0 < nbags; g0 += nwarps * kWarp) {
+        // ---- metadata of bag g0 + lane
+        const int64_t g = g0 + lane;
+        int len = -1;                             // -1: no bag
+        int64_t row = -1, orow = 0;
+        if (g < nbags) {
+            const int t = (int)(g / B);
+            const int b = (int)(g - (int64_t)t * B);
+            int64_t s, e;
+            bag_bounds(offsets, g, nnz, status, s, e);
+            len = (int)(e - s);
+            orow = (int64_t)b * F + t;
+            if (len == 1) {
+                const int64_t base = row_base[t];
+                row = resolve_row(indices[s], base, row_base[t + 1] - base, hash, status);
             }
-            src[k] = nsrc[k];
-            len[k] = nlen[k];
+        }
+        // ---- rows of bags with at most one index (bit copies; zeros for empty or skipped)
+#pragma unroll
+        for (int k0 = 0; k0 < kWarp; k0 += RPI * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int src_lane = k0 + u * RPI + sub;
+                const int64_t r = __shfl_sync(0xffffffffu, row, src_lane);
+                v[u] = (r >= 0 && active) ? ldg_nc_v4(tables + r * D + (int64_t)cl * V) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int src_lane = k0 + u * RPI + sub;
+                const int l = __shfl_sync(0xffffffffu, len, src_lane);
+                const int64_t o = __shfl_sync(0xffffffffu, orow, src_lane);
+                if (l >= 0 && l <= 1 && active)
+                    *reinterpret_cast<uint4*>(pooled + o * D + (int64_t)cl * V) = v[u];
+            }
+        }
+        // ---- bags with several indices: the whole warp, RPI bags at a time
+        uint32_t multi = __ballot_sync(0xffffffffu, len > 1);
+        while (multi) {
+            int pick[RPI];
+#pragma unroll
+            for (int q = 0; q < RPI; ++q) {
+                pick[q] = multi ? __ffs(multi) - 1 : -1;
+                if (multi) multi &= multi - 1;
+            }
+            const int mine = pick[sub];
+            const int src = mine < 0 ? 0 : mine;
+            const int64_t gg = g0 + src;
+            const int64_t o = __shfl_sync(0xffffffffu, orow, src);
+            if (mine >= 0 && active) {
+                const int t = (int)(gg / B);
+                int64_t s, e;
+                bag_bounds(offsets, gg, nnz, status, s, e);
+                const int64_t base = row_base[t];
+                const uint4 r = pool_bag<T, 4>(tables, indices, s, e, base, row_base[t + 1] - base, D, cl,
+                                               hash, status);
+                *reinterpret_cast<uint4*>(pooled + o * D + (int64_t)cl * V) = r;
+            }
         }
     }
 }
@@ -232,9 +237,8 @@ void launch(const void* tables, const int64_t* row_base, int F, int D, int B,
             const int32_t* indices, const int32_t* offsets, void* pooled, bool hash,
             uint32_t* status, int64_t nbags, int64_t nnz, bool single_hot, cudaStream_t stream)
 {
-    constexpr int NB = 4;
     if (single_hot && D / Vec<T>::n <= G)
-        emb_fwd_single_kernel<T, G, NB><<<(int)grid_for((nbags + NB - 1) / NB, G), kThreads, 0, stream>>>(
+        emb_fwd_single_kernel<T, G><<<(int)grid_for((nbags + kWarp - 1) / kWarp, kWarp), kThreads, 0, stream>>>(
             (const T*)tables, row_base, F, D, B, indices, offsets, (T*)pooled, hash, status, nbags, nnz);
     else
         emb_fwd_multi_kernel<T, G><<<(int)grid_for(nbags, G), kThreads, 0, stream>>>(

@@ -6,26 +6,37 @@
 //
 // One warp per sample.  G's triangle is fetched with all loads in flight and
 // M is expanded from it into shared memory (row stride padded to a multiple
-// of 4 so a row is read with broadcast float4 loads); lane l
-// owns columns l + 32m of Z, held in registers for all F+1 rows, so each
-// output element is an in-register fp32 FMA chain over j (fixed order).
-// Columns are processed 64 at a time; every global access is a coalesced
-// 128-byte row segment.
+// of 4 so a row is read with broadcast float4 loads); lane l owns columns
+// 4l..4l+3 of a 128-column slab of Z, held in registers for all F+1 rows, so
+// each output element is an in-register fp32 FMA chain over j (fixed order).
+// Every global access is a 16-byte vector, 512 contiguous bytes per warp.
 #include "common.cuh"
 
 namespace dlrm {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kMC = 2;   // columns per lane per pass (64-column passes)
 
+// Four consecutive elements of a row as fp32 (fp16 widened exactly).
 template <typename T>
-__device__ __forceinline__ float ld_elem(const T* p)
+__device__ __forceinline__ float4 ld4(const T* p)
 {
-    if constexpr (sizeof(T) == 4)
-        return __ldg(reinterpret_cast<const float*>(p));
-    else
-        return __half2float(*p);
+    if constexpr (sizeof(T) == 4) {
+        return __ldg(reinterpret_cast<const float4*>(p));
+    } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+}
+
+__device__ __forceinline__ void fma4(float4& acc, float c, const float4& z)
+{
+    acc.x = fmaf(c, z.x, acc.x);
+    acc.y = fmaf(c, z.y, acc.y);
+    acc.z = fmaf(c, z.z, acc.z);
+    acc.w = fmaf(c, z.w, acc.w);
 }
 
 template <typename T, int RMAX>
@@ -34,7 +45,7 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     const T* __restrict__ pooled, int F, int D, int B, int P,
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
-    constexpr int RS = RMAX;                     // smem row stride of M (multiple of 4)
+    constexpr int RS = (RMAX + 3) / 4 * 4;       // smem row stride of M (multiple of 4)
     constexpr int NT = RMAX * (RMAX - 1) / 2;    // largest triangle
     __shared__ __align__(16) float msh[kWarps][RMAX * RS];
     __shared__ float tsh[kWarps][NT];
@@ -66,44 +77,37 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
             M[x] = v;
         }
         __syncwarp();
-        for (int c0 = 0; c0 < D; c0 += kMC * kWarp) {
-            float z[RMAX][kMC];
+        for (int c0 = 0; c0 < D; c0 += 4 * kWarp) {
+            const int k = c0 + 4 * lane;              // this lane's 4 columns
+            const bool on = k < D;
+            float4 z[RMAX];
 #pragma unroll
-            for (int j = 0; j < RMAX; ++j)
-#pragma unroll
-                for (int m = 0; m < kMC; ++m) {
-                    const int k = c0 + lane + m * kWarp;
-                    z[j][m] = 0.f;
-                    if (j < R && k < D) {
-                        const T* src = (j == 0) ? dense + (int64_t)b * D + k
-                                                : pooled + ((int64_t)b * F + (j - 1)) * D + k;
-                        z[j][m] = ld_elem(src);
-                    }
-                }
+            for (int j = 0; j < RMAX; ++j) {
+                z[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < R && on)
+                    z[j] = ld4((j == 0) ? dense + (int64_t)b * D + k : pooled + ((int64_t)b * F + (j - 1)) * D + k);
+            }
             for (int i = 0; i < R; ++i) {
-                float acc[kMC];
-#pragma unroll
-                for (int m = 0; m < kMC; ++m) acc[m] = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 const float4* mrow = reinterpret_cast<const float4*>(M + i * RS);
 #pragma unroll
-                for (int j4 = 0; j4 < RMAX / 4; ++j4) {
+                for (int j4 = 0; j4 < RS / 4; ++j4) {
                     const float4 c = mrow[j4];
-#pragma unroll
-                    for (int m = 0; m < kMC; ++m) {
-                        acc[m] = fmaf(c.x, z[4 * j4 + 0][m], acc[m]);
-                        acc[m] = fmaf(c.y, z[4 * j4 + 1][m], acc[m]);
-                        acc[m] = fmaf(c.z, z[4 * j4 + 2][m], acc[m]);
-                        acc[m] = fmaf(c.w, z[4 * j4 + 3][m], acc[m]);
-                    }
+                    if (4 * j4 + 0 < RMAX) fma4(acc, c.x, z[(4 * j4 + 0) % RMAX]);
+                    if (4 * j4 + 1 < RMAX) fma4(acc, c.y, z[(4 * j4 + 1) % RMAX]);
+                    if (4 * j4 + 2 < RMAX) fma4(acc, c.z, z[(4 * j4 + 2) % RMAX]);
+                    if (4 * j4 + 3 < RMAX) fma4(acc, c.w, z[(4 * j4 + 3) % RMAX]);
                 }
-#pragma unroll
-                for (int m = 0; m < kMC; ++m) {
-                    const int k = c0 + lane + m * kWarp;
-                    if (k < D) {
-                        if (i == 0)
-                            grad_dense[(int64_t)b * D + k] = __ldg(G + k) + acc[m];
-                        else
-                            grad_pooled[((int64_t)b * F + (i - 1)) * D + k] = acc[m];
+                if (on) {
+                    if (i == 0) {
+                        // scalar loads: a grad_out row is only 4-byte aligned when out_cols % 4 != 0
+                        acc.x += __ldg(G + k);
+                        acc.y += __ldg(G + k + 1);
+                        acc.z += __ldg(G + k + 2);
+                        acc.w += __ldg(G + k + 3);
+                        *reinterpret_cast<float4*>(grad_dense + (int64_t)b * D + k) = acc;
+                    } else {
+                        *reinterpret_cast<float4*>(grad_pooled + ((int64_t)b * F + (i - 1)) * D + k) = acc;
                     }
                 }
             }
@@ -135,6 +139,7 @@ dlrm_status dispatch(const float* grad_out, const void* dense, const void* poole
     const int R = F + 1;
     if (R <= 8) return launch<T, 8>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
     if (R <= 16) return launch<T, 16>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
+    if (R <= 28) return launch<T, 28>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
     if (R <= 32) return launch<T, 32>(grad_out, dense, pooled, F, D, B, P, gd, gp, stream);
     return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: F > 31 is not implemented");
 }

@@ -21,7 +21,7 @@
 namespace dlrm {
 namespace {
 
-constexpr int kMaxWarpsPerBlock = 4;
+constexpr int kMaxWarpsPerBlock = 2;
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -42,7 +42,7 @@ __host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
     g.ld = round_up(D, 32);
     g.P = P;
     g.z_floats = g.R4 * g.ld;
-    g.warp_floats = g.z_floats + round_up(P, 4);
+    g.warp_floats = 2 * g.z_floats + round_up(P, 4);   // double-buffered Z + output row
     return g;
 }
 
@@ -58,15 +58,16 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most one committed group (the prefetch) is still in flight.
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Stage Z of sample b (row 0 = dense[b], rows 1..F = pooled[b]) into zs.
-// fp32: every 16-byte chunk is an independent cp.async, so the whole sample is
-// one memory latency.  fp16: chunks are loaded 8 at a time into registers,
-// widened and stored.
+// fp32: every 16-byte chunk is an independent cp.async (the caller commits and
+// waits), so a sample is one memory latency and overlaps the previous
+// sample's arithmetic.  fp16: chunks are loaded 8 at a time into registers,
+// widened and stored before returning.
 template <typename T>
 __device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restrict__ dense,
                                              const T* __restrict__ pooled, int64_t b, int F, int D, int lane)
@@ -81,7 +82,6 @@ __device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restr
             const float* src = i == 0 ? dense + b * D + 4 * c : prow + (int64_t)(i - 1) * D + 4 * c;
             cp_async16(zs + zoff(i, c, ld), src);
         }
-        cp_async_wait_all();
     } else {
         for (int x0 = 0; x0 < total; x0 += 8 * kWarp) {
             uint4 v[8];
@@ -127,20 +127,35 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
     const FfmaGeom geo = ffma_geom(F, D, P);
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
-    float* zs = smem + warp * geo.warp_floats;
-    float* os = zs + geo.z_floats;
+    float* zbuf[2] = {smem + warp * geo.warp_floats, smem + warp * geo.warp_floats + geo.z_floats};
+    float* os = zbuf[1] + geo.z_floats;
     const int nb = geo.R4 / 4;
     const int nblocks = nb * (nb + 1) / 2;
     const int W = D + F * (F + 1) / 2;
 
     // rows >= R stay zero for the whole kernel
-    for (int x = lane; x < (geo.R4 - geo.R) * geo.ld; x += kWarp) zs[geo.R * geo.ld + x] = 0.f;
+    for (int x = lane; x < (geo.R4 - geo.R) * geo.ld; x += kWarp) {
+        zbuf[0][geo.R * geo.ld + x] = 0.f;
+        zbuf[1][geo.R * geo.ld + x] = 0.f;
+    }
     for (int x = W + lane; x < P; x += kWarp) os[x] = 0.f;
 
     const int warps_total = gridDim.x * (blockDim.x / kWarp);
-    for (int b = blockIdx.x * (blockDim.x / kWarp) + warp; b < B; b += warps_total) {
+    int b = blockIdx.x * (blockDim.x / kWarp) + warp;
+    if (sizeof(T) == 4 && b < B) stage_sample(zbuf[0], geo.ld, dense, pooled, (int64_t)b, F, D, lane);
+    cp_async_commit();
+    for (int cur = 0; b < B; b += warps_total, cur ^= 1) {
+        float* zs = zbuf[cur];
         __syncwarp();
-        stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, lane);
+        if constexpr (sizeof(T) == 4) {
+            // prefetch the next sample into the other buffer, then wait for this one
+            if (b + warps_total < B)
+                stage_sample(zbuf[cur ^ 1], geo.ld, dense, pooled, (int64_t)(b + warps_total), F, D, lane);
+            cp_async_commit();
+            cp_async_wait_prev();
+        } else {
+            stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, lane);
+        }
         __syncwarp();
         // dense block of the output: exact copy of z_0
         for (int k = lane; k < D; k += kWarp) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];
