@@ -5,7 +5,7 @@
 //   dZ = M Z,  grad_dense = G[0..D) + dZ_0,  grad_pooled[t] = dZ_{t+1}.
 //
 // One warp per sample.  G's triangle is fetched with all loads in flight and
-// M is expanded from it into shared memory (row stride padded to a multiple
+// written straight into both halves of M in shared memory (row stride padded to a multiple
 // of 4 so a row is read with broadcast float4 loads); lane l owns columns
 // 4l..4l+3 of a 128-column slab of Z, held in registers for all F+1 rows, so
 // each output element is an in-register fp32 FMA chain over j (fixed order).
@@ -46,35 +46,27 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
     constexpr int RS = (RMAX + 3) / 4 * 4;       // smem row stride of M (multiple of 4)
-    constexpr int NT = RMAX * (RMAX - 1) / 2;    // largest triangle
     __shared__ __align__(16) float msh[kWarps][RMAX * RS];
-    __shared__ float tsh[kWarps][NT];
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int R = F + 1;
     float* M = msh[warp];
-    float* T_ = tsh[warp];
-    const int ntri = F * (F + 1) / 2;
     const int warps_total = gridDim.x * kWarps;
+
+    // the diagonal and everything outside R x R stay zero for the whole kernel
+    for (int x = lane; x < RMAX * RS; x += kWarp) M[x] = 0.f;
 
     for (int b = blockIdx.x * kWarps + warp; b < B; b += warps_total) {
         const float* G = grad_out + (int64_t)b * P;
         __syncwarp();
-        // the upstream triangle, all loads in flight together
+        // row hi of the triangle goes to M[hi][lo] and M[lo][hi]; all loads in flight together
 #pragma unroll
-        for (int u = 0; u < (NT + kWarp - 1) / kWarp; ++u) {
-            const int x = u * kWarp + lane;
-            if (x < ntri) T_[x] = __ldg(G + D + x);
-        }
-        __syncwarp();
-        for (int x = lane; x < RMAX * RS; x += kWarp) {
-            const int i = x / RS, j = x % RS;
-            float v = 0.f;
-            if (i < R && j < R && i != j) {
-                const int hi = i > j ? i : j, lo = i > j ? j : i;
-                v = T_[hi * (hi - 1) / 2 + lo];
+        for (int hi = 1; hi < RMAX; ++hi) {
+            if (hi < R && lane < hi) {
+                const float v = __ldg(G + D + hi * (hi - 1) / 2 + lane);
+                M[hi * RS + lane] = v;
+                M[lane * RS + hi] = v;
             }
-            M[x] = v;
         }
         __syncwarp();
         for (int c0 = 0; c0 < D; c0 += 4 * kWarp) {

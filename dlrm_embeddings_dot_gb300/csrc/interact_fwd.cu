@@ -7,21 +7,25 @@
 // TF32 cannot meet fp32 accuracy) and for fp16 shapes the tensor-core kernel
 // does not take, plus the entry point that picks between the two.
 //
-// FFMA kernel: one warp per sample.  Z = [dense; pooled rows] is staged in
-// shared memory as fp32 (all 16-byte chunks of a sample in flight at once),
-// rows padded to a multiple of 4 and to 128-byte strides, with the 16-byte
-// chunk index XOR-swizzled by (row / 4) so that the float4 reads of up to 8
-// row-blocks in one instruction hit distinct banks.
-// Lane l owns 4x4 blocks (I, J), J <= I, of the lower block triangle of Z Z^T
-// and walks k in steps of 4: 8 LDS.128 feed 64 FFMA.  Entries with i > j are
-// staged into a shared output row, which the warp then writes coalesced.
+// FFMA kernel: one CTA of 4 warps per sample at a time.  Z = [dense; pooled
+// rows] is staged in shared memory as fp32 (all 16-byte chunks of a sample in
+// flight at once via cp.async), rows padded to a multiple of 4 and to
+// 128-byte strides, with the 16-byte chunk index XOR-swizzled by (row / 4)
+// so that the float4 reads of up to 8 row-blocks in one instruction hit
+// distinct banks.  Lane l owns 4x4 blocks (I, J), J <= I, of the lower block
+// triangle of Z Z^T; warp w covers the 16-byte chunks c = w, w+4, ... of K, so
+// the four warps split K and their partial blocks are added in the fixed
+// order w = 0..3 through shared memory.  A CTA holds one sample (about 23 KB
+// for F = 26, D = 128), so ~9 CTAs (36 warps) share an SM and hide each
+// other's staging latency.
 #include "common.cuh"
 #include "interact_tc.cuh"
 
 namespace dlrm {
 namespace {
 
-constexpr int kMaxWarpsPerBlock = 2;
+constexpr int kSplit = 4;                     // warps per sample (K split)
+constexpr int kFfmaThreads = kSplit * kWarp;
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -29,9 +33,10 @@ struct FfmaGeom {
     int R;        // F + 1 vectors
     int R4;       // rounded up to 4
     int ld;       // floats per smem row (multiple of 32)
-    int P;        // out_cols
+    int nblocks;  // 4x4 blocks of the lower block triangle
     int z_floats; // R4 * ld
-    int warp_floats;
+    int p_floats; // kSplit partial blocks: [kSplit][16][nblocks]
+    int smem_floats;
 };
 
 __host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
@@ -40,9 +45,11 @@ __host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
     g.R = F + 1;
     g.R4 = round_up(g.R, 4);
     g.ld = round_up(D, 32);
-    g.P = P;
+    const int nb = g.R4 / 4;
+    g.nblocks = nb * (nb + 1) / 2;
     g.z_floats = g.R4 * g.ld;
-    g.warp_floats = 2 * g.z_floats + round_up(P, 4);   // double-buffered Z + output row
+    g.p_floats = kSplit * 16 * g.nblocks;
+    g.smem_floats = g.z_floats + g.p_floats + round_up(P, 4);
     return g;
 }
 
@@ -58,36 +65,32 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Wait until at most one committed group (the prefetch) is still in flight.
-__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-// Stage Z of sample b (row 0 = dense[b], rows 1..F = pooled[b]) into zs.
-// fp32: every 16-byte chunk is an independent cp.async (the caller commits and
-// waits), so a sample is one memory latency and overlaps the previous
-// sample's arithmetic.  fp16: chunks are loaded 8 at a time into registers,
-// widened and stored before returning.
+// Stage Z of sample b (row 0 = dense[b], rows 1..F = pooled[b]) into zs with
+// all threads of the CTA.  fp32: independent cp.async per 16-byte chunk;
+// fp16: 16-byte loads widened to fp32 in registers.
 template <typename T>
 __device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restrict__ dense,
-                                             const T* __restrict__ pooled, int64_t b, int F, int D, int lane)
+                                             const T* __restrict__ pooled, int64_t b, int F, int D, int tid)
 {
     constexpr int V = 16 / sizeof(T);          // elements per 16-byte chunk
     const int cpr = D / V;                      // chunks per row
     const int total = (F + 1) * cpr;
     const T* prow = pooled + b * F * D;
     if constexpr (sizeof(T) == 4) {
-        for (int x = lane; x < total; x += kWarp) {
+        for (int x = tid; x < total; x += kFfmaThreads) {
             const int i = x / cpr, c = x - i * cpr;
             const float* src = i == 0 ? dense + b * D + 4 * c : prow + (int64_t)(i - 1) * D + 4 * c;
             cp_async16(zs + zoff(i, c, ld), src);
         }
+        cp_async_wait_all();
     } else {
-        for (int x0 = 0; x0 < total; x0 += 8 * kWarp) {
-            uint4 v[8];
+        for (int x0 = 0; x0 < total; x0 += 4 * kFfmaThreads) {
+            uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int x = x0 + u * kWarp + lane;
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * kFfmaThreads + tid;
                 if (x < total) {
                     const int i = x / cpr, c = x - i * cpr;
                     const __half* src = i == 0 ? dense + b * D + 8 * c : prow + (int64_t)(i - 1) * D + 8 * c;
@@ -95,8 +98,8 @@ __device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restr
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int x = x0 + u * kWarp + lane;
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * kFfmaThreads + tid;
                 if (x < total) {
                     const int i = x / cpr, c = x - i * cpr;
                     float f[8];
@@ -119,47 +122,30 @@ __device__ __forceinline__ T to_out(float v)
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kMaxWarpsPerBlock * kWarp)
+__global__ void __launch_bounds__(kFfmaThreads, 8)
 interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D,
                          int B, T* __restrict__ out, int P)
 {
     extern __shared__ __align__(16) float smem[];
     const FfmaGeom geo = ffma_geom(F, D, P);
-    const int lane = threadIdx.x % kWarp;
-    const int warp = threadIdx.x / kWarp;
-    float* zbuf[2] = {smem + warp * geo.warp_floats, smem + warp * geo.warp_floats + geo.z_floats};
-    float* os = zbuf[1] + geo.z_floats;
-    const int nb = geo.R4 / 4;
-    const int nblocks = nb * (nb + 1) / 2;
+    const int tid = threadIdx.x;
+    const int lane = tid % kWarp;
+    const int warp = tid / kWarp;
+    float* zs = smem;
+    float* part = smem + geo.z_floats;          // [kSplit][16][nblocks]
+    float* os = part + geo.p_floats;
     const int W = D + F * (F + 1) / 2;
+    const int C = D / 4;                        // 16-byte chunks of K
 
-    // rows >= R stay zero for the whole kernel
-    for (int x = lane; x < (geo.R4 - geo.R) * geo.ld; x += kWarp) {
-        zbuf[0][geo.R * geo.ld + x] = 0.f;
-        zbuf[1][geo.R * geo.ld + x] = 0.f;
-    }
-    for (int x = W + lane; x < P; x += kWarp) os[x] = 0.f;
+    // rows >= R and the output padding stay zero for the whole kernel
+    for (int x = tid; x < (geo.R4 - geo.R) * geo.ld; x += kFfmaThreads) zs[geo.R * geo.ld + x] = 0.f;
+    for (int x = W + tid; x < P; x += kFfmaThreads) os[x] = 0.f;
 
-    const int warps_total = gridDim.x * (blockDim.x / kWarp);
-    int b = blockIdx.x * (blockDim.x / kWarp) + warp;
-    if (sizeof(T) == 4 && b < B) stage_sample(zbuf[0], geo.ld, dense, pooled, (int64_t)b, F, D, lane);
-    cp_async_commit();
-    for (int cur = 0; b < B; b += warps_total, cur ^= 1) {
-        float* zs = zbuf[cur];
-        __syncwarp();
-        if constexpr (sizeof(T) == 4) {
-            // prefetch the next sample into the other buffer, then wait for this one
-            if (b + warps_total < B)
-                stage_sample(zbuf[cur ^ 1], geo.ld, dense, pooled, (int64_t)(b + warps_total), F, D, lane);
-            cp_async_commit();
-            cp_async_wait_prev();
-        } else {
-            stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, lane);
-        }
-        __syncwarp();
-        // dense block of the output: exact copy of z_0
-        for (int k = lane; k < D; k += kWarp) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];
-        for (int blk = lane; blk < nblocks; blk += kWarp) {
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, tid);
+        __syncthreads();
+        for (int k = tid; k < D; k += kFfmaThreads) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];
+        for (int blk = lane; blk < geo.nblocks; blk += kWarp) {
             int I = 0;
             while ((I + 1) * (I + 2) / 2 <= blk) ++I;
             const int J = blk - I * (I + 1) / 2;
@@ -168,12 +154,17 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
-            for (int c = 0; c < D / 4; ++c) {
+            const float* arow = zs + 4 * I * geo.ld;
+            const float* brow = zs + 4 * J * geo.ld;
+#pragma unroll 1
+            for (int c = warp; c < C; c += kSplit) {
+                const int ca = (((c & ~7) | ((c ^ I) & 7)) << 2);
+                const int cb = (((c & ~7) | ((c ^ J) & 7)) << 2);
                 float4 a[4], bq[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(zs + zoff(4 * I + r, c, geo.ld));
+                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(arow + r * geo.ld + ca);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) bq[q] = *reinterpret_cast<const float4*>(zs + zoff(4 * J + q, c, geo.ld));
+                for (int q = 0; q < 4; ++q) bq[q] = *reinterpret_cast<const float4*>(brow + q * geo.ld + cb);
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -187,14 +178,26 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = 4 * I + r, j = 4 * J + q;
-                    if (i < geo.R && j < i) os[D + i * (i - 1) / 2 + j] = acc[r][q];
-                }
+                for (int q = 0; q < 4; ++q) part[(warp * 16 + r * 4 + q) * geo.nblocks + blk] = acc[r][q];
         }
-        __syncwarp();
+        __syncthreads();
+        // partial blocks of the four K quarters, added in a fixed order
+        for (int x = tid; x < 16 * geo.nblocks; x += kFfmaThreads) {
+            const int blk = x % geo.nblocks, rq = x / geo.nblocks;
+            int I = 0;
+            while ((I + 1) * (I + 2) / 2 <= blk) ++I;
+            const int J = blk - I * (I + 1) / 2;
+            const int i = 4 * I + (rq >> 2), j = 4 * J + (rq & 3);
+            if (i < geo.R && j < i) {
+                float v = part[rq * geo.nblocks + blk];
+#pragma unroll
+                for (int w = 1; w < kSplit; ++w) v += part[(w * 16 + rq) * geo.nblocks + blk];
+                os[D + i * (i - 1) / 2 + j] = v;
+            }
+        }
+        __syncthreads();
         T* orow = out + (int64_t)b * P;
-        for (int x = lane; x < P; x += kWarp) orow[x] = to_out<T>(os[x]);
+        for (int x = tid; x < P; x += kFfmaThreads) orow[x] = to_out<T>(os[x]);
     }
 }
 
@@ -203,22 +206,19 @@ dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int
                         cudaStream_t stream)
 {
     const FfmaGeom g = ffma_geom(F, D, P);
-    const size_t per_warp = (size_t)g.warp_floats * sizeof(float);
-    if (per_warp > 200 * 1024)
+    const size_t smem = (size_t)g.smem_floats * sizeof(float);
+    if (smem > 200 * 1024)
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: (F+1) x D too large for the CUDA-core kernel");
-    int wpb = (int)((200 * 1024) / per_warp);
-    if (wpb > kMaxWarpsPerBlock) wpb = kMaxWarpsPerBlock;
-    const size_t smem = per_warp * wpb;
     cudaError_t e = cudaFuncSetAttribute(interact_fwd_ffma_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: %s", cudaGetErrorString(e));
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_fwd_ffma_kernel<T>, wpb * kWarp, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_fwd_ffma_kernel<T>, kFfmaThreads, smem);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
-    int64_t blocks = ((int64_t)B + wpb - 1) / wpb;
+    int64_t blocks = B;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    interact_fwd_ffma_kernel<T><<<(int)blocks, wpb * kWarp, smem, stream>>>(
+    interact_fwd_ffma_kernel<T><<<(int)blocks, kFfmaThreads, smem, stream>>>(
         (const T*)dense, (const T*)pooled, F, D, B, (T*)out, P);
     return check_launch("interact_fwd_ffma_kernel");
 }
