@@ -36,7 +36,8 @@ struct FfmaGeom {
     int nblocks;  // 4x4 blocks of the lower block triangle
     int z_floats; // R4 * ld
     int p_floats; // kSplit partial blocks: [kSplit][16][nblocks]
-    int smem_floats;
+    int o_floats; // output row
+    int smem_bytes;
 };
 
 __host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
@@ -49,14 +50,17 @@ __host__ __device__ inline FfmaGeom ffma_geom(int F, int D, int P)
     g.nblocks = nb * (nb + 1) / 2;
     g.z_floats = g.R4 * g.ld;
     g.p_floats = kSplit * 16 * g.nblocks;
-    g.smem_floats = g.z_floats + g.p_floats + round_up(P, 4);
+    g.o_floats = round_up(P, 4);
+    // + one int per partial-slot: the output column it lands in (or -1)
+    g.smem_bytes = 4 * (g.z_floats + g.p_floats + g.o_floats + 16 * g.nblocks);
     return g;
 }
 
-// float offset of 16-byte chunk c of row i (XOR swizzle within 128-byte segments)
+// Float offset of 16-byte chunk c of row i: the low 3 bits of the chunk index
+// are XOR-ed with (row / 4), a permutation within each 128-byte segment.
 __device__ __forceinline__ int zoff(int i, int c, int ld)
 {
-    return i * ld + (((c & ~7) | ((c ^ (i >> 2)) & 7)) << 2);
+    return i * ld + ((c ^ ((i >> 2) & 7)) << 2);
 }
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
@@ -67,49 +71,12 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Stage Z of sample b (row 0 = dense[b], rows 1..F = pooled[b]) into zs with
-// all threads of the CTA.  fp32: independent cp.async per 16-byte chunk;
-// fp16: 16-byte loads widened to fp32 in registers.
-template <typename T>
-__device__ __forceinline__ void stage_sample(float* zs, int ld, const T* __restrict__ dense,
-                                             const T* __restrict__ pooled, int64_t b, int F, int D, int tid)
+// Lower-triangle 4x4 block number -> (I, J), J <= I.
+__device__ __forceinline__ void block_ij(int blk, int& I, int& J)
 {
-    constexpr int V = 16 / sizeof(T);          // elements per 16-byte chunk
-    const int cpr = D / V;                      // chunks per row
-    const int total = (F + 1) * cpr;
-    const T* prow = pooled + b * F * D;
-    if constexpr (sizeof(T) == 4) {
-        for (int x = tid; x < total; x += kFfmaThreads) {
-            const int i = x / cpr, c = x - i * cpr;
-            const float* src = i == 0 ? dense + b * D + 4 * c : prow + (int64_t)(i - 1) * D + 4 * c;
-            cp_async16(zs + zoff(i, c, ld), src);
-        }
-        cp_async_wait_all();
-    } else {
-        for (int x0 = 0; x0 < total; x0 += 4 * kFfmaThreads) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int x = x0 + u * kFfmaThreads + tid;
-                if (x < total) {
-                    const int i = x / cpr, c = x - i * cpr;
-                    const __half* src = i == 0 ? dense + b * D + 8 * c : prow + (int64_t)(i - 1) * D + 8 * c;
-                    v[u] = ldg_nc_v4(src);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int x = x0 + u * kFfmaThreads + tid;
-                if (x < total) {
-                    const int i = x / cpr, c = x - i * cpr;
-                    float f[8];
-                    h8_to_f8(v[u], f);
-                    *reinterpret_cast<float4*>(zs + zoff(i, 2 * c, ld)) = make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4*>(zs + zoff(i, 2 * c + 1, ld)) = make_float4(f[4], f[5], f[6], f[7]);
-                }
-            }
-        }
-    }
+    I = 0;
+    while ((I + 1) * (I + 2) / 2 <= blk) ++I;
+    J = blk - I * (I + 1) / 2;
 }
 
 template <typename T>
@@ -121,78 +88,125 @@ __device__ __forceinline__ T to_out(float v)
         return __float2half_rn(v);
 }
 
-template <typename T>
+// One 4x4 block of Z Z^T over this warp's K chunks (c = warp, warp+4, ...).
+template <int DT>
+__device__ __forceinline__ void block_dot(const float* zs, int ld, int C, int warp, int I, int J, float (&acc)[4][4])
+{
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+    const float* arow = zs + 4 * I * ld;
+    const float* brow = zs + 4 * J * ld;
+    const int I7 = I & 7, J7 = J & 7;
+    constexpr int CT = DT / 4;
+#pragma unroll 1
+    for (int c = warp; c < (DT ? CT : C); c += kSplit) {
+        const float* pa = arow + ((c ^ I7) << 2);
+        const float* pb = brow + ((c ^ J7) << 2);
+        float4 a[4], bq[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(pa + r * ld);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bq[q] = *reinterpret_cast<const float4*>(pb + q * ld);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[r][q] = fmaf(a[r].x, bq[q].x, acc[r][q]);
+                acc[r][q] = fmaf(a[r].y, bq[q].y, acc[r][q]);
+                acc[r][q] = fmaf(a[r].z, bq[q].z, acc[r][q]);
+                acc[r][q] = fmaf(a[r].w, bq[q].w, acc[r][q]);
+            }
+    }
+}
+
+// DT: D as a compile-time constant (0 = taken at run time).
+template <typename T, int DT>
 __global__ void __launch_bounds__(kFfmaThreads, 8)
-interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D,
+interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D_rt,
                          int B, T* __restrict__ out, int P)
 {
     extern __shared__ __align__(16) float smem[];
+    const int D = DT ? DT : D_rt;
     const FfmaGeom geo = ffma_geom(F, D, P);
+    const int ld = DT ? (DT + 31) / 32 * 32 : geo.ld;
     const int tid = threadIdx.x;
     const int lane = tid % kWarp;
     const int warp = tid / kWarp;
     float* zs = smem;
     float* part = smem + geo.z_floats;          // [kSplit][16][nblocks]
     float* os = part + geo.p_floats;
+    int* slot_col = reinterpret_cast<int*>(os + geo.o_floats);
     const int W = D + F * (F + 1) / 2;
-    const int C = D / 4;                        // 16-byte chunks of K
+    const int C = D / 4;                        // 16-byte fp32 chunks of K
+    constexpr int V = 16 / sizeof(T);           // elements per 16-byte global chunk
+    const int cpr = D / V;                      // global chunks per row
 
-    // rows >= R and the output padding stay zero for the whole kernel
-    for (int x = tid; x < (geo.R4 - geo.R) * geo.ld; x += kFfmaThreads) zs[geo.R * geo.ld + x] = 0.f;
+    // ---- once per CTA: zero padding, partial-slot -> output column map
+    for (int x = tid; x < (geo.R4 - geo.R) * ld; x += kFfmaThreads) zs[geo.R * ld + x] = 0.f;
     for (int x = W + tid; x < P; x += kFfmaThreads) os[x] = 0.f;
+    for (int x = tid; x < 16 * geo.nblocks; x += kFfmaThreads) {
+        int I, J;
+        block_ij(x % geo.nblocks, I, J);
+        const int rq = x / geo.nblocks;
+        const int i = 4 * I + (rq >> 2), j = 4 * J + (rq & 3);
+        slot_col[x] = (i < geo.R && j < i) ? D + i * (i - 1) / 2 + j : -1;
+    }
+    int myI = 0, myJ = 0;
+    if (lane < geo.nblocks) block_ij(lane, myI, myJ);
+    // staging: when 128 % cpr == 0 every thread owns one chunk column
+    const bool fixed_col = (kFfmaThreads % cpr) == 0;
+    const int c0 = tid % cpr, i0 = tid / cpr, istep = kFfmaThreads / cpr;
+    __syncthreads();
 
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        stage_sample(zs, geo.ld, dense, pooled, (int64_t)b, F, D, tid);
-        __syncthreads();
-        for (int k = tid; k < D; k += kFfmaThreads) os[k] = zs[zoff(0, k >> 2, geo.ld) + (k & 3)];
-        for (int blk = lane; blk < geo.nblocks; blk += kWarp) {
-            int I = 0;
-            while ((I + 1) * (I + 2) / 2 <= blk) ++I;
-            const int J = blk - I * (I + 1) / 2;
-            float acc[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
-            const float* arow = zs + 4 * I * geo.ld;
-            const float* brow = zs + 4 * J * geo.ld;
-#pragma unroll 1
-            for (int c = warp; c < C; c += kSplit) {
-                const int ca = (((c & ~7) | ((c ^ I) & 7)) << 2);
-                const int cb = (((c & ~7) | ((c ^ J) & 7)) << 2);
-                float4 a[4], bq[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(arow + r * geo.ld + ca);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) bq[q] = *reinterpret_cast<const float4*>(brow + q * geo.ld + cb);
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[r][q] = fmaf(a[r].x, bq[q].x, acc[r][q]);
-                        acc[r][q] = fmaf(a[r].y, bq[q].y, acc[r][q]);
-                        acc[r][q] = fmaf(a[r].z, bq[q].z, acc[r][q]);
-                        acc[r][q] = fmaf(a[r].w, bq[q].w, acc[r][q]);
-                    }
+        const T* drow = dense + (int64_t)b * D;
+        const T* prow = pooled + (int64_t)b * F * D - D;   // row i >= 1 of Z at prow + i*D
+        // ---- stage Z (all chunks of the sample in flight)
+        if constexpr (sizeof(T) == 4) {
+            if (fixed_col) {
+                for (int i = i0; i < geo.R; i += istep)
+                    cp_async16(zs + zoff(i, c0, ld), (i == 0 ? drow : prow + (int64_t)i * D) + 4 * c0);
+            } else {
+                for (int x = tid; x < geo.R * cpr; x += kFfmaThreads) {
+                    const int i = x / cpr, c = x - i * cpr;
+                    cp_async16(zs + zoff(i, c, ld), (i == 0 ? drow : prow + (int64_t)i * D) + 4 * c);
+                }
             }
+            cp_async_wait_all();
+        } else {
+            for (int x = tid; x < geo.R * cpr; x += kFfmaThreads) {
+                const int i = x / cpr, c = x - i * cpr;
+                float f[8];
+                h8_to_f8(ldg_nc_v4((i == 0 ? drow : prow + (int64_t)i * D) + 8 * c), f);
+                *reinterpret_cast<float4*>(zs + zoff(i, 2 * c, ld)) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4*>(zs + zoff(i, 2 * c + 1, ld)) = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+        __syncthreads();
+        for (int k = tid; k < D; k += kFfmaThreads) os[k] = zs[zoff(0, k >> 2, ld) + (k & 3)];
+        // ---- this warp's quarter of K for every 4x4 block
+        for (int blk = lane; blk < geo.nblocks; blk += kWarp) {
+            int I = myI, J = myJ;
+            if (blk != lane) block_ij(blk, I, J);
+            float acc[4][4];
+            block_dot<DT>(zs, ld, C, warp, I, J, acc);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) part[(warp * 16 + r * 4 + q) * geo.nblocks + blk] = acc[r][q];
         }
         __syncthreads();
-        // partial blocks of the four K quarters, added in a fixed order
-        for (int x = tid; x < 16 * geo.nblocks; x += kFfmaThreads) {
-            const int blk = x % geo.nblocks, rq = x / geo.nblocks;
-            int I = 0;
-            while ((I + 1) * (I + 2) / 2 <= blk) ++I;
-            const int J = blk - I * (I + 1) / 2;
-            const int i = 4 * I + (rq >> 2), j = 4 * J + (rq & 3);
-            if (i < geo.R && j < i) {
-                float v = part[rq * geo.nblocks + blk];
+        // ---- the four K quarters, added in a fixed order
+        const int nslot = 16 * geo.nblocks;
+        for (int x = tid; x < nslot; x += kFfmaThreads) {
+            const int col = slot_col[x];
+            if (col >= 0) {
+                float v = part[x];
 #pragma unroll
-                for (int w = 1; w < kSplit; ++w) v += part[(w * 16 + rq) * geo.nblocks + blk];
-                os[D + i * (i - 1) / 2 + j] = v;
+                for (int w = 1; w < kSplit; ++w) v += part[w * nslot + x];
+                os[col] = v;
             }
         }
         __syncthreads();
@@ -201,26 +215,33 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
     }
 }
 
-template <typename T>
-dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
-                        cudaStream_t stream)
+template <typename T, int DT>
+dlrm_status launch_ffma_t(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
+                          cudaStream_t stream)
 {
     const FfmaGeom g = ffma_geom(F, D, P);
-    const size_t smem = (size_t)g.smem_floats * sizeof(float);
+    const size_t smem = (size_t)g.smem_bytes;
     if (smem > 200 * 1024)
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: (F+1) x D too large for the CUDA-core kernel");
-    cudaError_t e = cudaFuncSetAttribute(interact_fwd_ffma_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = interact_fwd_ffma_kernel<T, DT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: %s", cudaGetErrorString(e));
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_fwd_ffma_kernel<T>, kFfmaThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFfmaThreads, smem);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
     int64_t blocks = B;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    interact_fwd_ffma_kernel<T><<<(int)blocks, kFfmaThreads, smem, stream>>>(
-        (const T*)dense, (const T*)pooled, F, D, B, (T*)out, P);
+    kern<<<(int)blocks, kFfmaThreads, smem, stream>>>((const T*)dense, (const T*)pooled, F, D, B, (T*)out, P);
     return check_launch("interact_fwd_ffma_kernel");
+}
+
+template <typename T>
+dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
+                        cudaStream_t stream)
+{
+    if (D == 128) return launch_ffma_t<T, 128>(dense, pooled, F, D, B, out, P, stream);
+    return launch_ffma_t<T, 0>(dense, pooled, F, D, B, out, P, stream);
 }
 
 }  // namespace
