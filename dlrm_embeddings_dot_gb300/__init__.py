@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_emb_bwd_sgd_workspace_size.restype = ctypes.c_size_t
     L.dlrm_emb_bwd_sgd.argtypes = [_P, _P, _I64, _I, _I, _I, _P, _P, _I64, _P, ctypes.c_float, _P,
                                    ctypes.c_size_t, ctypes.c_uint, _P, _P]
+    L.dlrm_emb_bwd_sgd_noalloc.argtypes = [_P, _P, _I64, _I, _I, _I, _P, _P, _I64, _P, ctypes.c_float,
+                                           ctypes.c_uint, _P, _P]
     L.dlrm_ws_align.argtypes = [ctypes.c_size_t]
     L.dlrm_ws_align.restype = ctypes.c_size_t
     L.dlrm_last_error.argtypes = []
@@ -65,7 +67,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_synth_fill_uniform.argtypes = [_P, _I, ctypes.c_uint64, _I64, _I64, ctypes.c_double,
                                           ctypes.c_double, _P]
     for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core",
-              "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_synth_fill_uniform"):
+              "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
         getattr(L, f).restype = _I
     if path is None:
         _lib = L
@@ -150,6 +152,17 @@ def dlrm_emb_bwd_sgd(tables, row_base, total_rows, F, D, B, indices, offsets, gr
                                  _ptr(offsets), indices.numel(), _ptr(grad_pooled), float(lr),
                                  _ptr(workspace), ws_bytes, flags, _ptr(status), _stream(stream))
     _check("dlrm_emb_bwd_sgd", rc)
+
+
+def dlrm_emb_bwd_sgd_noalloc(tables, row_base, total_rows, F, D, B, indices, offsets, grad_pooled, lr,
+                             flags=0, status=None, stream=None):
+    """dlrm_emb_bwd_sgd without a workspace argument, for callers that cannot
+    allocate device memory: the scratch is an array built into the library
+    (calls that overlap on the GPU share it and must be serialised)."""
+    rc = load().dlrm_emb_bwd_sgd_noalloc(_ptr(tables), _ptr(row_base), total_rows, F, D, B, _ptr(indices),
+                                         _ptr(offsets), indices.numel(), _ptr(grad_pooled), float(lr), flags,
+                                         _ptr(status), _stream(stream))
+    _check("dlrm_emb_bwd_sgd_noalloc", rc)
 
 
 def dlrm_synth_fill_uniform(dst, seed, first_elem, lo=-0.05, hi=0.05, stream=None):

@@ -24,6 +24,8 @@
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
 //   partials[2 * nchunks][D] | split_list[nchunks] | counter
 // The sort ends in keysA/valsA, which the caller may read after the call.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dlrm {
@@ -541,4 +543,67 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
     if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
     return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+}
+
+// --------------------------------------------------------------------------
+// Variant of dlrm_emb_bwd_sgd for callers that cannot allocate device memory
+// (for example a plugin invoked from a host framework's execute callback,
+// where the framework owns all device memory and forbids allocation while it
+// runs).  The scratch lives in this file-scope device array instead of a
+// caller-provided workspace.  Every GPU that loads the library holds it until
+// the process exits.
+// --------------------------------------------------------------------------
+namespace dlrm {
+namespace {
+
+constexpr size_t kStaticScratchBytes = DLRM_NOALLOC_SCRATCH_BYTES;
+
+static __device__ __align__(256) unsigned char g_sgd_scratch[kStaticScratchBytes];
+
+// Device address of g_sgd_scratch for the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is queried once
+// per device (with that device current) and cached.
+dlrm_status static_scratch(void** out)
+{
+    static std::mutex mu;
+    static void* cache[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd_noalloc: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd_noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_sgd_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return DLRM_OK;
+}
+
+}  // namespace
+}  // namespace dlrm
+
+extern "C" dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
+                                                int F, int D, int B, const int32_t* d_indices,
+                                                const int32_t* d_offsets, int64_t nnz,
+                                                const float* d_grad_pooled, float lr, unsigned flags,
+                                                uint32_t* d_status, void* stream)
+{
+    clear_error();
+    const size_t need = dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows);
+    if (need == 0 && nnz != 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd_noalloc: invalid nnz, D or total_rows");
+    if (need > dlrm::kStaticScratchBytes)
+        return fail(DLRM_ERR_UNSUPPORTED,
+                    "dlrm_emb_bwd_sgd_noalloc: needs %zu bytes of scratch, the built-in array holds %zu "
+                    "(use dlrm_emb_bwd_sgd with a caller workspace)",
+                    need, dlrm::kStaticScratchBytes);
+    void* scratch = nullptr;
+    dlrm_status s = dlrm::static_scratch(&scratch);
+    if (s != DLRM_OK) return s;
+    return dlrm_emb_bwd_sgd(d_tables, d_row_base, total_rows, F, D, B, d_indices, d_offsets, nnz, d_grad_pooled, lr,
+                            scratch, dlrm::kStaticScratchBytes, flags, d_status, stream);
 }

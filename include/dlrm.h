@@ -181,6 +181,40 @@ dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t
                              size_t workspace_bytes, unsigned flags, uint32_t* d_status,
                              void* stream);
 
+/*
+ * dlrm_emb_bwd_sgd_noalloc -- dlrm_emb_bwd_sgd for callers that cannot
+ * allocate device memory.  (The paper has no counterpart: this is an
+ * interface convenience, not part of the method.)
+ *
+ * Some callers may not call cudaMalloc at all -- for example a plugin run
+ * from a host framework's execute callback, where the framework owns every
+ * byte of device memory and forbids allocation while it runs -- and cannot
+ * hand dlrm_emb_bwd_sgd a workspace either.  This entry point takes the same
+ * arguments minus the workspace and uses a scratch array of
+ * DLRM_NOALLOC_SCRATCH_BYTES built into the library (a file-scope __device__
+ * array; every GPU that loads the library holds it until the process exits).
+ * It allocates nothing and calls no allocating routine.
+ *
+ *  - Sizes whose dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows) exceeds
+ *    DLRM_NOALLOC_SCRATCH_BYTES are rejected with DLRM_ERR_UNSUPPORTED (at
+ *    D = 128 the limit is 344,960 indices; at D = 16, 813,312).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, which keeps the previous call's
+ *    contents (everything that must start at zero is cleared by each call).
+ *    Calls that overlap on the GPU -- on different streams, or from several
+ *    host threads -- race on it and must be serialised by the caller.
+ * Results are identical to dlrm_emb_bwd_sgd; the sorted keys are not
+ * returned.
+ */
+#define DLRM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
+                                     int F, int D, int B, const int32_t* d_indices,
+                                     const int32_t* d_offsets, int64_t nnz,
+                                     const float* d_grad_pooled, float lr, unsigned flags,
+                                     uint32_t* d_status, void* stream);
+
 /* Round a byte count up to the workspace sub-buffer alignment (256 bytes). */
 size_t dlrm_ws_align(size_t bytes);
 
