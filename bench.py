@@ -450,6 +450,124 @@ def run_op(args) -> None:
                       "status": int(status.item())}), flush=True)
 
 
+def _time_ops(torch, stream, ops, steps, warmup):
+    """Per-op mean ms (events around each op) and total ms per step (one event pair)."""
+    for _ in range(warmup):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize()
+    per = {name: 0.0 for name, _ in ops}
+    for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+        ev[0].record(stream)
+        for k, (_, fn) in enumerate(ops):
+            fn()
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        for k, (name, _) in enumerate(ops):
+            per[name] += ev[k].elapsed_time(ev[k + 1])
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        for _, fn in ops:
+            fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return {k: v / steps for k, v in per.items()}, t0.elapsed_time(t1) / steps
+
+
+CONFIGS = {
+    "tiny": "batch 256, 3 fp32 tables x 1000 rows x 16, one uniform index per feature, 22 outputs; forward",
+    "tiny-train": "the tiny slice with Zipf 1.2 indices: forward + interaction backward + sparse SGD (lr 0.1)",
+    "default-fwd": "batch 65536, 26 single-hot fp16 tables (rows log-uniform 10..4e6), D=128, Zipf 1.05, 480 "
+                   "columns; forward (lookup + tcgen05 interaction)",
+    "train-64k": WORKLOAD,
+    "multi-hot": "batch 16384, 26 fp32 tables x 1e6 rows x 128, pooling U{1..100}, Zipf 1.05; forward lookup, "
+                 "then backward + SGD from an N(0,1e-2) grad_pooled",
+    "large-tables": "26 fp16 tables D=128 (three of 40M rows, 23 log-uniform 10..4e6), single-hot Zipf 1.05; "
+                    "forward at batch 1K..1M",
+}
+
+
+def run_config(args, name) -> None:
+    """Measure one workload of the pages' configurations and print a JSON line."""
+    import torch
+
+    import dlrm_embeddings_dot_gb300 as dl
+    from dlrm_embeddings_dot_gb300 import inputs
+
+    dl.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def setup(w, tt):
+        with torch.cuda.stream(stream):
+            tab = torch.empty(w.total_rows, w.D, dtype=tt, device=dev)
+            dl.dlrm_synth_fill_uniform(tab, w.table_seed, 0, stream=stream)
+            rb = torch.from_numpy(w.row_base).to(dev)
+            idx = torch.from_numpy(w.indices).to(dev)
+            off = torch.from_numpy(w.offsets).to(dev)
+        torch.cuda.synchronize()
+        return tab, rb, idx, off
+
+    batches = [args.batch]
+    if name == "large-tables":
+        batches = [1024, 4096, 16384, 65536, 262144, 1048576]
+    for B in batches:
+        if name in ("tiny", "tiny-train"):
+            w = inputs.tiny_slice(seed=0, train=(name == "tiny-train"))
+        elif name == "default-fwd":
+            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD)
+        elif name == "train-64k":
+            w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True)
+        elif name == "multi-hot":
+            w = inputs.multi_hot(B=B if B != BATCH else 16384)
+        else:
+            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, rows=inputs.large_tables_rows())
+        tt = torch.float16 if w.dtype == inputs.F16 else torch.float32
+        es = 2 if tt == torch.float16 else 4
+        F, D, Bw, P = w.F, w.D, w.B, w.out_cols
+        tab, rb, idx, off = setup(w, tt)
+        pooled = torch.empty(Bw, F, D, dtype=tt, device=dev)
+        dense = torch.from_numpy(w.dense.astype(np.float16 if tt == torch.float16 else np.float32)).to(dev)
+        out = torch.empty(Bw, P, dtype=tt, device=dev)
+        ops = [("emb_fwd", lambda: dl.dlrm_emb_fwd(tab, rb, F, D, Bw, idx, off, pooled, status=status,
+                                                   stream=stream))]
+        if name != "multi-hot":
+            ops.append(("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, Bw, out, P,
+                                                                     status=status, stream=stream)))
+        train = name in ("tiny-train", "train-64k", "multi-hot")
+        if train:
+            gp = torch.empty(Bw, F, D, device=dev)
+            ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
+                             device=dev)
+            if name == "multi-hot":
+                gp.normal_(0.0, 1e-2)
+            else:
+                go = torch.from_numpy(w.grad_out).to(dev)
+                gd = torch.empty(Bw, D, device=dev)
+                ops.append(("interact_bwd", lambda: dl.dlrm_interact_bwd(go, dense, pooled, F, D, Bw, P, gd, gp,
+                                                                         stream=stream)))
+            ops.append(("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, Bw, idx, off, gp,
+                                                                   w.lr, ws, status=status, stream=stream)))
+        per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
+        nnz = w.nnz
+        alg = {"emb_fwd": nnz * (4 + D * es) + Bw * F * (4 + D * es),
+               "interact_fwd": Bw * (D * es + F * D * es + P * es),
+               "interact_bwd": Bw * (P * 4 + D * es + F * D * es + D * 4 + F * D * 4),
+               "emb_bwd_sgd": nnz * (4 + 4 + D * 4)}
+        fwd_ms = per["emb_fwd"] + per.get("interact_fwd", 0.0)
+        line = {"config": name, "workload": CONFIGS[name], "batch": Bw, "nnz": nnz, "steps": args.steps,
+                "ms_per_step": round(ms, 4), "ops_ms": {k: round(v, 4) for k, v in per.items()},
+                "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
+                "fwd_samples_per_s": round(Bw / (fwd_ms / 1e3), 1),
+                "step_samples_per_s": round(Bw / (ms / 1e3), 1), "device_status": int(status.item())}
+        print(json.dumps(line), flush=True)
+        del tab, pooled, out, dense
+        torch.cuda.empty_cache()
+
+
 def run_reference(args) -> None:
     """The CPU oracle, timed as it stands, on bounded samples of the same workload."""
     rank, world, _ = dist_env()
@@ -489,13 +607,18 @@ def main(argv=None) -> None:
     ap.add_argument("--ref-samples", type=int, default=512,
                     help="samples per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", choices=sorted(CONFIGS), action="append",
+                    help="measure one of the pages' workloads instead of the headline step (repeatable)")
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
                                      "emb_bwd_sgd"],
                     help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.op:
+    if args.config:
+        for name in args.config:
+            run_config(args, name)
+    elif args.op:
         run_op(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -64,8 +64,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_ws_align.restype = ctypes.c_size_t
     L.dlrm_last_error.argtypes = []
     L.dlrm_last_error.restype = ctypes.c_char_p
-    L.dlrm_synth_fill_uniform.argtypes = [_P, _I, ctypes.c_uint64, _I64, _I64, ctypes.c_double,
-                                          ctypes.c_double, _P]
+    L.dlrm_synth_fill_uniform.argtypes = [_P, _I, ctypes.c_uint64, _I64, _I64, ctypes.c_double, _P]
     for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core",
               "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
         getattr(L, f).restype = _I
@@ -165,7 +164,7 @@ def dlrm_emb_bwd_sgd_noalloc(tables, row_base, total_rows, F, D, B, indices, off
     _check("dlrm_emb_bwd_sgd_noalloc", rc)
 
 
-def dlrm_synth_fill_uniform(dst, seed, first_elem, lo=-0.05, hi=0.05, stream=None):
+def dlrm_synth_fill_uniform(dst, seed, first_elem, amplitude=0.05, stream=None):
     rc = load().dlrm_synth_fill_uniform(_ptr(dst), _dtype_code(dst), seed & (2**64 - 1), first_elem,
-                                        dst.numel(), lo, hi, _stream(stream))
+                                        dst.numel(), amplitude, _stream(stream))
     _check("dlrm_synth_fill_uniform", rc)

@@ -47,15 +47,13 @@ __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t e)
 }
 
 template <typename T>
-__global__ void synth_uniform_kernel(T* dst, uint64_t seed, int64_t first, int64_t count, double lo,
-                                     double width)
+__global__ void synth_uniform_kernel(T* dst, uint64_t seed, int64_t first, int64_t count, float scale)
 {
     int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
-        uint64_t z = splitmix64_at(seed, (uint64_t)(first + i));
-        double u = __dmul_rn((double)(z >> 40) + 0.5, 1.0 / 16777216.0);
-        double v = __dadd_rn(__dmul_rn(u, width), lo);   // two roundings, never fused
-        float f = __double2float_rn(v);
+        const uint64_t z = splitmix64_at(seed, (uint64_t)(first + i));
+        const int x = (int)(z >> 40) - (1 << 23);               // exact in fp32
+        const float f = __fmul_rn((float)x, scale);             // one rounding
         if constexpr (sizeof(T) == 2)
             dst[i] = __float2half_rn(f);
         else
@@ -72,8 +70,8 @@ extern "C" size_t dlrm_ws_align(size_t bytes) { return (bytes + 255) & ~(size_t)
 extern "C" const char* dlrm_last_error(void) { return g_last_error; }
 
 extern "C" dlrm_status dlrm_synth_fill_uniform(void* d_dst, dlrm_dtype dtype, uint64_t seed,
-                                               int64_t first_elem, int64_t count, double lo,
-                                               double hi, void* stream)
+                                               int64_t first_elem, int64_t count, double amplitude,
+                                               void* stream)
 {
     clear_error();
     if (!d_dst) return fail(DLRM_ERR_INVALID_ARG, "dlrm_synth_fill_uniform: d_dst is NULL");
@@ -81,15 +79,15 @@ extern "C" dlrm_status dlrm_synth_fill_uniform(void* d_dst, dlrm_dtype dtype, ui
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_synth_fill_uniform: negative count or first_elem");
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_synth_fill_uniform: bad dtype");
     if (count == 0) return DLRM_OK;
-    double width = hi - lo;
+    const float scale = (float)(amplitude / 8388608.0);
     int threads = 256;
     int64_t want = (count + threads - 1) / threads;
     int blocks = (int)(want < (int64_t)num_sms() * 16 ? want : (int64_t)num_sms() * 16);
     if (dtype == DLRM_F16)
         synth_uniform_kernel<__half><<<blocks, threads, 0, as_stream(stream)>>>(
-            (__half*)d_dst, seed, first_elem, count, lo, width);
+            (__half*)d_dst, seed, first_elem, count, scale);
     else
         synth_uniform_kernel<float><<<blocks, threads, 0, as_stream(stream)>>>(
-            (float*)d_dst, seed, first_elem, count, lo, width);
+            (float*)d_dst, seed, first_elem, count, scale);
     return check_launch("synth_uniform_kernel");
 }

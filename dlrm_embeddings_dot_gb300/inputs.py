@@ -16,8 +16,8 @@ Generators (each written from its published definition):
 
 * ``splitmix64`` (Steele, Lea & Flood, "Fast splittable pseudorandom number
   generators", OOPSLA 2014): element ``e`` of a table gets
-  ``mix(seed + (e + 1) * 0x9E3779B97F4A7C15)``; the top 24 bits give a uniform
-  in (0, 1).  The CUDA library carries its own implementation of the same
+  ``mix(seed + (e + 1) * 0x9E3779B97F4A7C15)``; its top 24 bits give a
+  uniform value on a 2^24-point grid.  The CUDA library carries its own implementation of the same
   generator (``dlrm_synth_fill_uniform``) so that multi-GB tables can be made
   on the device; tests check the two bit for bit.
 * bounded Zipf by rejection-inversion (Hörmann & Derflinger, "Rejection-
@@ -55,31 +55,28 @@ def splitmix64(seed: int, counters: np.ndarray) -> np.ndarray:
     return z
 
 
-def uniform_values(seed: int, elems: np.ndarray, lo: float, hi: float) -> np.ndarray:
-    """fp32 values ``lo + (hi - lo) * u`` for global element numbers ``elems``.
+def uniform_values(seed: int, elems: np.ndarray, amplitude: float) -> np.ndarray:
+    """fp32 values in [-amplitude, amplitude) for global element numbers ``elems``.
 
-    ``u = (top24(z) + 0.5) / 2**24``; the scale and shift are two separately
-    rounded float64 operations (no fused multiply-add), then one rounding to
-    fp32.  The device generator performs exactly these operations.
+    ``x = top24(z) - 2**23`` is a signed 24-bit integer (exact in fp32) and the
+    value is the single fp32 product ``x * c`` with ``c = fp32(amplitude / 2**23)``.
+    The device generator performs exactly these operations.
     """
     z = splitmix64(seed, elems)
-    u24 = (z >> np.uint64(40)).astype(np.float64)
-    x = (u24 + 0.5) * (1.0 / 16777216.0)
-    width = float(hi) - float(lo)
-    v = x * width
-    v = v + float(lo)
-    return v.astype(np.float32)
+    x = ((z >> np.uint64(40)).astype(np.int64) - (1 << 23)).astype(np.float32)
+    c = np.float32(float(amplitude) / 8388608.0)
+    return x * c
 
 
 def table_rows(seed: int, global_rows: np.ndarray, D: int, dtype: int,
-               lo: float = -0.05, hi: float = 0.05) -> np.ndarray:
-    """Rows ``global_rows`` of the joint table, shape ``[len(rows), D]``.
-
-    fp16 tables are the fp32 values rounded once to fp16 (round to nearest even).
+               amplitude: float = 0.05) -> np.ndarray:
+    """Rows ``global_rows`` of the joint table, shape ``[len(rows), D]``, values
+    uniform in [-0.05, 0.05).  fp16 tables are the fp32 values rounded once to
+    fp16 (round to nearest even).
     """
     rows = np.asarray(global_rows, dtype=np.int64)
     elems = (rows[:, None] * D + np.arange(D, dtype=np.int64)[None, :]).astype(np.uint64)
-    v = uniform_values(seed, elems, lo, hi)
+    v = uniform_values(seed, elems, amplitude)
     if dtype == F16:
         return v.astype(np.float16)
     return v

@@ -22,16 +22,16 @@ extern "C" {
  * e = first_elem + i:
  *   z = splitmix64 output number e of the stream seeded with `seed`
  *       (z = mix(seed + (e + 1) * 0x9E3779B97F4A7C15)),
- *   u = ((z >> 40) + 0.5) / 2^24                      (double, exact)
- *   v = u * (hi - lo), then v + lo                    (two rounded double ops, no FMA)
- *   stored as (float)v, or as fp16 of (float)v (round to nearest even).
- * For a joint table [rows][D], element e = row * D + col.
+ *   x = (z >> 40) - 2^23                  (signed 24-bit integer, exact in fp32)
+ *   v = fp32(x) * fp32(amplitude / 2^23)  (one fp32 rounding)
+ * stored as v, or as fp16 of v (round to nearest even); v lies in
+ * [-amplitude, amplitude).  For a joint table [rows][D], e = row * D + col.
  *
  *   d_dst  device buffer of `count` elements of dtype (no alignment needed)
  * Returns DLRM_ERR_INVALID_ARG for a null pointer or count < 0.
  */
 dlrm_status dlrm_synth_fill_uniform(void* d_dst, dlrm_dtype dtype, uint64_t seed,
-                                    int64_t first_elem, int64_t count, double lo, double hi,
+                                    int64_t first_elem, int64_t count, double amplitude,
                                     void* stream);
 
 #ifdef __cplusplus

@@ -112,9 +112,9 @@ def test_sgd_workspace_and_validation(L):
 
 def test_synth_validation(L):
     f = L.dlrm_synth_fill_uniform
-    assert f(None, 0, 1, 0, 10, -0.05, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
-    assert f(FAKE, 0, 1, 0, -1, -0.05, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
-    assert f(FAKE, 0, 1, 0, 0, -0.05, 0.05, None) == dl.DLRM_OK
+    assert f(None, 0, 1, 0, 10, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, 1, 0, -1, 0.05, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, 1, 0, 0, 0.05, None) == dl.DLRM_OK
 
 
 def test_binding_refuses_missing_library(tmp_path):

@@ -27,11 +27,22 @@ def test_splitmix64_matches_integer_definition():
 
 
 def test_uniform_values_range_and_moments():
-    v = inputs.uniform_values(3, np.arange(200000, dtype=np.uint64), -0.05, 0.05)
+    v = inputs.uniform_values(3, np.arange(200000, dtype=np.uint64), 0.05)
     assert v.dtype == np.float32
-    assert v.min() > -0.05 and v.max() < 0.05
+    assert v.min() >= -0.05 and v.max() < 0.05
     assert abs(v.mean()) < 1e-3
     assert v.std() == pytest.approx(0.1 / math.sqrt(12), rel=1e-2)
+
+
+def test_uniform_values_are_single_fp32_products():
+    """x * c with x a 24-bit integer and c = fp32(a / 2^23): one rounding, so the
+    exact product in float64 rounds to the same fp32 value."""
+    e = np.arange(5000, dtype=np.uint64)
+    z = inputs.splitmix64(11, e)
+    x = (z >> np.uint64(40)).astype(np.int64) - (1 << 23)
+    c = np.float32(0.05 / 8388608.0)
+    exact = x.astype(np.float64) * np.float64(c)      # exact: 24-bit x 24-bit < 53 bits
+    assert np.array_equal(inputs.uniform_values(11, e, 0.05), exact.astype(np.float32))
 
 
 def test_table_rows_fp16_is_rounded_fp32():
