@@ -419,8 +419,11 @@ def run_op(args) -> None:
                 dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status)
     else:
         dt = inputs.F16 if args.op == "emb_fwd16" else inputs.F32
+        rows = None
+        if args.small_tables:   # ~10x fewer rows: keeps an ncu capture's device memory to a few hundred MB
+            rows = inputs.log_uniform_rows(np.random.default_rng(np.random.SeedSequence([0, 11])), 26, 10, 4e5)
         w = inputs.dlrm_default(B=B, dtype=dt, alpha=ALPHA_FWD if dt == inputs.F16 else ALPHA_TRAIN,
-                                train=True)
+                                train=True, rows=rows)
         tt = torch.float16 if dt == inputs.F16 else torch.float32
         tables = torch.empty(w.total_rows, D, dtype=tt, device=dev)
         dl.dlrm_synth_fill_uniform(tables, w.table_seed, 0)
@@ -612,6 +615,8 @@ def main(argv=None) -> None:
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
                                      "emb_bwd_sgd"],
                     help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
+    ap.add_argument("--small-tables", action="store_true",
+                    help="with --op: tables with 10x fewer rows (log-uniform in [10, 4e5])")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
