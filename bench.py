@@ -123,23 +123,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def lib_digest() -> str:
+def source_digest(files) -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "dlrm_embeddings_dot_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+    for f in files:
+        with open(os.path.join(ROOT, "dlrm_embeddings_dot_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, digest: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    e = d.get(kernel)
-    if not e or e.get("source_digest") != digest:
+        e = json.load(f).get(kernel)
+    if not e or e.get("source_digest") != source_digest(e.get("source_files", [])):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -352,12 +351,13 @@ def run_ours(args) -> None:
     }
     dom = max(op_ms, key=op_ms.get)
     kernel_names = {"emb_fwd": "emb_fwd_single_kernel", "interact_fwd": "interact_fwd_ffma_kernel",
-                    "interact_bwd": "interact_bwd_kernel", "emb_bwd_sgd": "emb_bwd_sgd (12 kernels)"}
+                    "interact_bwd": "interact_bwd_kernel",
+                    "emb_bwd_sgd": f"emb_bwd_sgd ({kernels_per_step(w.total_rows) - 3} kernels)"}
     achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": ncu_traffic(kernel_names[dom], lib_digest()),
+            "traffic": ncu_traffic(kernel_names[dom]),
             "algorithmic_bytes_per_launch": alg[dom], "launch_ms": round(op_ms[dom], 4)}
 
     line = {
