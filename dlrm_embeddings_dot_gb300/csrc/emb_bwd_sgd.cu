@@ -16,13 +16,15 @@
 //     keys inside its chunk.  A run wholly inside the chunk updates its row
 //     at once (w = fmaf(-lr, g, w)); a run crossing a chunk edge leaves one
 //     partial sum per chunk it touches.
-//  4. fixup: one block per run that crossed a chunk edge finds the run's last
-//     chunk (32 chunks per probe), adds its partial sums in a fixed order and
-//     updates the row.
+//  4. fixup: one warp per run that crossed a chunk edge finds the run's last
+//     chunk (32 chunks per probe), adds its partial sums in chunk order and
+//     updates the row; runs of more than 64 pieces are handed to one block
+//     each (8 warps add interleaved pieces, then the 8 sums in warp order).
 // Every order of summation is fixed by the data, so results are bitwise
 // reproducible.  Workspace layout (256-byte aligned pieces):
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
-//   partials[2 * nchunks][D] | split_list[nchunks] | counter
+//   partials[2 * nchunks][D] | split_list[nchunks] | long_list[nchunks] |
+//   counters
 // The sort ends in keysA/valsA, which the caller may read after the call.
 #include <mutex>
 
@@ -44,7 +46,8 @@ struct Ws {
     uint32_t* totals;
     float* partials;
     uint32_t* split_list;
-    uint32_t* split_count;
+    uint32_t* split_count;   // [0] split runs, [1] long split runs
+    uint32_t* long_list;
     size_t bytes;
 };
 
@@ -68,7 +71,8 @@ Ws carve(void* base, int64_t nnz, int D)
     w.totals = (uint32_t*)take(4 * 256);
     w.partials = (float*)take(4 * 2 * (size_t)nchunks * D);
     w.split_list = (uint32_t*)take(4 * (size_t)nchunks);
-    w.split_count = (uint32_t*)take(4);
+    w.long_list = (uint32_t*)take(4 * (size_t)nchunks);
+    w.split_count = (uint32_t*)take(8);
     w.bytes = off;
     return w;
 }
@@ -154,10 +158,18 @@ radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t 
     h[threadIdx.x] = 0;
     __syncthreads();
     const int64_t base = (int64_t)blockIdx.x * kTile;
+    const uint32_t lt = (1u << (threadIdx.x % kWarp)) - 1u;
+    uint32_t d[kItems];
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
         const int64_t p = base + r * kSortThreads + threadIdx.x;
-        if (p < n) atomicAdd(&h[(keys[p] >> shift) & mask], 1u);
+        d[r] = p < n ? (keys[p] >> shift) & mask : 0x100u;
+    }
+    // Zipf-skewed keys repeat digits: one shared atomic per distinct digit per warp
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, d[r]);
+        if (d[r] < 0x100u && (peers & lt) == 0) atomicAdd(&h[d[r]], (uint32_t)__popc(peers));
     }
     __syncthreads();
     hist[(int64_t)threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
@@ -344,39 +356,117 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
 }
 
 // ----------------------------------------------------------------- 4. fixup
+constexpr int kLongPieces = 64;   // runs with more chunk pieces go to a block-per-run pass
+
+// Last chunk a run that starts in chunk c0 (and continues past it) touches:
+// chunks c0+1, c0+2, ... are probed 32 at a time (keys are sorted, so the run
+// touches chunk c iff the first key of c is K).
+__device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ keys, int64_t n, int64_t c0,
+                                                  uint32_t K, int lane)
+{
+    for (int64_t base = c0 + 1;; base += kWarp) {
+        const int64_t c = base + lane;
+        const bool touches = c * kChunk < n && keys[c * kChunk] == K;
+        const uint32_t m = __ballot_sync(0xffffffffu, touches);
+        if (m != 0xffffffffu) return base + (__ffs(~m) - 1) - 1;
+    }
+}
+
+template <int MC>
+__device__ __forceinline__ void apply_sgd(float* __restrict__ tables, int64_t row, int D, float lr, int lane,
+                                          const float4 (&g)[MC])
+{
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        const int col = lane + m * kWarp;
+        if (col < D / 4) {
+            float4* wp = reinterpret_cast<float4*>(tables + row * D + 4 * col);
+            float4 x = *wp;
+            x.x = fmaf(-lr, g[m].x, x.x);
+            x.y = fmaf(-lr, g[m].y, x.y);
+            x.z = fmaf(-lr, g[m].z, x.z);
+            x.w = fmaf(-lr, g[m].w, x.w);
+            *wp = x;
+        }
+    }
+}
+
+// One warp per split run: pieces (partial sums) added in chunk order.  Runs
+// of more than kLongPieces pieces are appended to a list for fixup_long_kernel.
+template <int MC>
+__global__ void __launch_bounds__(256)
+fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
+             const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ split_count,
+             uint32_t* __restrict__ long_list, uint32_t* __restrict__ long_count, int D,
+             float* __restrict__ tables, int64_t total_rows, float lr)
+{
+    const int lane = threadIdx.x % kWarp;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
+    const int c4 = D / 4;
+    const uint32_t count = *split_count;
+    for (int64_t i = warp_id; i < count; i += nwarps) {
+        const int64_t c0 = split_list[i];
+        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
+        const int64_t pieces = run_last_chunk(keys, n, c0, K, lane) - c0 + 1;
+        if (pieces > kLongPieces) {
+            if (lane == 0) long_list[atomicAdd(long_count, 1u)] = (uint32_t)i;
+            continue;
+        }
+        float4 acc[MC];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t j = 0; j < pieces; j += 4) {
+            float4 v[4][MC];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t slot = (j + u) == 0 ? 2 * c0 + 1 : 2 * (c0 + j + u);
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    const int col = lane + m * kWarp;
+                    v[u][m] = (j + u < pieces && col < c4) ? reinterpret_cast<const float4*>(partials + slot * D)[col]
+                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + u < pieces)
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        acc[m].x += v[u][m].x;
+                        acc[m].y += v[u][m].y;
+                        acc[m].z += v[u][m].z;
+                        acc[m].w += v[u][m].w;
+                    }
+        }
+        if ((int64_t)K < total_rows) apply_sgd<MC>(tables, K, D, lr, lane, acc);
+    }
+}
+
+// One block per long split run: warp w adds pieces w, w+8, ... in order, then
+// warp 0 adds the 8 warp sums in warp order and applies the update.
 template <int MC>
 __global__ void __launch_bounds__(kFixThreads)
-fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
-             const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ split_count, int D,
-             float* __restrict__ tables, int64_t total_rows, float lr)
+fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
+                  const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ long_list,
+                  const uint32_t* __restrict__ long_count, int D, float* __restrict__ tables, int64_t total_rows,
+                  float lr)
 {
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
     __shared__ int64_t s_cend;
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const int c4 = D / 4;
-    const uint32_t count = *split_count;
+    const uint32_t count = *long_count;
     for (uint32_t i = blockIdx.x; i < count; i += gridDim.x) {
-        const int64_t c0 = split_list[i];
+        const int64_t c0 = split_list[long_list[i]];
         const uint32_t K = keys[c0 * kChunk + kChunk - 1];
         if (warp == 0) {
-            // Last chunk the run touches: chunks c0+1, c0+2, ... are checked 32 at a
-            // time (keys are sorted, so the run touches chunk c iff its first key is K).
-            int64_t base = c0 + 1;
-            for (;;) {
-                const int64_t c = base + lane;
-                const bool touches = c * kChunk < n && keys[c * kChunk] == K;
-                const uint32_t m = __ballot_sync(0xffffffffu, touches);
-                if (m != 0xffffffffu) {
-                    if (lane == 0) s_cend = base + (__ffs(~m) - 1) - 1;
-                    break;
-                }
-                base += kWarp;
-            }
+            const int64_t ce = run_last_chunk(keys, n, c0, K, lane);
+            if (lane == 0) s_cend = ce;
         }
         __syncthreads();
-        const int64_t c_end = s_cend;
-        const int64_t pieces = c_end - c0 + 1;
+        const int64_t pieces = s_cend - c0 + 1;
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -400,28 +490,24 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
             if (col < c4) reinterpret_cast<float4*>(red + warp * D)[col] = acc[m];
         }
         __syncthreads();
-        if (warp == 0 && (int64_t)K < total_rows) {
+        if (warp == 0) {
+            float4 g[MC];
 #pragma unroll
             for (int m = 0; m < MC; ++m) {
                 const int col = lane + m * kWarp;
+                g[m] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (col < c4) {
-                    float4 g = reinterpret_cast<const float4*>(red)[col];
+                    g[m] = reinterpret_cast<const float4*>(red)[col];
                     for (int w = 1; w < kW; ++w) {
                         const float4 v = reinterpret_cast<const float4*>(red + w * D)[col];
-                        g.x += v.x;
-                        g.y += v.y;
-                        g.z += v.z;
-                        g.w += v.w;
+                        g[m].x += v.x;
+                        g[m].y += v.y;
+                        g[m].z += v.z;
+                        g[m].w += v.w;
                     }
-                    float4* wp = reinterpret_cast<float4*>(tables + (int64_t)K * D + 4 * col);
-                    float4 x = *wp;
-                    x.x = fmaf(-lr, g.x, x.x);
-                    x.y = fmaf(-lr, g.y, x.y);
-                    x.z = fmaf(-lr, g.z, x.z);
-                    x.w = fmaf(-lr, g.w, x.w);
-                    *wp = x;
                 }
             }
+            if ((int64_t)K < total_rows) apply_sgd<MC>(tables, K, D, lr, lane, g);
         }
         __syncthreads();
     }
@@ -446,15 +532,23 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, 
                                                     w.partials, w.split_list, w.split_count, nchunks, nbags);
     dlrm_status s = check_launch("segment_kernel");
     if (s != DLRM_OK) return s;
-    int64_t fblocks = nchunks < (int64_t)num_sms() * 4 ? nchunks : (int64_t)num_sms() * 4;
+    int64_t fblocks = (nchunks * kWarp + 255) / 256;
+    if (fblocks > cap) fblocks = cap;
+    fixup_kernel<MC><<<(int)fblocks, 256, 0, st>>>(w.keys[0], nnz, w.partials, w.split_list, w.split_count,
+                                                   w.long_list, w.split_count + 1, D, tables, total_rows, lr);
+    s = check_launch("fixup_kernel");
+    if (s != DLRM_OK) return s;
+    const int64_t lblocks = nchunks < (int64_t)num_sms() * 2 ? nchunks : (int64_t)num_sms() * 2;
     const size_t smem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(fixup_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(fixup_long_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
     }
-    fixup_kernel<MC><<<(int)fblocks, kFixThreads, smem, st>>>(w.keys[0], nnz, w.partials, w.split_list,
-                                                              w.split_count, D, tables, total_rows, lr);
-    return check_launch("fixup_kernel");
+    fixup_long_kernel<MC><<<(int)lblocks, kFixThreads, smem, st>>>(w.keys[0], nnz, w.partials, w.split_list,
+                                                                   w.long_list, w.split_count + 1, D, tables,
+                                                                   total_rows, lr);
+    return check_launch("fixup_long_kernel");
 }
 
 }  // namespace
@@ -504,7 +598,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     const int nbits = key_bits(total_rows);
     const int npasses = (nbits + 7) / 8;
     int cur = npasses & 1;   // the last pass lands in buffer 0
-    cudaError_t ce = cudaMemsetAsync(w.split_count, 0, sizeof(uint32_t), st);
+    cudaError_t ce = cudaMemsetAsync(w.split_count, 0, 2 * sizeof(uint32_t), st);
     if (ce != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(ce));
 
     const int64_t nbags = (int64_t)F * B;
