@@ -4,12 +4,15 @@
 // symmetric (F+1)x(F+1) matrix holding G's triangle (zero diagonal),
 //   dZ = M Z,  grad_dense = G[0..D) + dZ_0,  grad_pooled[t] = dZ_{t+1}.
 //
-// One warp per sample.  G's triangle is fetched with all loads in flight and
-// written straight into both halves of M in shared memory (row stride padded to a multiple
-// of 4 so a row is read with broadcast float4 loads); lane l owns columns
-// 4l..4l+3 of a 128-column slab of Z, held in registers for all F+1 rows, so
-// each output element is an in-register fp32 FMA chain over j (fixed order).
-// Every global access is a 16-byte vector, 512 contiguous bytes per warp.
+// One warp per sample.  The sample's Z and upstream gradient row are staged
+// in shared memory with cp.async, and the next sample's copy is issued as soon
+// as the current one has been read into registers, so the loads run behind
+// the arithmetic.  G's triangle is written into both halves of M (row stride
+// padded to a multiple of 4 so a row is read with broadcast float4 loads);
+// lane l owns columns 4l..4l+3 of a 128-column slab of Z, held in registers
+// for all F+1 rows, so each output element is an in-register fp32 FMA chain
+// over j (fixed order).  Outputs are 16-byte stores, 512 contiguous bytes per
+// warp.
 #include "common.cuh"
 
 namespace dlrm {
@@ -17,14 +20,29 @@ namespace {
 
 constexpr int kWarps = 4;
 
-// Four consecutive elements of a row as fp32 (fp16 widened exactly).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Four consecutive elements of a staged row as fp32 (fp16 widened exactly).
 template <typename T>
-__device__ __forceinline__ float4 ld4(const T* p)
+__device__ __forceinline__ float4 lds4(const T* p)
 {
     if constexpr (sizeof(T) == 4) {
-        return __ldg(reinterpret_cast<const float4*>(p));
+        return *reinterpret_cast<const float4*>(p);
     } else {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
         const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
         return make_float4(a.x, a.y, b.x, b.y);
@@ -39,6 +57,37 @@ __device__ __forceinline__ void fma4(float4& acc, float c, const float4& z)
     acc.w = fmaf(c, z.w, acc.w);
 }
 
+struct BwdSmem {
+    int z_bytes, g_floats, m_floats, warp_bytes;
+};
+
+template <int RMAX>
+__host__ __device__ inline BwdSmem bwd_smem(int F, int D, int P, int es)
+{
+    BwdSmem m;
+    m.z_bytes = ((F + 1) * D * es + 15) / 16 * 16;
+    m.g_floats = (P + 3) / 4 * 4;
+    m.m_floats = RMAX * ((RMAX + 3) / 4 * 4);
+    m.warp_bytes = m.z_bytes + 4 * (m.g_floats + m.m_floats);
+    return m;
+}
+
+// Copy sample b's Z (dense row, then the F pooled rows) and its upstream
+// gradient row into this warp's staging area, all asynchronously.
+template <typename T>
+__device__ __forceinline__ void stage_bwd(unsigned char* zs, float* gs, const float* __restrict__ grad_out,
+                                          const T* __restrict__ dense, const T* __restrict__ pooled, int64_t b,
+                                          int F, int D, int P, int lane)
+{
+    const int dchunks = D * (int)sizeof(T) / 16;             // 16-byte chunks of one row
+    const unsigned char* drow = reinterpret_cast<const unsigned char*>(dense + b * D);
+    const unsigned char* prow = reinterpret_cast<const unsigned char*>(pooled + b * F * D);
+    for (int x = lane; x < dchunks; x += kWarp) cp_async16(zs + 16 * x, drow + 16 * x);
+    for (int x = lane; x < F * dchunks; x += kWarp) cp_async16(zs + 16 * (dchunks + x), prow + 16 * x);
+    const float* G = grad_out + b * P;
+    for (int x = lane; x < P; x += kWarp) cp_async4(gs + x, G + x);   // rows are only 4-byte aligned in general
+}
+
 template <typename T, int RMAX>
 __global__ void __launch_bounds__(kWarps * kWarp)
 interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ dense,
@@ -46,29 +95,34 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
     constexpr int RS = (RMAX + 3) / 4 * 4;       // smem row stride of M (multiple of 4)
-    __shared__ __align__(16) float msh[kWarps][RMAX * RS];
+    extern __shared__ __align__(16) unsigned char bwd_smem_raw[];
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int R = F + 1;
-    float* M = msh[warp];
+    const BwdSmem L = bwd_smem<RMAX>(F, D, P, (int)sizeof(T));
+    unsigned char* zs = bwd_smem_raw + (size_t)warp * L.warp_bytes;
+    float* gs = reinterpret_cast<float*>(zs + L.z_bytes);
+    float* M = gs + L.g_floats;
     const int warps_total = gridDim.x * kWarps;
 
     // the diagonal and everything outside R x R stay zero for the whole kernel
     for (int x = lane; x < RMAX * RS; x += kWarp) M[x] = 0.f;
 
-    for (int b = blockIdx.x * kWarps + warp; b < B; b += warps_total) {
-        const float* G = grad_out + (int64_t)b * P;
+    int b = blockIdx.x * kWarps + warp;
+    if (b < B) stage_bwd(zs, gs, grad_out, dense, pooled, (int64_t)b, F, D, P, lane);
+    cp_async_commit();
+    for (; b < B; b += warps_total) {
+        cp_async_wait_all();
         __syncwarp();
-        // row hi of the triangle goes to M[hi][lo] and M[lo][hi]; all loads in flight together
+        // row hi of the upstream triangle goes to M[hi][lo] and M[lo][hi]
 #pragma unroll
         for (int hi = 1; hi < RMAX; ++hi) {
             if (hi < R && lane < hi) {
-                const float v = __ldg(G + D + hi * (hi - 1) / 2 + lane);
+                const float v = gs[D + hi * (hi - 1) / 2 + lane];
                 M[hi * RS + lane] = v;
                 M[lane * RS + hi] = v;
             }
         }
-        __syncwarp();
         for (int c0 = 0; c0 < D; c0 += 4 * kWarp) {
             const int k = c0 + 4 * lane;              // this lane's 4 columns
             const bool on = k < D;
@@ -76,8 +130,16 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
 #pragma unroll
             for (int j = 0; j < RMAX; ++j) {
                 z[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < R && on)
-                    z[j] = ld4((j == 0) ? dense + (int64_t)b * D + k : pooled + ((int64_t)b * F + (j - 1)) * D + k);
+                if (j < R && on) z[j] = lds4(reinterpret_cast<const T*>(zs) + (int64_t)j * D + k);
+            }
+            float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (on) g0 = make_float4(gs[k], gs[k + 1], gs[k + 2], gs[k + 3]);
+            __syncwarp();
+            if (c0 + 4 * kWarp >= D) {
+                // this sample's staging area has been read: fetch the next sample behind the arithmetic
+                if (b + warps_total < B)
+                    stage_bwd(zs, gs, grad_out, dense, pooled, (int64_t)(b + warps_total), F, D, P, lane);
+                cp_async_commit();
             }
             for (int i = 0; i < R; ++i) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -92,11 +154,10 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                 }
                 if (on) {
                     if (i == 0) {
-                        // scalar loads: a grad_out row is only 4-byte aligned when out_cols % 4 != 0
-                        acc.x += __ldg(G + k);
-                        acc.y += __ldg(G + k + 1);
-                        acc.z += __ldg(G + k + 2);
-                        acc.w += __ldg(G + k + 3);
+                        acc.x += g0.x;
+                        acc.y += g0.y;
+                        acc.z += g0.z;
+                        acc.w += g0.w;
                         *reinterpret_cast<float4*>(grad_dense + (int64_t)b * D + k) = acc;
                     } else {
                         *reinterpret_cast<float4*>(grad_pooled + ((int64_t)b * F + (i - 1)) * D + k) = acc;
@@ -104,6 +165,7 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                 }
             }
         }
+        __syncwarp();   // M is rebuilt for the next sample
     }
 }
 
@@ -111,16 +173,22 @@ template <typename T, int RMAX>
 dlrm_status launch(const float* grad_out, const void* dense, const void* pooled, int F, int D, int B, int P,
                    float* gd, float* gp, cudaStream_t stream)
 {
+    const BwdSmem L = bwd_smem<RMAX>(F, D, P, (int)sizeof(T));
+    const size_t smem = (size_t)kWarps * L.warp_bytes;
+    if (smem > 200 * 1024)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: (F+1) x D too large for the staged backward");
+    auto kern = interact_bwd_kernel<T, RMAX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_bwd: %s", cudaGetErrorString(e));
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, interact_bwd_kernel<T, RMAX>, kWarps * kWarp, 0) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * kWarp, smem) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    interact_bwd_kernel<T, RMAX><<<(int)blocks, kWarps * kWarp, 0, stream>>>(
-        grad_out, (const T*)dense, (const T*)pooled, F, D, B, P, gd, gp);
+    kern<<<(int)blocks, kWarps * kWarp, smem, stream>>>(grad_out, (const T*)dense, (const T*)pooled, F, D, B, P,
+                                                        gd, gp);
     return check_launch("interact_bwd_kernel");
 }
 
