@@ -300,6 +300,22 @@ def run_ours(args) -> None:
     f1.record(stream)
     torch.cuda.synchronize()
     fms = reduce_max(f0.elapsed_time(f1), world, dev)
+
+    def fused_step():
+        dl.dlrm_emb_interact_fwd(tab16, rb16, F, D, B, idx16, off16, dense16, out16, P, status=status,
+                                 stream=stream)
+
+    for _ in range(args.warmup):
+        fused_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(args.steps):
+        fused_step()
+    u1.record(stream)
+    torch.cuda.synchronize()
+    ums = reduce_max(u0.elapsed_time(u1), world, dev)
     del tab16, pooled16, out16
 
     # ---- end to end through the public API from pinned host buffers
@@ -375,7 +391,12 @@ def run_ours(args) -> None:
                 "workload": "dlrm-default 64K forward: 26 single-hot fp16 tables, Zipf 1.05, 480 columns",
                 "ops_ms": {"emb_fwd": round(f_emb, 4), "interact_fwd_tcgen05": round(f_int, 4)},
                 "alg_GBps": {"emb_fwd": round(B * F * (8 + 2 * D * 2) / (f_emb / 1e3) / 1e9, 1),
-                             "interact_fwd": round(B * (D * 2 + F * D * 2 + P * 2) / (f_int / 1e3) / 1e9, 1)}},
+                             "interact_fwd": round(B * (D * 2 + F * D * 2 + P * 2) / (f_int / 1e3) / 1e9, 1)},
+                "fused": {"value": round(B * world * args.steps / (ums / 1e3), 1), "unit": "samples/s",
+                          "ms_per_step": round(ums / args.steps, 4),
+                          "entry_point": "dlrm_emb_interact_fwd (lookup + tcgen05 interaction in one kernel)",
+                          "alg_GBps": round(B * (F * (8 + D * 2) + D * 2 + P * 2) / (ums / args.steps / 1e3) / 1e9,
+                                            1)}},
         "e2e": {"value": round(B * world * e_steps / (ems / 1e3), 1), "unit": "samples/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": kernels_per_step(w.total_rows) * args.steps,
@@ -555,6 +576,11 @@ def run_config(args, name) -> None:
             ops.append(("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, Bw, idx, off, gp,
                                                                    w.lr, ws, status=status, stream=stream)))
         per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
+        fused_ms = None
+        if tt == torch.float16 and not train:
+            fop = [("emb_interact_fwd", lambda: dl.dlrm_emb_interact_fwd(tab, rb, F, D, Bw, idx, off, dense, out, P,
+                                                                         status=status, stream=stream))]
+            _, fused_ms = _time_ops(torch, stream, fop, args.steps, args.warmup)
         nnz = w.nnz
         alg = {"emb_fwd": nnz * (4 + D * es) + Bw * F * (4 + D * es),
                "interact_fwd": Bw * (D * es + F * D * es + P * es),
@@ -566,6 +592,10 @@ def run_config(args, name) -> None:
                 "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
                 "fwd_samples_per_s": round(Bw / (fwd_ms / 1e3), 1),
                 "step_samples_per_s": round(Bw / (ms / 1e3), 1), "device_status": int(status.item())}
+        if fused_ms is not None:
+            line["fused_fwd"] = {"ms": round(fused_ms, 4), "samples_per_s": round(Bw / (fused_ms / 1e3), 1),
+                                 "alg_GBps": round(Bw * (F * (8 + D * 2) + D * 2 + P * 2) / (fused_ms / 1e3) / 1e9,
+                                                   1)}
         print(json.dumps(line), flush=True)
         del tab, pooled, out, dense
         torch.cuda.empty_cache()

@@ -53,6 +53,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_emb_fwd.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, ctypes.c_uint, _P, _P]
     L.dlrm_interact_fwd.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P]
     L.dlrm_interact_fwd_cuda_core.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I, _P]
+    L.dlrm_emb_interact_fwd.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, _P, _I, ctypes.c_uint, _P, _P]
     L.dlrm_interact_bwd.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
     L.dlrm_emb_bwd_sgd_workspace_size.argtypes = [_I64, _I, _I64]
     L.dlrm_emb_bwd_sgd_workspace_size.restype = ctypes.c_size_t
@@ -65,7 +66,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_last_error.argtypes = []
     L.dlrm_last_error.restype = ctypes.c_char_p
     L.dlrm_synth_fill_uniform.argtypes = [_P, _I, ctypes.c_uint64, _I64, _I64, ctypes.c_double, _P]
-    for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core",
+    for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core", "dlrm_emb_interact_fwd",
               "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
         getattr(L, f).restype = _I
     if path is None:
@@ -128,6 +129,15 @@ def dlrm_interact_fwd_cuda_core(dense, pooled, F, D, B, out, out_cols, stream=No
     rc = load().dlrm_interact_fwd_cuda_core(_ptr(dense), _ptr(pooled), _dtype_code(pooled), F, D, B,
                                             _ptr(out), out_cols, _stream(stream))
     _check("dlrm_interact_fwd_cuda_core", rc)
+
+
+def dlrm_emb_interact_fwd(tables, row_base, F, D, B, indices, offsets, dense, out, out_cols, flags=0,
+                          status=None, stream=None):
+    """Lookup + interaction in one pass (inference); see ``include/dlrm.h``."""
+    rc = load().dlrm_emb_interact_fwd(_ptr(tables), _dtype_code(tables), _ptr(row_base), F, D, B, _ptr(indices),
+                                      _ptr(offsets), indices.numel(), _ptr(dense), _ptr(out), out_cols, flags,
+                                      _ptr(status), _stream(stream))
+    _check("dlrm_emb_interact_fwd", rc)
 
 
 def dlrm_interact_bwd(grad_out, dense, pooled, F, D, B, out_cols, grad_dense, grad_pooled, stream=None):

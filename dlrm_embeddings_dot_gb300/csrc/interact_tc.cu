@@ -23,6 +23,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane quarter q
 //               = warp % 4 holds sample q of the tile), triangle extraction
 //               into a shared output row, coalesced 16-byte stores.
+// Fused variant (dlrm_emb_interact_fwd, inference): the producer warp gathers
+// each bag's table row straight into the sample slots with cp.async, so the
+// pooled tensor never goes to HBM.
 // Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 overlap the
 // epilogue of tile i.  Every mbarrier wait is bounded; on timeout the kernel
 // sets DLRM_STATUS_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -66,6 +69,18 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+// Adds to the expected transaction bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_add_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
@@ -204,15 +219,26 @@ __host__ __device__ inline Layout make_layout(int KH, int P, int ns)
     L.stage_bytes = KH * kKBlockBytes;
     L.ns = ns;
     L.out_bytes = (kGroup * P * 2 + 15) / 16 * 16;
-    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16;
+    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16 + 8 * kGroup * kSlot;
     return L;
 }
 
+// Operands of the fused lookup (kFused): the joint fp16 table and the CSR lists.
+struct GatherArgs {
+    const __half* tables;
+    const int64_t* row_base;
+    const int32_t* indices;
+    const int32_t* offsets;
+    int64_t nnz;
+    bool hash;
+};
+
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                    const __grid_constant__ CUtensorMap map_dense, const __half* __restrict__ dense,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
-                   uint32_t* status)
+                   uint32_t* status, GatherArgs ga)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -225,6 +251,9 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // fused producer: source row of each (sample, table) of the tile being gathered
+    // (>= 0 row, -1 zero row, -2 several indices: summed by the producer)
+    int64_t* rowsrc = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(tempty + 2) + 16);
 
     const int warp = threadIdx.x / kWarp;
     const int lane = threadIdx.x % kWarp;
@@ -251,6 +280,16 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             for (int x = threadIdx.x; x < (kDenseRows - kGroup) * 128 / 16; x += kThreads)
                 z[x] = make_uint4(0, 0, 0, 0);
         }
+    if (kFused) {   // rows F..31 of each sample slot are never written by the gather
+        const int per_slot = (kSlot - F) * 8;   // 16-byte chunks of rows F..31 in one K block
+        for (int s = 0; s < NS; ++s)
+            for (int kb = 0; kb < KH; ++kb)
+                for (int x = threadIdx.x; x < kGroup * per_slot; x += kThreads) {
+                    const int slot = x / per_slot, r = F + (x % per_slot) / 8, c = x % 8;
+                    *reinterpret_cast<uint4*>(stages + (size_t)s * L.stage_bytes + kb * kKBlockBytes +
+                                              (slot * kSlot + r) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                }
+    }
     for (int x = threadIdx.x; x < kGroup * P; x += kThreads) ostage[x] = __float2half_rn(0.f);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
@@ -266,22 +305,143 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int it = 0;
+        if constexpr (!kFused) {
+            if (lane == 0) {
+                // ------------------------------------------------ TMA producer
+                int it = 0;
+                for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+                    const int stage = it % NS;
+                    const uint32_t ph = (uint32_t)(it / NS) & 1u;
+                    if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) break;
+                    uint8_t* sb = stages + (size_t)stage * L.stage_bytes;
+                    mbar_expect_tx(&full[stage], (uint32_t)KH * (kEBytes + kGroup * 128));
+                    for (int kb = 0; kb < KH; ++kb) {
+                        tma_load_3d(sb + kb * kKBlockBytes, &map_pooled, kb * kKB, 0, tile * kGroup, &full[stage]);
+                        tma_load_2d(sb + kb * kKBlockBytes + kEBytes, &map_dense, kb * kKB, tile * kGroup,
+                                    &full[stage]);
+                    }
+                }
+                if (*abort_flag) {   // let the copies already issued land before the CTA exits
+                    for (int j = (it > NS ? it - NS : 0); j < it; ++j)
+                        mbar_drain(&full[j % NS], (uint32_t)(j / NS) & 1u);
+                }
+            }
+        } else {
+            // ------------------------------------ gather producer (whole warp)
+            // Table rows go straight from the table into the swizzled sample slots
+            // with cp.async (16 lanes per 256-byte row, so every load is a full
+            // sector); the dense rows come by TMA.  A tile's arrive on its full
+            // barrier is posted one tile later, after its copies have landed and
+            // a proxy fence, so two tiles of gathers are in flight.
+            const int cpr = D / 8;                       // 16-byte chunks per row
+            int it = 0, prev = -1;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
                 const int stage = it % NS;
                 const uint32_t ph = (uint32_t)(it / NS) & 1u;
-                if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) break;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(&empty[stage], ph ^ 1u, abort_flag);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
                 uint8_t* sb = stages + (size_t)stage * L.stage_bytes;
-                mbar_expect_tx(&full[stage], (uint32_t)KH * (kEBytes + kGroup * 128));
-                for (int kb = 0; kb < KH; ++kb) {
-                    tma_load_3d(sb + kb * kKBlockBytes, &map_pooled, kb * kKB, 0, tile * kGroup, &full[stage]);
-                    tma_load_2d(sb + kb * kKBlockBytes + kEBytes, &map_dense, kb * kKB, tile * kGroup,
-                                &full[stage]);
+                if (lane == 0) {
+                    mbar_add_tx(&full[stage], (uint32_t)KH * (kGroup * 128));
+                    for (int kb = 0; kb < KH; ++kb)
+                        tma_load_2d(sb + kb * kKBlockBytes + kEBytes, &map_dense, kb * kKB, tile * kGroup,
+                                    &full[stage]);
                 }
+                // source rows of the tile's kGroup x F bags
+                for (int e = lane; e < kGroup * F; e += kWarp) {
+                    const int sm = e / F, t = e - sm * F;
+                    const int64_t b = (int64_t)tile * kGroup + sm;
+                    int64_t src = -1;
+                    if (b < B) {
+                        const int64_t bag = (int64_t)t * B + b;
+                        int64_t s0 = ga.offsets[bag], e0 = ga.offsets[bag + 1];
+                        if (s0 < 0 || e0 < s0 || e0 > ga.nnz) {
+                            set_status(status, DLRM_STATUS_BAD_OFFSETS);
+                            s0 = s0 < 0 ? 0 : (s0 > ga.nnz ? ga.nnz : s0);
+                            e0 = e0 < s0 ? s0 : (e0 > ga.nnz ? ga.nnz : e0);
+                        }
+                        if (e0 - s0 == 1) {
+                            int64_t i = ga.indices[s0];
+                            const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
+                            if (ga.hash && n > 0) {
+                                i %= n;
+                                if (i < 0) i += n;
+                                src = base + i;
+                            } else if (!ga.hash && i >= 0 && i < n) {
+                                src = base + i;
+                            } else {
+                                set_status(status, DLRM_STATUS_OOB_INDEX);
+                            }
+                        } else if (e0 - s0 > 1) {
+                            src = -2;
+                        }
+                    }
+                    rowsrc[sm * kSlot + t] = src;
+                }
+                __syncwarp();
+                const uint32_t sbase = smem_u32(sb);
+                for (int x = lane; x < kGroup * F * cpr; x += kWarp) {
+                    const int e = x / cpr, c = x - e * cpr;
+                    const int sm = e / F, t = e - sm * F;
+                    const int row = sm * kSlot + t;
+                    const int64_t src = rowsrc[sm * kSlot + t];
+                    const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    if (src >= 0)
+                        cp_async16(dst, ga.tables + src * D + 8 * c);
+                    else if (src == -1)
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+                }
+                // bags of several indices (rare here): fp32 sum in bag order, one rounding
+                for (int e = 0; e < kGroup * F; ++e) {
+                    if (rowsrc[(e / F) * kSlot + e % F] != -2) continue;
+                    const int sm = e / F, t = e - sm * F;
+                    const int64_t bag = (int64_t)t * B + (int64_t)tile * kGroup + sm;
+                    int64_t s0 = ga.offsets[bag], e0 = ga.offsets[bag + 1];
+                    s0 = s0 < 0 ? 0 : (s0 > ga.nnz ? ga.nnz : s0);
+                    e0 = e0 < s0 ? s0 : (e0 > ga.nnz ? ga.nnz : e0);
+                    const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
+                    const int row = sm * kSlot + t;
+                    for (int c = lane; c < cpr; c += kWarp) {
+                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        for (int64_t p = s0; p < e0; ++p) {
+                            int64_t i = ga.indices[p];
+                            if (ga.hash && n > 0) {
+                                i %= n;
+                                if (i < 0) i += n;
+                            } else if (ga.hash || i < 0 || i >= n) {
+                                set_status(status, DLRM_STATUS_OOB_INDEX);
+                                continue;
+                            }
+                            float f[8];
+                            h8_to_f8(ldg_nc_v4(ga.tables + (base + i) * D + 8 * c), f);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) acc[u] += f[u];
+                        }
+                        const uint4 v = f8_to_h8(acc);
+                        const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
+                                     "r"(v.w)
+                                     : "memory");
+                    }
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (prev >= 0) {   // the previous tile's rows have landed: publish them
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[prev]);
+                }
+                prev = stage;
+                __syncwarp();   // rowsrc is rewritten for the next tile
             }
-            if (*abort_flag) {   // let the copies already issued land before the CTA exits
+            if (prev >= 0) {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[prev]);
+            }
+            if (*abort_flag && lane == 0) {   // the dense copies already issued must land before exit
                 for (int j = (it > NS ? it - NS : 0); j < it; ++j)
                     mbar_drain(&full[j % NS], (uint32_t)(j / NS) & 1u);
             }
@@ -394,42 +554,101 @@ bool tc_interact_supported(int F, int D, int out_cols, const void* dense, const 
            out_cols <= 2048 && aligned16(dense) && aligned16(pooled) && aligned16(out);
 }
 
-dlrm_status tc_interact_fwd(const void* dense, const void* pooled, int F, int D, int B, void* out,
-                            int out_cols, uint32_t* status, cudaStream_t stream)
+// Tensor maps + launch of the tcgen05 kernel.  pooled == nullptr selects the
+// fused lookup (rows gathered from ga.tables).
+dlrm_status tc_launch(const void* dense, const void* pooled, const GatherArgs& ga, int F, int D, int B, void* out,
+                      int out_cols, uint32_t* status, cudaStream_t stream, const char* who)
 {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: cuTensorMapEncodeTiled unavailable");
+    if (!enc) return fail(DLRM_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", who);
     const int KH = D / kKB;
     int ns = kMaxStages;
     while (ns > 1 && make_layout(KH, out_cols, ns).smem > (size_t)kSmemLimit) --ns;
     const Layout L = make_layout(KH, out_cols, ns);
     if (ns < 2 || L.smem > (size_t)kSmemLimit)
-        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd: tensor-core tile does not fit shared memory");
+        return fail(DLRM_ERR_UNSUPPORTED, "%s: tensor-core tile does not fit shared memory", who);
 
     CUtensorMap mp, md;
-    const cuuint64_t pdims[3] = {(cuuint64_t)D, (cuuint64_t)F, (cuuint64_t)B};
-    const cuuint64_t pstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)F * D * 2};
-    const cuuint32_t pbox[3] = {(cuuint32_t)kKB, (cuuint32_t)kSlot, (cuuint32_t)kGroup};
     const cuuint32_t ones[3] = {1, 1, 1};
-    CUresult r = enc(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pooled), pdims, pstr, pbox, ones,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: encoding the pooled tensor map failed (%d)", (int)r);
     const cuuint64_t ddims[2] = {(cuuint64_t)D, (cuuint64_t)B};
     const cuuint64_t dstr[1] = {(cuuint64_t)D * 2};
     const cuuint32_t dbox[2] = {(cuuint32_t)kKB, (cuuint32_t)kGroup};
-    r = enc(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(dense), ddims, dstr, dbox, ones,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: encoding the dense tensor map failed (%d)", (int)r);
-
-    cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
-    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: %s", cudaGetErrorString(e));
+    CUresult r = enc(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(dense), ddims, dstr, dbox, ones,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DLRM_ERR_CUDA, "%s: encoding the dense tensor map failed (%d)", who, (int)r);
+    if (pooled) {
+        const cuuint64_t pdims[3] = {(cuuint64_t)D, (cuuint64_t)F, (cuuint64_t)B};
+        const cuuint64_t pstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)F * D * 2};
+        const cuuint32_t pbox[3] = {(cuuint32_t)kKB, (cuuint32_t)kSlot, (cuuint32_t)kGroup};
+        r = enc(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pooled), pdims, pstr, pbox, ones,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(DLRM_ERR_CUDA, "%s: encoding the pooled tensor map failed (%d)", who, (int)r);
+    } else {
+        mp = md;   // unused by the fused kernel
+    }
     const int ntiles = (B + kGroup - 1) / kGroup;
     const int grid = ntiles < num_sms() ? ntiles : num_sms();
-    interact_tc_kernel<<<grid, kThreads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F, D, B,
-                                                           out_cols, KH, ns, status);
+    if (pooled) {
+        cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L.smem);
+        if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+        interact_tc_kernel<false><<<grid, kThreads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
+                                                                      D, B, out_cols, KH, ns, status, ga);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L.smem);
+        if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+        interact_tc_kernel<true><<<grid, kThreads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
+                                                                     D, B, out_cols, KH, ns, status, ga);
+    }
     return check_launch("interact_tc_kernel");
 }
 
+dlrm_status tc_interact_fwd(const void* dense, const void* pooled, int F, int D, int B, void* out,
+                            int out_cols, uint32_t* status, cudaStream_t stream)
+{
+    return tc_launch(dense, pooled, GatherArgs{}, F, D, B, out, out_cols, status, stream, "dlrm_interact_fwd");
+}
+
 }  // namespace dlrm
+
+using namespace dlrm;
+
+extern "C" dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                             int F, int D, int B, const int32_t* d_indices,
+                                             const int32_t* d_offsets, int64_t nnz, const void* d_dense,
+                                             void* d_out, int out_cols, unsigned flags, uint32_t* d_status,
+                                             void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: bad dtype");
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: need F >= 1, D >= 1, B >= 0");
+    if (nnz < 0 || nnz >= (int64_t)1 << 31 || (int64_t)F * B >= (int64_t)1 << 31)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: nnz and F*B must be below 2^31");
+    const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
+    if (out_cols < W)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: out_cols %d < D + F(F+1)/2 = %lld", out_cols,
+                    (long long)W);
+    if (!d_tables || !d_row_base || !d_offsets || !d_dense || !d_out || (nnz > 0 && !d_indices))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: null device pointer");
+    if (flags & ~DLRM_FLAG_HASH_INDICES)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: unknown flag bits 0x%x", flags);
+    if (dtype != DLRM_F16 || !tc_interact_supported(F, D, out_cols, d_dense, d_dense, d_out) || !aligned16(d_tables))
+        return fail(DLRM_ERR_UNSUPPORTED,
+                    "dlrm_emb_interact_fwd: needs fp16, F <= 32, D a multiple of 64 up to 256, out_cols a multiple "
+                    "of 8 and 16-byte aligned pointers (use dlrm_emb_fwd + dlrm_interact_fwd otherwise)");
+    if (B == 0) return DLRM_OK;
+    GatherArgs ga;
+    ga.tables = (const __half*)d_tables;
+    ga.row_base = d_row_base;
+    ga.indices = d_indices;
+    ga.offsets = d_offsets;
+    ga.nnz = nnz;
+    ga.hash = (flags & DLRM_FLAG_HASH_INDICES) != 0;
+    return tc_launch(d_dense, nullptr, ga, F, D, B, d_out, out_cols, d_status, as_stream(stream),
+                     "dlrm_emb_interact_fwd");
+}

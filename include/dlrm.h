@@ -126,6 +126,29 @@ dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const void* d_poole
                                         void* stream);
 
 /*
+ * dlrm_emb_interact_fwd -- dlrm_emb_fwd followed by dlrm_interact_fwd in one
+ * pass, for inference: each bag's table row is gathered straight into the
+ * tensor-core tile, so the pooled tensor is never written to HBM.
+ * (The same two operations as above: "DLRM For PyTorch", §Model
+ * architecture; the interaction output is concatenated with the bottom-MLP
+ * output.)
+ *
+ *   out[b] = dlrm_interact_fwd(dense[b], dlrm_emb_fwd(bags of sample b))
+ *
+ * Results are bit-identical to the two calls (bags of one index are copied,
+ * larger bags are summed in fp32 in bag order and rounded once to fp16).
+ * Arguments as in dlrm_emb_fwd and dlrm_interact_fwd.  Requires fp16,
+ * F <= 32, D a multiple of 64 up to 256, out_cols a multiple of 8 and 16-byte
+ * aligned tables, dense and out; otherwise DLRM_ERR_UNSUPPORTED (use the two
+ * calls).  Status bits as in dlrm_emb_fwd, plus DLRM_STATUS_TIMEOUT.
+ */
+dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                  int F, int D, int B, const int32_t* d_indices,
+                                  const int32_t* d_offsets, int64_t nnz, const void* d_dense,
+                                  void* d_out, int out_cols, unsigned flags, uint32_t* d_status,
+                                  void* stream);
+
+/*
  * dlrm_interact_bwd -- gradient of dlrm_interact_fwd.
  * With G = grad_out[b][0..W) (pad columns ignored) and M the symmetric
  * (F+1)x(F+1) matrix M_ij = M_ji = G[D + i(i-1)/2 + j] (i > j), M_ii = 0:
