@@ -439,7 +439,7 @@ def run_op(args) -> None:
             else:
                 dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status)
     else:
-        dt = inputs.F16 if args.op == "emb_fwd16" else inputs.F32
+        dt = inputs.F16 if args.op in ("emb_fwd16", "emb_interact16") else inputs.F32
         rows = None
         if args.small_tables:   # ~10x fewer rows: keeps an ncu capture's device memory to a few hundred MB
             rows = inputs.log_uniform_rows(np.random.default_rng(np.random.SeedSequence([0, 11])), 26, 10, 4e5)
@@ -456,9 +456,14 @@ def run_op(args) -> None:
         ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
                          device=dev)
 
+        dense16 = torch.from_numpy(w.dense.astype(np.float16)).to(dev) if dt == inputs.F16 else None
+        out16 = torch.empty(B, P, dtype=torch.float16, device=dev) if dt == inputs.F16 else None
+
         def once():
             if args.op == "emb_bwd_sgd":
                 dl.dlrm_emb_bwd_sgd(tables, rb, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status)
+            elif args.op == "emb_interact16":
+                dl.dlrm_emb_interact_fwd(tables, rb, F, D, B, idx, off, dense16, out16, P, status=status)
             else:
                 dl.dlrm_emb_fwd(tables, rb, F, D, B, idx, off, pooled, status=status)
     for _ in range(args.warmup):
@@ -643,7 +648,7 @@ def main(argv=None) -> None:
     ap.add_argument("--config", choices=sorted(CONFIGS), action="append",
                     help="measure one of the pages' workloads instead of the headline step (repeatable)")
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
-                                     "emb_bwd_sgd"],
+                                     "emb_bwd_sgd", "emb_interact16"],
                     help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
     ap.add_argument("--small-tables", action="store_true",
                     help="with --op: tables with 10x fewer rows (log-uniform in [10, 4e5])")

@@ -48,6 +48,10 @@ constexpr int kKBlockBytes = kEBytes + kDBytes;   // 18 KB (multiple of 1 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;
 constexpr int kThreads = 192;
+constexpr int kThreadsFused = 256;                // + two resolver warps
+constexpr int kGatherDepth = 3;                   // tiles of cp.async gathers in flight
+constexpr int kResolveBatch = 3;                  // tiles a resolver warp resolves at once
+constexpr int kMetaSlots = 4 * kResolveBatch;     // rows-to-gather ring (two batches per resolver warp)
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;                // 227 KB opt-in per block
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
@@ -219,7 +223,8 @@ __host__ __device__ inline Layout make_layout(int KH, int P, int ns)
     L.stage_bytes = KH * kKBlockBytes;
     L.ns = ns;
     L.out_bytes = (kGroup * P * 2 + 15) / 16 * 16;
-    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16 + 8 * kGroup * kSlot;
+    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16 +
+             (size_t)kMetaSlots * (8 * kGroup * kSlot + 16);
     return L;
 }
 
@@ -234,7 +239,7 @@ struct GatherArgs {
 };
 
 template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFused ? kThreadsFused : kThreads, 1)
 interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                    const __grid_constant__ CUtensorMap map_dense, const __half* __restrict__ dense,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
@@ -251,9 +256,13 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    // fused producer: source row of each (sample, table) of the tile being gathered
-    // (>= 0 row, -1 zero row, -2 several indices: summed by the producer)
-    int64_t* rowsrc = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(tempty + 2) + 16);
+    // fused mode: ring of kMetaSlots tiles' source rows per (sample, table)
+    // (>= 0 row, -1 zero row, -2 several indices: summed by the producer),
+    // filled by the resolver warps, and its full/empty barriers
+    int64_t* ring = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(tempty + 2) + 16);
+    uint64_t* meta_full = reinterpret_cast<uint64_t*>(ring + kMetaSlots * kGroup * kSlot);
+    uint64_t* meta_empty = meta_full + kMetaSlots;
+    const int nthreads = kFused ? kThreadsFused : kThreads;
 
     const int warp = threadIdx.x / kWarp;
     const int lane = threadIdx.x % kWarp;
@@ -269,6 +278,11 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], kGroup);
         }
+        if (kFused)
+            for (int i = 0; i < kMetaSlots; ++i) {
+                mbar_init(&meta_full[i], 1);
+                mbar_init(&meta_empty[i], 1);
+            }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -277,20 +291,20 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
         for (int kb = 0; kb < KH; ++kb) {
             uint4* z = reinterpret_cast<uint4*>(stages + (size_t)s * L.stage_bytes + kb * kKBlockBytes +
                                                 kEBytes + kGroup * 128);
-            for (int x = threadIdx.x; x < (kDenseRows - kGroup) * 128 / 16; x += kThreads)
+            for (int x = threadIdx.x; x < (kDenseRows - kGroup) * 128 / 16; x += nthreads)
                 z[x] = make_uint4(0, 0, 0, 0);
         }
     if (kFused) {   // rows F..31 of each sample slot are never written by the gather
         const int per_slot = (kSlot - F) * 8;   // 16-byte chunks of rows F..31 in one K block
         for (int s = 0; s < NS; ++s)
             for (int kb = 0; kb < KH; ++kb)
-                for (int x = threadIdx.x; x < kGroup * per_slot; x += kThreads) {
+                for (int x = threadIdx.x; x < kGroup * per_slot; x += nthreads) {
                     const int slot = x / per_slot, r = F + (x % per_slot) / 8, c = x % 8;
                     *reinterpret_cast<uint4*>(stages + (size_t)s * L.stage_bytes + kb * kKBlockBytes +
                                               (slot * kSlot + r) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
                 }
     }
-    for (int x = threadIdx.x; x < kGroup * P; x += kThreads) ostage[x] = __float2half_rn(0.f);
+    for (int x = threadIdx.x; x < kGroup * P; x += nthreads) ostage[x] = __float2half_rn(0.f);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -331,10 +345,10 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             // Table rows go straight from the table into the swizzled sample slots
             // with cp.async (16 lanes per 256-byte row, so every load is a full
             // sector); the dense rows come by TMA.  A tile's arrive on its full
-            // barrier is posted one tile later, after its copies have landed and
-            // a proxy fence, so two tiles of gathers are in flight.
+            // barrier is posted kGatherDepth - 1 tiles later, after its copies
+            // have landed and a proxy fence, so kGatherDepth tiles are in flight.
             const int cpr = D / 8;                       // 16-byte chunks per row
-            int it = 0, prev = -1;
+            int it = 0, published = 0;   // tiles [published, it) have copies in flight
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
                 const int stage = it % NS;
                 const uint32_t ph = (uint32_t)(it / NS) & 1u;
@@ -348,52 +362,45 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                         tma_load_2d(sb + kb * kKBlockBytes + kEBytes, &map_dense, kb * kKB, tile * kGroup,
                                     &full[stage]);
                 }
-                // source rows of the tile's kGroup x F bags
-                for (int e = lane; e < kGroup * F; e += kWarp) {
-                    const int sm = e / F, t = e - sm * F;
-                    const int64_t b = (int64_t)tile * kGroup + sm;
-                    int64_t src = -1;
-                    if (b < B) {
-                        const int64_t bag = (int64_t)t * B + b;
-                        int64_t s0 = ga.offsets[bag], e0 = ga.offsets[bag + 1];
-                        if (s0 < 0 || e0 < s0 || e0 > ga.nnz) {
-                            set_status(status, DLRM_STATUS_BAD_OFFSETS);
-                            s0 = s0 < 0 ? 0 : (s0 > ga.nnz ? ga.nnz : s0);
-                            e0 = e0 < s0 ? s0 : (e0 > ga.nnz ? ga.nnz : e0);
-                        }
-                        if (e0 - s0 == 1) {
-                            int64_t i = ga.indices[s0];
-                            const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
-                            if (ga.hash && n > 0) {
-                                i %= n;
-                                if (i < 0) i += n;
-                                src = base + i;
-                            } else if (!ga.hash && i >= 0 && i < n) {
-                                src = base + i;
-                            } else {
-                                set_status(status, DLRM_STATUS_OOB_INDEX);
-                            }
-                        } else if (e0 - s0 > 1) {
-                            src = -2;
-                        }
-                    }
-                    rowsrc[sm * kSlot + t] = src;
-                }
+                // source rows of the tile's kGroup x F bags, from the resolver warps
+                const int mslot = it % kMetaSlots;
+                if (lane == 0) ok = mbar_wait(&meta_full[mslot], (uint32_t)(it / kMetaSlots) & 1u, abort_flag);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                const int64_t* rowsrc = ring + mslot * kGroup * kSlot;
                 __syncwarp();
                 const uint32_t sbase = smem_u32(sb);
-                for (int x = lane; x < kGroup * F * cpr; x += kWarp) {
-                    const int e = x / cpr, c = x - e * cpr;
-                    const int sm = e / F, t = e - sm * F;
+                auto gather_chunk = [&](int sm, int t, int c) {
                     const int row = sm * kSlot + t;
-                    const int64_t src = rowsrc[sm * kSlot + t];
+                    const int64_t src = rowsrc[row];
                     const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
                     if (src >= 0)
                         cp_async16(dst, ga.tables + src * D + 8 * c);
                     else if (src == -1)
                         asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+                };
+                if (kWarp % cpr == 0) {
+                    // each lane keeps one chunk column c; rows advance by 32 / cpr per step
+                    const int step = kWarp / cpr, c = lane % cpr;
+                    int sm = 0, t = lane / cpr;
+                    for (int e = lane / cpr; e < kGroup * F; e += step) {
+                        while (t >= F) {
+                            t -= F;
+                            ++sm;
+                        }
+                        gather_chunk(sm, t, c);
+                        t += step;
+                    }
+                } else {
+                    for (int x = lane; x < kGroup * F * cpr; x += kWarp) {
+                        const int e = x / cpr, c = x - e * cpr;
+                        const int sm = e / F;
+                        gather_chunk(sm, e - sm * F, c);
+                    }
                 }
-                // bags of several indices (rare here): fp32 sum in bag order, one rounding
-                for (int e = 0; e < kGroup * F; ++e) {
+                // bags of several indices (rare): fp32 sum in bag order, one rounding
+                bool any_multi = false;
+                for (int e = lane; e < kGroup * F; e += kWarp) any_multi |= rowsrc[(e / F) * kSlot + e % F] == -2;
+                for (int e = 0; __any_sync(0xffffffffu, any_multi) && e < kGroup * F; ++e) {
                     if (rowsrc[(e / F) * kSlot + e % F] != -2) continue;
                     const int sm = e / F, t = e - sm * F;
                     const int64_t bag = (int64_t)t * B + (int64_t)tile * kGroup + sm;
@@ -425,22 +432,28 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                                      : "memory");
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&meta_empty[mslot]);   // the ring slot has been read
                 asm volatile("cp.async.commit_group;" ::: "memory");
-                if (prev >= 0) {   // the previous tile's rows have landed: publish them
-                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                // (the stage ring must be deeper than the gathers in flight, or the
+                // producer would wait on a stage whose tile it has not published yet)
+                if (it + 1 - published >= (NS > kGatherDepth ? kGatherDepth : NS - 1)) {
+                    // the oldest tile's rows have landed: publish it
+                    if (NS > kGatherDepth)
+                        asm volatile("cp.async.wait_group %0;" ::"n"(kGatherDepth - 1) : "memory");
+                    else
+                        asm volatile("cp.async.wait_group 0;" ::: "memory");
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[prev]);
+                    if (lane == 0) mbar_arrive(&full[published % NS]);
+                    ++published;
                 }
-                prev = stage;
-                __syncwarp();   // rowsrc is rewritten for the next tile
             }
-            if (prev >= 0) {
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[prev]);
-            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            for (; published < it; ++published)
+                if (lane == 0) mbar_arrive(&full[published % NS]);
             if (*abort_flag && lane == 0) {   // the dense copies already issued must land before exit
                 for (int j = (it > NS ? it - NS : 0); j < it; ++j)
                     mbar_drain(&full[j % NS], (uint32_t)(j / NS) & 1u);
@@ -473,7 +486,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             if (*abort_flag && it > 0)   // MMAs already issued must finish before TMEM is freed
                 mbar_drain(&tfull[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u);
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;                     // TMEM lane quarter == sample in tile
         __half* os = ostage + q * P;
@@ -514,6 +527,90 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             }
         }
         (void)W;
+    } else if constexpr (kFused) {
+        // ---------------------------------------------------- resolvers
+        // Warp 6 + r resolves batches of kResolveBatch consecutive tiles of this
+        // CTA (batches r, r + 2, ...): offsets -> index -> hashed or checked
+        // global row, with all offset loads and then all index loads of the
+        // batch in flight together, into ring slots it % kMetaSlots.
+        const int r = warp - 6;
+        constexpr int kPer = (kGroup * kSlot + kWarp - 1) / kWarp;   // entries per lane per tile
+        for (int g = r;; g += 2) {
+            const int it0 = g * kResolveBatch;
+            if (blockIdx.x + it0 * (int)gridDim.x >= ntiles) break;
+            int ok = 1;
+            if (lane == 0)
+                for (int k = 0; k < kResolveBatch && ok; ++k) {
+                    const int it = it0 + k;
+                    if (blockIdx.x + it * (int)gridDim.x < ntiles)
+                        ok = mbar_wait(&meta_empty[it % kMetaSlots], ((uint32_t)(it / kMetaSlots) & 1u) ^ 1u,
+                                       abort_flag);
+                }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            int64_t s0[kResolveBatch][kPer], e0[kResolveBatch][kPer];
+#pragma unroll
+            for (int k = 0; k < kResolveBatch; ++k)
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int e = lane + u * kWarp;
+                    const int64_t tile = (int64_t)blockIdx.x + (int64_t)(it0 + k) * gridDim.x;
+                    s0[k][u] = e0[k][u] = 0;
+                    if (e < kGroup * F && tile < ntiles) {
+                        const int sm = e / F, t = e - sm * F;
+                        const int64_t b = tile * kGroup + sm;
+                        if (b < B) {
+                            s0[k][u] = ga.offsets[(int64_t)t * B + b];
+                            e0[k][u] = ga.offsets[(int64_t)t * B + b + 1];
+                        }
+                    }
+                }
+            int32_t idx[kResolveBatch][kPer];
+#pragma unroll
+            for (int k = 0; k < kResolveBatch; ++k)
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int64_t a = s0[k][u];
+                    idx[k][u] = (e0[k][u] - a == 1 && a >= 0 && a < ga.nnz) ? ga.indices[a] : 0;
+                }
+#pragma unroll
+            for (int k = 0; k < kResolveBatch; ++k) {
+                const int it = it0 + k;
+                if (blockIdx.x + it * (int)gridDim.x >= ntiles) break;
+                int64_t* rowsrc = ring + (it % kMetaSlots) * kGroup * kSlot;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int e = lane + u * kWarp;
+                    if (e >= kGroup * F) continue;
+                    const int sm = e / F, t = e - sm * F;
+                    int64_t a = s0[k][u], z = e0[k][u];
+                    if (a < 0 || z < a || z > ga.nnz) {
+                        set_status(status, DLRM_STATUS_BAD_OFFSETS);
+                        a = a < 0 ? 0 : (a > ga.nnz ? ga.nnz : a);
+                        z = z < a ? a : (z > ga.nnz ? ga.nnz : z);
+                    }
+                    int64_t src = -1;
+                    if (z - a == 1) {
+                        if (e0[k][u] - s0[k][u] != 1) idx[k][u] = ga.indices[a];   // clamped bag
+                        int64_t i = idx[k][u];
+                        const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
+                        if (ga.hash && n > 0) {
+                            i %= n;
+                            if (i < 0) i += n;
+                            src = base + i;
+                        } else if (!ga.hash && i >= 0 && i < n) {
+                            src = base + i;
+                        } else {
+                            set_status(status, DLRM_STATUS_OOB_INDEX);
+                        }
+                    } else if (z - a > 1) {
+                        src = -2;
+                    }
+                    rowsrc[sm * kSlot + t] = src;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&meta_full[it % kMetaSlots]);
+            }
+        }
     }
 
     tc_fence_before();
@@ -601,7 +698,7 @@ dlrm_status tc_launch(const void* dense, const void* pooled, const GatherArgs& g
         cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)L.smem);
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-        interact_tc_kernel<true><<<grid, kThreads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
+        interact_tc_kernel<true><<<grid, kThreadsFused, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
                                                                      D, B, out_cols, KH, ns, status, ga);
     }
     return check_launch("interact_tc_kernel");
