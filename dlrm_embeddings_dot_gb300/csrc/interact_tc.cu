@@ -4,8 +4,9 @@
 //
 // Per sample, Z = [d; e_0 .. e_{F-1}] and the output needs z_i . z_j for
 // i > j.  Four samples form one M = 128 tile: sample s's F embedding rows sit
-// at rows 32s .. 32s+F-1 (rows F..31 zero), so the 128 x 128 product of the
-// tile with itself holds each sample's E E^T in a 32 x 32 diagonal block.  The
+// at rows 32s .. 32s+F-1, so the 128 x 128 product of the tile with itself
+// holds each sample's E E^T in a 32 x 32 diagonal block.  Rows F..31 of a
+// slot may hold anything: every product they enter is left unread.  The
 // dense rows of the four samples are appended as B rows 128..131 (rows
 // 132..143 zero), so one tcgen05.mma of M = 128, N = 144 per 16-wide K step
 // also yields every e_r . d.  The 75 % of the product outside the diagonal
@@ -23,9 +24,12 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane quarter q
 //               = warp % 4 holds sample q of the tile), triangle extraction
 //               into a shared output row, coalesced 16-byte stores.
-// Fused variant (dlrm_emb_interact_fwd, inference): the producer warp gathers
-// each bag's table row straight into the sample slots with cp.async, so the
-// pooled tensor never goes to HBM.
+// Fused variant (dlrm_emb_interact_fwd, inference): each sample slot of a
+// tile is filled by one gather warp straight from the table, so the pooled
+// tensor never goes to HBM.  Twelve gather warps (warp 0 and warps 6..16, in
+// teams of four) fill three tiles at once with 16-byte register loads: a
+// table row is only 256 bytes, and the TMA engine's rate for such small row
+// gathers (tile::gather4) is several times below what the warps reach.
 // Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 overlap the
 // epilogue of tile i.  Every mbarrier wait is bounded; on timeout the kernel
 // sets DLRM_STATUS_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -48,10 +52,9 @@ constexpr int kKBlockBytes = kEBytes + kDBytes;   // 18 KB (multiple of 1 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;
 constexpr int kThreads = 192;
-constexpr int kThreadsFused = 256;                // + two resolver warps
-constexpr int kGatherDepth = 3;                   // tiles of cp.async gathers in flight
-constexpr int kResolveBatch = 3;                  // tiles a resolver warp resolves at once
-constexpr int kMetaSlots = 4 * kResolveBatch;     // rows-to-gather ring (two batches per resolver warp)
+constexpr int kTeams = 3;                         // fused: tiles gathered at once, four warps each
+constexpr int kThreadsFused = (5 + kGroup * kTeams) * 32;   // + gather warps 6.. (warp 0 gathers too)
+constexpr int kGatherU = 13;                      // fused: 16-byte row loads in flight per lane
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;                // 227 KB opt-in per block
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
@@ -73,18 +76,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
-}
-
-// Adds to the expected transaction bytes of the current phase without arriving.
-__device__ __forceinline__ void mbar_add_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
@@ -223,8 +214,7 @@ __host__ __device__ inline Layout make_layout(int KH, int P, int ns)
     L.stage_bytes = KH * kKBlockBytes;
     L.ns = ns;
     L.out_bytes = (kGroup * P * 2 + 15) / 16 * 16;
-    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16 +
-             (size_t)kMetaSlots * (8 * kGroup * kSlot + 16);
+    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16;
     return L;
 }
 
@@ -238,10 +228,13 @@ struct GatherArgs {
     bool hash;
 };
 
-template <bool kFused>
+// kCpr: 16-byte chunks per table row when fixed at compile time (fused
+// gather, D = 64, 128, 256), else 0.
+template <bool kFused, int kCpr>
 __global__ void __launch_bounds__(kFused ? kThreadsFused : kThreads, 1)
 interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
-                   const __grid_constant__ CUtensorMap map_dense, const __half* __restrict__ dense,
+                   const __grid_constant__ CUtensorMap map_dense,
+                   const __half* __restrict__ dense,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
                    uint32_t* status, GatherArgs ga)
 {
@@ -256,12 +249,6 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    // fused mode: ring of kMetaSlots tiles' source rows per (sample, table)
-    // (>= 0 row, -1 zero row, -2 several indices: summed by the producer),
-    // filled by the resolver warps, and its full/empty barriers
-    int64_t* ring = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(tempty + 2) + 16);
-    uint64_t* meta_full = reinterpret_cast<uint64_t*>(ring + kMetaSlots * kGroup * kSlot);
-    uint64_t* meta_empty = meta_full + kMetaSlots;
     const int nthreads = kFused ? kThreadsFused : kThreads;
 
     const int warp = threadIdx.x / kWarp;
@@ -271,18 +258,13 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], kFused ? kGroup : 1);   // fused: one arrive per gather warp of the tile
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], kGroup);
         }
-        if (kFused)
-            for (int i = 0; i < kMetaSlots; ++i) {
-                mbar_init(&meta_full[i], 1);
-                mbar_init(&meta_empty[i], 1);
-            }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -294,16 +276,6 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             for (int x = threadIdx.x; x < (kDenseRows - kGroup) * 128 / 16; x += nthreads)
                 z[x] = make_uint4(0, 0, 0, 0);
         }
-    if (kFused) {   // rows F..31 of each sample slot are never written by the gather
-        const int per_slot = (kSlot - F) * 8;   // 16-byte chunks of rows F..31 in one K block
-        for (int s = 0; s < NS; ++s)
-            for (int kb = 0; kb < KH; ++kb)
-                for (int x = threadIdx.x; x < kGroup * per_slot; x += nthreads) {
-                    const int slot = x / per_slot, r = F + (x % per_slot) / 8, c = x % 8;
-                    *reinterpret_cast<uint4*>(stages + (size_t)s * L.stage_bytes + kb * kKBlockBytes +
-                                              (slot * kSlot + r) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                }
-    }
     for (int x = threadIdx.x; x < kGroup * P; x += nthreads) ostage[x] = __float2half_rn(0.f);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
@@ -318,7 +290,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    if (warp == 0) {
+    if (warp == 0 || warp >= 6) {
         if constexpr (!kFused) {
             if (lane == 0) {
                 // ------------------------------------------------ TMA producer
@@ -341,78 +313,145 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                 }
             }
         } else {
-            // ------------------------------------ gather producer (whole warp)
-            // Table rows go straight from the table into the swizzled sample slots
-            // with cp.async (16 lanes per 256-byte row, so every load is a full
-            // sector); the dense rows come by TMA.  A tile's arrive on its full
-            // barrier is posted kGatherDepth - 1 tiles later, after its copies
-            // have landed and a proxy fence, so kGatherDepth tiles are in flight.
-            const int cpr = D / 8;                       // 16-byte chunks per row
-            int it = 0, published = 0;   // tiles [published, it) have copies in flight
-            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+            // ------------------------------------ gather warps
+            // Warp gi (warp 0, then warps 6..) fills slot sm = gi % 4 of the
+            // tiles of team gi / 4: tiles team, team + kTeams, ... of this CTA.
+            // Lane t < F owns bag (t, b) of the slot's sample b.  Offsets are
+            // read two tiles ahead and the index one tile ahead, so each tile
+            // costs the warp one memory round trip: the table rows (16 lanes
+            // per 256-byte row, 16-byte loads into registers) are in flight
+            // before the warp waits for the stage, then stored swizzled.
+            const int gi = warp == 0 ? 0 : warp - 5;
+            const int team = gi / kGroup, sm = gi % kGroup;
+            const int cpr = D / 8;                        // 16-byte chunks per row
+            const int nchunks = F * cpr;
+            int64_t tbase = 0, tn = 0;                    // lane t < F: table t's first row and row count
+            if (lane < F) {
+                tbase = ga.row_base[lane];
+                tn = ga.row_base[lane + 1] - tbase;
+            }
+            const int64_t tstride = (int64_t)kTeams * gridDim.x;
+            auto load_bounds = [&](int64_t tile, int& s0, int& e0) {
+                s0 = e0 = 0;
+                const int64_t b = tile * kGroup + sm;
+                if (lane < F && tile < ntiles && b < B) {
+                    s0 = __ldg(ga.offsets + (int64_t)lane * B + b);
+                    e0 = __ldg(ga.offsets + (int64_t)lane * B + b + 1);
+                }
+            };
+            auto clamp_bounds = [&](int& s0, int& e0) {   // into [0, nnz], flagging malformed lists
+                int64_t a = s0, z = e0;
+                if (a < 0 || z < a || z > ga.nnz) {
+                    set_status(status, DLRM_STATUS_BAD_OFFSETS);
+                    a = a < 0 ? 0 : (a > ga.nnz ? ga.nnz : a);
+                    z = z < a ? a : (z > ga.nnz ? ga.nnz : z);
+                }
+                s0 = (int)a;
+                e0 = (int)z;
+            };
+            // bag -> source: a table row (32 bits: a joint table of 2^32 rows of
+            // at least 128 bytes would not fit in memory), kRowZero (empty bag,
+            // rejected index) or kRowMulti (several indices)
+            constexpr uint32_t kRowZero = 0xffffffffu, kRowMulti = 0xfffffffeu;
+            auto resolve = [&](int a, int z, int idx) -> uint32_t {
+                if (lane >= F || z - a == 0) return kRowZero;
+                if (z - a > 1) return kRowMulti;
+                int64_t i = idx;
+                if (ga.hash && tn > 0) {
+                    i %= tn;
+                    if (i < 0) i += tn;
+                } else if (ga.hash || i < 0 || i >= tn || tbase + i >= (int64_t)kRowMulti) {
+                    set_status(status, DLRM_STATUS_OOB_INDEX);
+                    return kRowZero;
+                }
+                return (uint32_t)(tbase + i);
+            };
+            // chunk k of this lane: row e of the slot, 16-byte column c.  With
+            // 32 % cpr == 0 (D = 64, 128, 256) the column is fixed per lane.
+            const int Dr = kCpr > 0 ? 8 * kCpr : D;
+            auto chunk_of = [&](int k, int& e, int& c) {
+                if constexpr (kCpr > 0 && kWarp % kCpr == 0) {
+                    e = lane / kCpr + k * (kWarp / kCpr);
+                    c = lane % kCpr;
+                } else {
+                    const int x = lane + kWarp * k;
+                    e = x / cpr;
+                    c = x - e * cpr;
+                }
+            };
+            const int nsteps = (nchunks + kWarp - 1) / kWarp;
+            int64_t tile = blockIdx.x + (int64_t)team * gridDim.x;
+            int it = team;
+            int a0, z0, a1, z1, idx0 = 0;
+            load_bounds(tile, a0, z0);
+            load_bounds(tile + tstride, a1, z1);
+            clamp_bounds(a0, z0);
+            if (z0 - a0 == 1) idx0 = __ldg(ga.indices + a0);
+            clamp_bounds(a1, z1);
+            for (; tile < ntiles; tile += tstride, it += kTeams) {
                 const int stage = it % NS;
                 const uint32_t ph = (uint32_t)(it / NS) & 1u;
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(&empty[stage], ph ^ 1u, abort_flag);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                const uint32_t row0 = resolve(a0, z0, idx0);
+                // in flight together: next tile's index, the bounds two tiles on, this tile's rows
+                int idx1 = 0, a2, z2;
+                if (z1 - a1 == 1) idx1 = __ldg(ga.indices + a1);
+                load_bounds(tile + 2 * tstride, a2, z2);
+                const int64_t b = tile * kGroup + sm;
                 uint8_t* sb = stages + (size_t)stage * L.stage_bytes;
-                if (lane == 0) {
-                    mbar_add_tx(&full[stage], (uint32_t)KH * (kGroup * 128));
-                    for (int kb = 0; kb < KH; ++kb)
-                        tma_load_2d(sb + kb * kKBlockBytes + kEBytes, &map_dense, kb * kKB, tile * kGroup,
-                                    &full[stage]);
-                }
-                // source rows of the tile's kGroup x F bags, from the resolver warps
-                const int mslot = it % kMetaSlots;
-                if (lane == 0) ok = mbar_wait(&meta_full[mslot], (uint32_t)(it / kMetaSlots) & 1u, abort_flag);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                const int64_t* rowsrc = ring + mslot * kGroup * kSlot;
-                __syncwarp();
                 const uint32_t sbase = smem_u32(sb);
-                auto gather_chunk = [&](int sm, int t, int c) {
-                    const int row = sm * kSlot + t;
-                    const int64_t src = rowsrc[row];
-                    const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    if (src >= 0)
-                        cp_async16(dst, ga.tables + src * D + 8 * c);
-                    else if (src == -1)
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
-                };
-                if (kWarp % cpr == 0) {
-                    // each lane keeps one chunk column c; rows advance by 32 / cpr per step
-                    const int step = kWarp / cpr, c = lane % cpr;
-                    int sm = 0, t = lane / cpr;
-                    for (int e = lane / cpr; e < kGroup * F; e += step) {
-                        while (t >= F) {
-                            t -= F;
-                            ++sm;
+                uint4 dv = make_uint4(0, 0, 0, 0);
+                if (lane < cpr && b < B) dv = ldg_nc_v4(dense + b * D + 8 * lane);
+                bool ok = true;
+                for (int k0 = 0; k0 < nsteps; k0 += kGatherU) {
+                    uint4 v[kGatherU];
+                    uint32_t store = 0;
+#pragma unroll
+                    for (int u = 0; u < kGatherU; ++u) {
+                        int e, c;
+                        chunk_of(k0 + u, e, c);          // e >= F past the last step
+                        const uint32_t src = __shfl_sync(0xffffffffu, row0, e < F ? e : 0);
+                        v[u] = make_uint4(0, 0, 0, 0);
+                        if (e < F && src != kRowMulti) {
+                            store |= 1u << u;
+                            if (src != kRowZero) v[u] = ldg_nc_v4(ga.tables + (size_t)src * Dr + 8 * c);
                         }
-                        gather_chunk(sm, t, c);
-                        t += step;
                     }
-                } else {
-                    for (int x = lane; x < kGroup * F * cpr; x += kWarp) {
-                        const int e = x / cpr, c = x - e * cpr;
-                        const int sm = e / F;
-                        gather_chunk(sm, e - sm * F, c);
+                    if (k0 == 0) {
+                        int w = 1;
+                        if (lane == 0) w = mbar_wait(&empty[stage], ph ^ 1u, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+                        if (!ok) break;
                     }
+#pragma unroll
+                    for (int u = 0; u < kGatherU; ++u) {
+                        if (!(store >> u & 1u)) continue;
+                        int e, c;
+                        chunk_of(k0 + u, e, c);
+                        const int row = sm * kSlot + e;
+                        const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[u].x), "r"(v[u].y),
+                                     "r"(v[u].z), "r"(v[u].w)
+                                     : "memory");
+                    }
+                }
+                if (!ok) break;
+                if (lane < cpr) {   // dense row -> B row 128 + sm
+                    const uint32_t dst = sbase + (lane >> 3) * kKBlockBytes + kEBytes + sm * 128 +
+                                         (((lane & 7) ^ (sm & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(dv.x), "r"(dv.y), "r"(dv.z),
+                                 "r"(dv.w)
+                                 : "memory");
                 }
                 // bags of several indices (rare): fp32 sum in bag order, one rounding
-                bool any_multi = false;
-                for (int e = lane; e < kGroup * F; e += kWarp) any_multi |= rowsrc[(e / F) * kSlot + e % F] == -2;
-                for (int e = 0; __any_sync(0xffffffffu, any_multi) && e < kGroup * F; ++e) {
-                    if (rowsrc[(e / F) * kSlot + e % F] != -2) continue;
-                    const int sm = e / F, t = e - sm * F;
-                    const int64_t bag = (int64_t)t * B + (int64_t)tile * kGroup + sm;
-                    int64_t s0 = ga.offsets[bag], e0 = ga.offsets[bag + 1];
-                    s0 = s0 < 0 ? 0 : (s0 > ga.nnz ? ga.nnz : s0);
-                    e0 = e0 < s0 ? s0 : (e0 > ga.nnz ? ga.nnz : e0);
-                    const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
+                for (uint32_t multi = __ballot_sync(0xffffffffu, row0 == kRowMulti); multi; multi &= multi - 1) {
+                    const int t = __ffs(multi) - 1;
+                    const int s1 = __shfl_sync(0xffffffffu, a0, t), e1 = __shfl_sync(0xffffffffu, z0, t);
+                    const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
                     const int row = sm * kSlot + t;
                     for (int c = lane; c < cpr; c += kWarp) {
                         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int64_t p = s0; p < e0; ++p) {
-                            int64_t i = ga.indices[p];
+                        for (int p = s1; p < e1; ++p) {
+                            int64_t i = __ldg(ga.indices + p);
                             if (ga.hash && n > 0) {
                                 i %= n;
                                 if (i < 0) i += n;
@@ -425,38 +464,23 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
 #pragma unroll
                             for (int u = 0; u < 8; ++u) acc[u] += f[u];
                         }
-                        const uint4 v = f8_to_h8(acc);
+                        const uint4 w = f8_to_h8(acc);
                         const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
-                                     "r"(v.w)
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                                     "r"(w.w)
                                      : "memory");
                     }
                 }
+                // generic-proxy writes -> visible to the tensor core, then publish this slot
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&meta_empty[mslot]);   // the ring slot has been read
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                // (the stage ring must be deeper than the gathers in flight, or the
-                // producer would wait on a stage whose tile it has not published yet)
-                if (it + 1 - published >= (NS > kGatherDepth ? kGatherDepth : NS - 1)) {
-                    // the oldest tile's rows have landed: publish it
-                    if (NS > kGatherDepth)
-                        asm volatile("cp.async.wait_group %0;" ::"n"(kGatherDepth - 1) : "memory");
-                    else
-                        asm volatile("cp.async.wait_group 0;" ::: "memory");
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[published % NS]);
-                    ++published;
-                }
-            }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            for (; published < it; ++published)
-                if (lane == 0) mbar_arrive(&full[published % NS]);
-            if (*abort_flag && lane == 0) {   // the dense copies already issued must land before exit
-                for (int j = (it > NS ? it - NS : 0); j < it; ++j)
-                    mbar_drain(&full[j % NS], (uint32_t)(j / NS) & 1u);
+                if (lane == 0) mbar_arrive(&full[stage]);
+                a0 = a1;
+                z0 = z1;
+                idx0 = idx1;
+                clamp_bounds(a2, z2);
+                a1 = a2;
+                z1 = z2;
             }
         }
     } else if (warp == 1) {
@@ -527,90 +551,6 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             }
         }
         (void)W;
-    } else if constexpr (kFused) {
-        // ---------------------------------------------------- resolvers
-        // Warp 6 + r resolves batches of kResolveBatch consecutive tiles of this
-        // CTA (batches r, r + 2, ...): offsets -> index -> hashed or checked
-        // global row, with all offset loads and then all index loads of the
-        // batch in flight together, into ring slots it % kMetaSlots.
-        const int r = warp - 6;
-        constexpr int kPer = (kGroup * kSlot + kWarp - 1) / kWarp;   // entries per lane per tile
-        for (int g = r;; g += 2) {
-            const int it0 = g * kResolveBatch;
-            if (blockIdx.x + it0 * (int)gridDim.x >= ntiles) break;
-            int ok = 1;
-            if (lane == 0)
-                for (int k = 0; k < kResolveBatch && ok; ++k) {
-                    const int it = it0 + k;
-                    if (blockIdx.x + it * (int)gridDim.x < ntiles)
-                        ok = mbar_wait(&meta_empty[it % kMetaSlots], ((uint32_t)(it / kMetaSlots) & 1u) ^ 1u,
-                                       abort_flag);
-                }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            int64_t s0[kResolveBatch][kPer], e0[kResolveBatch][kPer];
-#pragma unroll
-            for (int k = 0; k < kResolveBatch; ++k)
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int e = lane + u * kWarp;
-                    const int64_t tile = (int64_t)blockIdx.x + (int64_t)(it0 + k) * gridDim.x;
-                    s0[k][u] = e0[k][u] = 0;
-                    if (e < kGroup * F && tile < ntiles) {
-                        const int sm = e / F, t = e - sm * F;
-                        const int64_t b = tile * kGroup + sm;
-                        if (b < B) {
-                            s0[k][u] = ga.offsets[(int64_t)t * B + b];
-                            e0[k][u] = ga.offsets[(int64_t)t * B + b + 1];
-                        }
-                    }
-                }
-            int32_t idx[kResolveBatch][kPer];
-#pragma unroll
-            for (int k = 0; k < kResolveBatch; ++k)
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int64_t a = s0[k][u];
-                    idx[k][u] = (e0[k][u] - a == 1 && a >= 0 && a < ga.nnz) ? ga.indices[a] : 0;
-                }
-#pragma unroll
-            for (int k = 0; k < kResolveBatch; ++k) {
-                const int it = it0 + k;
-                if (blockIdx.x + it * (int)gridDim.x >= ntiles) break;
-                int64_t* rowsrc = ring + (it % kMetaSlots) * kGroup * kSlot;
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int e = lane + u * kWarp;
-                    if (e >= kGroup * F) continue;
-                    const int sm = e / F, t = e - sm * F;
-                    int64_t a = s0[k][u], z = e0[k][u];
-                    if (a < 0 || z < a || z > ga.nnz) {
-                        set_status(status, DLRM_STATUS_BAD_OFFSETS);
-                        a = a < 0 ? 0 : (a > ga.nnz ? ga.nnz : a);
-                        z = z < a ? a : (z > ga.nnz ? ga.nnz : z);
-                    }
-                    int64_t src = -1;
-                    if (z - a == 1) {
-                        if (e0[k][u] - s0[k][u] != 1) idx[k][u] = ga.indices[a];   // clamped bag
-                        int64_t i = idx[k][u];
-                        const int64_t base = ga.row_base[t], n = ga.row_base[t + 1] - base;
-                        if (ga.hash && n > 0) {
-                            i %= n;
-                            if (i < 0) i += n;
-                            src = base + i;
-                        } else if (!ga.hash && i >= 0 && i < n) {
-                            src = base + i;
-                        } else {
-                            set_status(status, DLRM_STATUS_OOB_INDEX);
-                        }
-                    } else if (z - a > 1) {
-                        src = -2;
-                    }
-                    rowsrc[sm * kSlot + t] = src;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&meta_full[it % kMetaSlots]);
-            }
-        }
     }
 
     tc_fence_before();
@@ -651,6 +591,19 @@ bool tc_interact_supported(int F, int D, int out_cols, const void* dense, const 
            out_cols <= 2048 && aligned16(dense) && aligned16(pooled) && aligned16(out);
 }
 
+template <bool kFused, int kCpr>
+dlrm_status launch_kernel(int grid, int threads, const Layout& L, const CUtensorMap& mp, const CUtensorMap& md,
+                          const void* dense, void* out, int F, int D, int B, int P, int KH, int ns, uint32_t* status,
+                          const GatherArgs& ga, cudaStream_t stream, const char* who)
+{
+    cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<kFused, kCpr>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L.smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    interact_tc_kernel<kFused, kCpr><<<grid, threads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
+                                                                        D, B, P, KH, ns, status, ga);
+    return check_launch("interact_tc_kernel");
+}
+
 // Tensor maps + launch of the tcgen05 kernel.  pooled == nullptr selects the
 // fused lookup (rows gathered from ga.tables).
 dlrm_status tc_launch(const void* dense, const void* pooled, const GatherArgs& ga, int F, int D, int B, void* out,
@@ -688,20 +641,19 @@ dlrm_status tc_launch(const void* dense, const void* pooled, const GatherArgs& g
     }
     const int ntiles = (B + kGroup - 1) / kGroup;
     const int grid = ntiles < num_sms() ? ntiles : num_sms();
-    if (pooled) {
-        cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)L.smem);
-        if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-        interact_tc_kernel<false><<<grid, kThreads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
-                                                                      D, B, out_cols, KH, ns, status, ga);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)L.smem);
-        if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-        interact_tc_kernel<true><<<grid, kThreadsFused, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
-                                                                     D, B, out_cols, KH, ns, status, ga);
+    if (pooled)
+        return launch_kernel<false, 0>(grid, kThreads, L, mp, md, dense, out, F, D, B, out_cols, KH, ns, status, ga,
+                                       stream, who);
+    switch (D / 8) {
+    case 8: return launch_kernel<true, 8>(grid, kThreadsFused, L, mp, md, dense, out, F, D, B, out_cols, KH, ns, status,
+                                          ga, stream, who);
+    case 16: return launch_kernel<true, 16>(grid, kThreadsFused, L, mp, md, dense, out, F, D, B, out_cols, KH, ns,
+                                            status, ga, stream, who);
+    case 32: return launch_kernel<true, 32>(grid, kThreadsFused, L, mp, md, dense, out, F, D, B, out_cols, KH, ns,
+                                            status, ga, stream, who);
+    default: return launch_kernel<true, 0>(grid, kThreadsFused, L, mp, md, dense, out, F, D, B, out_cols, KH, ns,
+                                           status, ga, stream, who);
     }
-    return check_launch("interact_tc_kernel");
 }
 
 dlrm_status tc_interact_fwd(const void* dense, const void* pooled, int F, int D, int B, void* out,
