@@ -59,6 +59,26 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p)
     return r;
 }
 
+// 4-byte read-only load issued where it is written: volatile, so the compiler
+// neither sinks it to its first use nor reorders it with other volatile loads
+// (used to start index reads a pipeline step ahead of their use).
+__device__ __forceinline__ int ldg_early_s32(const int32_t* p)
+{
+    int r;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// 16-byte read-only load that allocates in L1 (gathers of Zipf-hot rows).
+__device__ __forceinline__ uint4 ldg_nc_l1_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // 16-byte streaming store (evict-first: outputs are not re-read by this kernel).
 __device__ __forceinline__ void stg_cs_v4(void* p, uint4 v)
 {

@@ -104,7 +104,7 @@ __device__ __forceinline__ uint4 pool_bag(const T* __restrict__ tables, const in
         }
         uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = src[u] ? ldg_nc_v4(src[u]) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < U; ++u) v[u] = src[u] ? ldg_nc_l1_v4(src[u]) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (src[u]) acc_chunk<T>(acc, v[u]);
@@ -187,7 +187,7 @@ emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ 
             for (int u = 0; u < U; ++u) {
                 const int src_lane = k0 + u * RPI + sub;
                 const int64_t r = __shfl_sync(0xffffffffu, row, src_lane);
-                v[u] = (r >= 0 && active) ? ldg_nc_v4(tables + r * D + (int64_t)cl * V) : make_uint4(0, 0, 0, 0);
+                v[u] = (r >= 0 && active) ? ldg_nc_l1_v4(tables + r * D + (int64_t)cl * V) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {

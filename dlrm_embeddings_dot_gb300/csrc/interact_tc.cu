@@ -26,9 +26,9 @@
 //               into a shared output row, coalesced 16-byte stores.
 // Fused variant (dlrm_emb_interact_fwd, inference): each sample slot of a
 // tile is filled by one gather warp straight from the table, so the pooled
-// tensor never goes to HBM.  Twelve gather warps (warp 0 and warps 6..16, in
-// teams of four) fill three tiles at once with 16-byte register loads: a
-// table row is only 256 bytes, and the TMA engine's rate for such small row
+// tensor never goes to HBM.  Eight gather warps (warp 0 and warps 6..12, in
+// teams of four) fill two tiles at once with 16-byte register loads: a table
+// row is only 256 bytes, and the TMA engine's rate for such small row
 // gathers (tile::gather4) is several times below what the warps reach.
 // Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 overlap the
 // epilogue of tile i.  Every mbarrier wait is bounded; on timeout the kernel
@@ -52,10 +52,12 @@ constexpr int kKBlockBytes = kEBytes + kDBytes;   // 18 KB (multiple of 1 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;
 constexpr int kThreads = 192;
-constexpr int kTeams = 3;                         // fused: tiles gathered at once, four warps each
+constexpr int kTeams = 2;                         // fused: tiles gathered at once, four warps each
 constexpr int kThreadsFused = (5 + kGroup * kTeams) * 32;   // + gather warps 6.. (warp 0 gathers too)
 constexpr int kGatherU = 13;                      // fused: 16-byte row loads in flight per lane
 constexpr int kMaxStages = 8;
+constexpr int kFusedStages = 4;
+constexpr int kSqRow = 17;                        // words per row of the epilogue's product square
 constexpr int kSmemLimit = 232448;                // 227 KB opt-in per block
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
 
@@ -138,6 +140,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Two floats as one word of round-to-nearest halves (a in the low half).
+__device__ __forceinline__ uint32_t h2_bits(float a, float b)
+{
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -204,7 +213,7 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32], uint32_t& x)
 }
 
 struct Layout {
-    int stage_bytes, ns, out_bytes;
+    int stage_bytes, ns, sq_bytes, tri_bytes;
     size_t smem;
 };
 
@@ -213,8 +222,10 @@ __host__ __device__ inline Layout make_layout(int KH, int P, int ns)
     Layout L;
     L.stage_bytes = KH * kKBlockBytes;
     L.ns = ns;
-    L.out_bytes = (kGroup * P * 2 + 15) / 16 * 16;
-    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.out_bytes + (2 * ns + 4) * 8 + 16;
+    L.sq_bytes = kGroup * kSlot * kSqRow * 4;
+    L.tri_bytes = (kSlot * (kSlot + 1) / 2 + 7) / 8 * 16;
+    L.smem = 1024 + (size_t)ns * L.stage_bytes + L.sq_bytes + L.tri_bytes + (2 * ns + 4) * 8 + 16;
+    (void)P;
     return L;
 }
 
@@ -242,8 +253,11 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const Layout L = make_layout(KH, P, NS);
     uint8_t* stages = smem;
-    __half* ostage = reinterpret_cast<__half*>(smem + (size_t)NS * L.stage_bytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * L.stage_bytes + L.out_bytes);
+    // epilogue: per sample a 32 x kSqRow-word square of its products as
+    // halves, and the triangle's offsets into it in output order
+    uint32_t* square = reinterpret_cast<uint32_t*>(smem + (size_t)NS * L.stage_bytes);
+    uint16_t* tri = reinterpret_cast<uint16_t*>(square + L.sq_bytes / 4);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * L.stage_bytes + L.sq_bytes + L.tri_bytes);
     uint64_t* empty = full + NS;
     uint64_t* tfull = empty + NS;
     uint64_t* tempty = tfull + 2;
@@ -276,7 +290,20 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             for (int x = threadIdx.x; x < (kDenseRows - kGroup) * 128 / 16; x += nthreads)
                 z[x] = make_uint4(0, 0, 0, 0);
         }
-    for (int x = threadIdx.x; x < kGroup * P; x += nthreads) ostage[x] = __float2half_rn(0.f);
+    // Output pair k = i (i + 1) / 2 + j (0 <= j <= i < F) sits at halfword
+    // i * 2 kSqRow + j of the square; tri[k] holds that offset, 0xffff (a
+    // zero half) past the end, up to a multiple of 8 pairs.
+    const int T = F * (F + 1) / 2;
+    const int T8 = (T + 7) / 8 * 8;
+    for (int k = threadIdx.x; k < T8; k += nthreads) {
+        uint16_t off = 0xffffu;
+        if (k < T) {
+            int i = 0;
+            while ((i + 1) * (i + 2) / 2 <= k) ++i;
+            off = (uint16_t)(i * 2 * kSqRow + (k - i * (i + 1) / 2));
+        }
+        tri[k] = off;
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -335,8 +362,8 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                 s0 = e0 = 0;
                 const int64_t b = tile * kGroup + sm;
                 if (lane < F && tile < ntiles && b < B) {
-                    s0 = __ldg(ga.offsets + (int64_t)lane * B + b);
-                    e0 = __ldg(ga.offsets + (int64_t)lane * B + b + 1);
+                    s0 = ldg_early_s32(ga.offsets + (int64_t)lane * B + b);
+                    e0 = ldg_early_s32(ga.offsets + (int64_t)lane * B + b + 1);
                 }
             };
             auto clamp_bounds = [&](int& s0, int& e0) {   // into [0, nnz], flagging malformed lists
@@ -370,7 +397,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             // 32 % cpr == 0 (D = 64, 128, 256) the column is fixed per lane.
             const int Dr = kCpr > 0 ? 8 * kCpr : D;
             auto chunk_of = [&](int k, int& e, int& c) {
-                if constexpr (kCpr > 0 && kWarp % kCpr == 0) {
+                if constexpr (kCpr > 0 && kWarp % (kCpr > 0 ? kCpr : 1) == 0) {
                     e = lane / kCpr + k * (kWarp / kCpr);
                     c = lane % kCpr;
                 } else {
@@ -394,7 +421,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                 const uint32_t row0 = resolve(a0, z0, idx0);
                 // in flight together: next tile's index, the bounds two tiles on, this tile's rows
                 int idx1 = 0, a2, z2;
-                if (z1 - a1 == 1) idx1 = __ldg(ga.indices + a1);
+                if (z1 - a1 == 1) idx1 = ldg_early_s32(ga.indices + a1);
                 load_bounds(tile + 2 * tstride, a2, z2);
                 const int64_t b = tile * kGroup + sm;
                 uint8_t* sb = stages + (size_t)stage * L.stage_bytes;
@@ -413,7 +440,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                         v[u] = make_uint4(0, 0, 0, 0);
                         if (e < F && src != kRowMulti) {
                             store |= 1u << u;
-                            if (src != kRowZero) v[u] = ldg_nc_v4(ga.tables + (size_t)src * Dr + 8 * c);
+                            if (src != kRowZero) v[u] = ldg_nc_l1_v4(ga.tables + (size_t)src * Dr + 8 * c);
                         }
                     }
                     if (k0 == 0) {
@@ -513,11 +540,22 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
     } else if (warp < 6) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;                     // TMEM lane quarter == sample in tile
-        __half* os = ostage + q * P;
+        uint32_t* sq = square + q * kSlot * kSqRow;
+        const __half* sqh = reinterpret_cast<const __half*>(sq);
+        // The sample's dense row is copied to the output from registers, loaded
+        // one tile ahead so its latency overlaps the wait for the accumulator.
+        auto load_dense = [&](int tile) {
+            const int64_t b = (int64_t)tile * kGroup + q;
+            return (tile < ntiles && b < B && lane < D / 8) ? ldg_nc_v4(dense + b * D + 8 * lane)
+                                                             : make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 dnext = load_dense(blockIdx.x);
         int it = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int buf = it & 1;
             const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+            const uint4 dcur = dnext;
+            dnext = load_dense(tile + gridDim.x);
             if (!mbar_wait(&tfull[buf], bph, abort_flag)) break;
             __syncwarp();
             tc_fence_after();
@@ -532,22 +570,41 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             if (lane == 0) mbar_arrive(&tempty[buf]);
             const int b = tile * kGroup + q;
             if (b < B) {
-                const __half* drow = dense + (int64_t)b * D;
-                for (int c = lane; c < D / 8; c += kWarp)
-                    *reinterpret_cast<uint4*>(os + 8 * c) = ldg_nc_v4(drow + 8 * c);
-                if (lane < F) {
-                    // row i = lane + 1 of Z: pairs (i, 0) .. (i, i-1)
-                    const int base = D + (lane + 1) * lane / 2;
-                    os[base] = __float2half_rn(__uint_as_float(dd));
+                // Lane i holds row i + 1 of Z against rows 0..31: h[0] = e_i . d,
+                // h[j] = e_i . e_{j-1}.  It writes them as halves to row i of the
+                // square (17-word rows: conflict-free), then the warp reads the
+                // triangle back in output order and stores it coalesced.
+                uint32_t* srow = sq + lane * kSqRow;
+                srow[0] = h2_bits(__uint_as_float(dd), __uint_as_float(v[0]));
 #pragma unroll
-                    for (int j = 1; j < 32; ++j)
-                        if (j <= lane) os[base + j] = __float2half_rn(__uint_as_float(v[j - 1]));
-                }
+                for (int m = 1; m < 16; ++m)
+                    srow[m] = h2_bits(__uint_as_float(v[2 * m - 1]), __uint_as_float(v[2 * m]));
                 __syncwarp();
                 __half* orow = out + (int64_t)b * P;
-                for (int c = lane; c < P / 8; c += kWarp)
-                    stg_cs_v4(orow + 8 * c, *reinterpret_cast<const uint4*>(os + 8 * c));
-                __syncwarp();
+                if (lane < D / 8) stg_cs_v4(orow + 8 * lane, dcur);
+                // lane: output pairs 8 (lane + 32 m) .. + 7, one 16-byte store each
+                constexpr int kTriIters = (kSlot * (kSlot + 1) / 2 + 8 * kWarp - 1) / (8 * kWarp);
+#pragma unroll
+                for (int m = 0; m < kTriIters; ++m) {
+                    const int k = 8 * (lane + kWarp * m);
+                    if (k < T) {
+                        const uint4 o = *reinterpret_cast<const uint4*>(tri + k);
+                        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+                        uint32_t hw[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const uint32_t o0 = ow[h] & 0xffffu, o1 = ow[h] >> 16;
+                            const uint32_t lo = o0 == 0xffffu ? 0u : __half_as_ushort(sqh[o0]);
+                            const uint32_t hi = o1 == 0xffffu ? 0u : __half_as_ushort(sqh[o1]);
+                            hw[h] = lo | (hi << 16);
+                        }
+                        stg_cs_v4(orow + D + k, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                    }
+                }
+                // zero padding past the triangle (rounded up to 8 pairs)
+                for (int c = D + ((T + 7) & ~7) + 8 * lane; c < P; c += 8 * kWarp)
+                    stg_cs_v4(orow + c, make_uint4(0u, 0u, 0u, 0u));
+                __syncwarp();   // the square is rewritten for the next tile
             }
         }
         (void)W;
@@ -612,7 +669,9 @@ dlrm_status tc_launch(const void* dense, const void* pooled, const GatherArgs& g
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(DLRM_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", who);
     const int KH = D / kKB;
-    int ns = kMaxStages;
+    // The fused kernel keeps to kFusedStages so that about 90 KB of the SM's
+    // 256 KB stays L1: the Zipf-hot table rows then hit in L1.
+    int ns = pooled ? kMaxStages : kFusedStages;
     while (ns > 1 && make_layout(KH, out_cols, ns).smem > (size_t)kSmemLimit) --ns;
     const Layout L = make_layout(KH, out_cols, ns);
     if (ns < 2 || L.smem > (size_t)kSmemLimit)
