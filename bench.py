@@ -515,6 +515,10 @@ CONFIGS = {
                  "then backward + SGD from an N(0,1e-2) grad_pooled",
     "large-tables": "26 fp16 tables D=128 (three of 40M rows, 23 log-uniform 10..4e6), single-hot Zipf 1.05; "
                     "forward at batch 1K..1M",
+    "default-fwd-uniform": "control: the default-fwd shapes with uniform indices (no Zipf reuse, so algorithmic "
+                           "bytes ~ DRAM bytes)",
+    "multi-hot-uniform": "control: the multi-hot shapes with uniform indices (no Zipf reuse); forward lookup, then "
+                         "backward + SGD",
 }
 
 
@@ -546,12 +550,13 @@ def run_config(args, name) -> None:
     for B in batches:
         if name in ("tiny", "tiny-train"):
             w = inputs.tiny_slice(seed=0, train=(name == "tiny-train"))
-        elif name == "default-fwd":
-            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD)
+        elif name in ("default-fwd", "default-fwd-uniform"):
+            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD,
+                                    uniform_indices=name.endswith("-uniform"))
         elif name == "train-64k":
             w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True)
-        elif name == "multi-hot":
-            w = inputs.multi_hot(B=B if B != BATCH else 16384)
+        elif name in ("multi-hot", "multi-hot-uniform"):
+            w = inputs.multi_hot(B=B if B != BATCH else 16384, uniform_indices=name.endswith("-uniform"))
         else:
             w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, rows=inputs.large_tables_rows())
         tt = torch.float16 if w.dtype == inputs.F16 else torch.float32
@@ -563,15 +568,16 @@ def run_config(args, name) -> None:
         out = torch.empty(Bw, P, dtype=tt, device=dev)
         ops = [("emb_fwd", lambda: dl.dlrm_emb_fwd(tab, rb, F, D, Bw, idx, off, pooled, status=status,
                                                    stream=stream))]
-        if name != "multi-hot":
+        multi = name.startswith("multi-hot")
+        if not multi:
             ops.append(("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, Bw, out, P,
                                                                      status=status, stream=stream)))
-        train = name in ("tiny-train", "train-64k", "multi-hot")
+        train = name in ("tiny-train", "train-64k") or multi
         if train:
             gp = torch.empty(Bw, F, D, device=dev)
             ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
                              device=dev)
-            if name == "multi-hot":
+            if multi:
                 gp.normal_(0.0, 1e-2)
             else:
                 go = torch.from_numpy(w.grad_out).to(dev)

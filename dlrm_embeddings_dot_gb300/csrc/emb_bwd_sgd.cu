@@ -19,7 +19,8 @@
 //  4. fixup: one warp per run that crossed a chunk edge finds the run's last
 //     chunk (32 chunks per probe), adds its partial sums in chunk order and
 //     updates the row; runs of more than 64 pieces are handed to one block
-//     each (8 warps add interleaved pieces, then the 8 sums in warp order).
+//     each (16 warps add 16 contiguous slices of pieces, then the 16 sums in
+//     slice order).  A lane keeps up to 4 partial-sum loads in flight.
 // Every order of summation is fixed by the data, so results are bitwise
 // reproducible.  Workspace layout (256-byte aligned pieces):
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
@@ -38,7 +39,7 @@ constexpr int kSortThreads = 256;
 constexpr int kItems = 8;
 constexpr int kTile = kSortThreads * kItems;   // 2048 keys per tile
 constexpr int kChunk = 32;                     // positions per segment chunk
-constexpr int kFixThreads = 256;
+constexpr int kFixThreads = 512;
 
 struct Ws {
     uint32_t *keys[2], *vals[2];
@@ -88,8 +89,8 @@ keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* _
     const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
     const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
     for (int64_t g = group; g < nbags; g += ngroups) {   // g = t*B + b (feature-major, like offsets)
-        const int t = (int)(g / B);
-        const int b = (int)(g - (int64_t)t * B);
+        const int t = (int)((uint32_t)g / (uint32_t)B);   // F * B < 2^31
+        const int b = (int)g - t * B;
         const int64_t base = row_base[t], n = row_base[t + 1] - base;
         const uint32_t val = (uint32_t)((int64_t)b * F + t);
         int64_t s = offsets[g], e = offsets[g + 1];
@@ -357,6 +358,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
 
 // ----------------------------------------------------------------- 4. fixup
 constexpr int kLongPieces = 64;   // runs with more chunk pieces go to a block-per-run pass
+constexpr int kFixRegs = 4;       // float4 partial-sum loads a lane has in flight
 
 // Last chunk a run that starts in chunk c0 (and continues past it) touches:
 // chunks c0+1, c0+2, ... are probed 32 at a time (keys are sorted, so the run
@@ -416,10 +418,11 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int64_t j = 0; j < pieces; j += 4) {
-            float4 v[4][MC];
+        constexpr int kFixBatch = kFixRegs / MC > 0 ? kFixRegs / MC : 1;   // pieces in flight
+        for (int64_t j = 0; j < pieces; j += kFixBatch) {
+            float4 v[kFixBatch][MC];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kFixBatch; ++u) {
                 const int64_t slot = (j + u) == 0 ? 2 * c0 + 1 : 2 * (c0 + j + u);
 #pragma unroll
                 for (int m = 0; m < MC; ++m) {
@@ -429,7 +432,7 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < kFixBatch; ++u)
                 if (j + u < pieces)
 #pragma unroll
                     for (int m = 0; m < MC; ++m) {
@@ -443,8 +446,9 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
     }
 }
 
-// One block per long split run: warp w adds pieces w, w+8, ... in order, then
-// warp 0 adds the 8 warp sums in warp order and applies the update.
+// One block per long split run: warp w adds the w-th of kW contiguous slices
+// of the run's pieces in order (kFixBatch loads in flight), then warp 0 adds
+// the kW slice sums in slice order and applies the update.
 template <int MC>
 __global__ void __launch_bounds__(kFixThreads)
 fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
@@ -470,19 +474,30 @@ fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __r
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int64_t j = warp; j < pieces; j += kW) {
-            const int64_t slot = j == 0 ? 2 * c0 + 1 : 2 * (c0 + j);
+        const int64_t j0 = pieces * warp / kW, j1 = pieces * (warp + 1) / kW;
+        constexpr int kFixBatch = kFixRegs / MC > 0 ? kFixRegs / MC : 1;   // pieces in flight
+        for (int64_t j = j0; j < j1; j += kFixBatch) {
+            float4 v[kFixBatch][MC];
 #pragma unroll
-            for (int m = 0; m < MC; ++m) {
-                const int col = lane + m * kWarp;
-                if (col < c4) {
-                    const float4 v = reinterpret_cast<const float4*>(partials + slot * D)[col];
-                    acc[m].x += v.x;
-                    acc[m].y += v.y;
-                    acc[m].z += v.z;
-                    acc[m].w += v.w;
+            for (int u = 0; u < kFixBatch; ++u) {
+                const int64_t slot = (j + u) == 0 ? 2 * c0 + 1 : 2 * (c0 + j + u);
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    const int col = lane + m * kWarp;
+                    v[u][m] = (j + u < j1 && col < c4) ? reinterpret_cast<const float4*>(partials + slot * D)[col]
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+#pragma unroll
+            for (int u = 0; u < kFixBatch; ++u)
+                if (j + u < j1)
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        acc[m].x += v[u][m].x;
+                        acc[m].y += v[u][m].y;
+                        acc[m].z += v[u][m].z;
+                        acc[m].w += v[u][m].w;
+                    }
         }
 #pragma unroll
         for (int m = 0; m < MC; ++m) {
