@@ -21,6 +21,7 @@ DLRM_ERR_INVALID_ARG = 1
 DLRM_ERR_UNSUPPORTED = 2
 DLRM_ERR_CUDA = 3
 DLRM_ERR_WORKSPACE = 4
+DLRM_ERR_NO_FIT = 5
 DLRM_F32 = 0
 DLRM_F16 = 1
 DLRM_FLAG_HASH_INDICES = 1
@@ -66,6 +67,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_last_error.argtypes = []
     L.dlrm_last_error.restype = ctypes.c_char_p
     L.dlrm_synth_fill_uniform.argtypes = [_P, _I, ctypes.c_uint64, _I64, _I64, ctypes.c_double, _P]
+    L.dlrm_plan_tables.argtypes = [_I, _P, _I, _P, _P]
+    L.dlrm_batch_shard.argtypes = [_I64, _I, _I, _P, _P]
+    L.dlrm_a2a_layout.argtypes = [_I, _P, _I64, _I, _I, _I64, _P, _P, _P, _P, _P]
+    for f in ("dlrm_plan_tables", "dlrm_batch_shard", "dlrm_a2a_layout"):
+        getattr(L, f).restype = _I
     for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core", "dlrm_emb_interact_fwd",
               "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
         getattr(L, f).restype = _I
@@ -178,3 +184,37 @@ def dlrm_synth_fill_uniform(dst, seed, first_elem, amplitude=0.05, stream=None):
     rc = load().dlrm_synth_fill_uniform(_ptr(dst), _dtype_code(dst), seed & (2**64 - 1), first_elem,
                                         dst.numel(), amplitude, _stream(stream))
     _check("dlrm_synth_fill_uniform", rc)
+
+
+# ---------------------------------------------------------------- host planning
+# Host-only calls (include/dlrm_plan.h): lists in, lists out, no GPU.
+
+def _host_i64(values):
+    return (ctypes.c_int64 * max(len(values), 1))(*values)
+
+
+def dlrm_plan_tables(table_bytes, gpu_free_bytes) -> list[int]:
+    """GPU of each table under the pages' placement heuristic (bottom MLP on GPU 0)."""
+    n = len(table_bytes)
+    dev = (ctypes.c_int * max(n, 1))()
+    rc = load().dlrm_plan_tables(n, _host_i64(table_bytes), len(gpu_free_bytes), _host_i64(gpu_free_bytes), dev)
+    _check("dlrm_plan_tables", rc)
+    return list(dev[:n])
+
+
+def dlrm_batch_shard(batch, n_ranks, rank) -> tuple[int, int]:
+    first, count = ctypes.c_int64(), ctypes.c_int64()
+    rc = load().dlrm_batch_shard(batch, n_ranks, rank, ctypes.byref(first), ctypes.byref(count))
+    _check("dlrm_batch_shard", rc)
+    return first.value, count.value
+
+
+def dlrm_a2a_layout(table_device, batch, n_ranks, rank, row_elems):
+    """(send_counts, send_displs, recv_counts, recv_displs, slot_table) of the forward exchange."""
+    n = len(table_device)
+    arrs = [(ctypes.c_int64 * n_ranks)() for _ in range(4)]
+    slots = (ctypes.c_int * max(n, 1))()
+    rc = load().dlrm_a2a_layout(n, (ctypes.c_int * max(n, 1))(*table_device), batch, n_ranks, rank, row_elems,
+                                *arrs, slots)
+    _check("dlrm_a2a_layout", rc)
+    return tuple(list(a) for a in arrs) + (list(slots[:n]),)

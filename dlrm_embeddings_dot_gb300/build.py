@@ -1,8 +1,8 @@
 """Build the CUDA library ``libdlrm_gb300.so`` (sm_103a) in the package directory.
 
-Each ``csrc/*.cu`` file is compiled by nvcc in parallel and linked into one
-shared object exporting the C ABI of ``include/dlrm.h`` and
-``include/dlrm_synth.h``.  The CUDA runtime is linked statically, so the
+Each ``csrc/*.cu`` (and host-only ``csrc/*.cpp``) file is compiled by nvcc
+in parallel and linked into one shared object exporting the C ABI of
+``include/*.h``.  The CUDA runtime is linked statically, so the
 library needs only the driver at run time.
 """
 
@@ -36,7 +36,7 @@ def _nvcc() -> str:
 
 
 def _sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _digest() -> str:
@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")

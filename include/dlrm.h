@@ -52,7 +52,8 @@ typedef enum {
     DLRM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, out_cols < W, ... */
     DLRM_ERR_UNSUPPORTED = 2,   /* a legal request this library does not implement */
     DLRM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message says which) */
-    DLRM_ERR_WORKSPACE = 4      /* workspace smaller than the size query returned */
+    DLRM_ERR_WORKSPACE = 4,     /* workspace smaller than the size query returned */
+    DLRM_ERR_NO_FIT = 5         /* table placement: a table does not fit on its GPU */
 } dlrm_status;
 
 typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
