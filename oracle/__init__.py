@@ -74,6 +74,7 @@ def _declare(L) -> None:
                                       ctypes.c_int, _P, ctypes.c_int]
     L.oracle_interact_bwd.argtypes = [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, _P, _P]
+    L.oracle_mlp_fwd.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]
     L.oracle_emb_bwd_sgd.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P,
                                      ctypes.c_int64, _P, ctypes.c_float, ctypes.c_uint, _P,
                                      _P, _P]
@@ -175,3 +176,22 @@ def emb_bwd_sgd(tables, row_base, F, D, B, indices, offsets, grad_pooled, lr, fl
     if rc:
         raise ValueError("oracle_emb_bwd_sgd rejected its arguments")
     return tables, int(status[0]), sk[:nnz], sv[:nnz]
+
+
+def mlp_fwd(x, weights, biases, half_io=False):
+    """Bottom MLP: relu(W h + b) per layer, double accumulation (see oracle.c).
+
+    x: [B][K0] float32; weights[l]: [N_l][K_l]; biases[l]: [N_l].  Returns
+    float64 [B][N_last] (binary16 values when half_io)."""
+    x = _c(x, np.float32)
+    B = x.shape[0]
+    dims = [x.shape[1]] + [int(w.shape[0]) for w in weights]
+    for l, w in enumerate(weights):
+        assert w.shape == (dims[l + 1], dims[l]) and biases[l].shape == (dims[l + 1],)
+    W = _c(np.concatenate([np.asarray(w, np.float32).reshape(-1) for w in weights]))
+    bb = _c(np.concatenate([np.asarray(b, np.float32) for b in biases]))
+    d = _c(np.array(dims, dtype=np.int32))
+    out = np.zeros((B, dims[-1]), dtype=np.float64)
+    rc = lib().oracle_mlp_fwd(_ptr(x), B, len(weights), _ptr(d), _ptr(W), _ptr(bb), int(bool(half_io)), _ptr(out))
+    assert rc == 0, rc
+    return out

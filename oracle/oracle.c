@@ -24,6 +24,11 @@
  *   - the optimizer is plain SGD, w := w - lr * g, g summed over every
  *     occurrence of the row in the batch (duplicates count each time).
  *
+ *   - §Model architecture / --bottom_mlp_sizes 512,256,128: the bottom MLP is
+ *     a chain of linear layers, each followed by a ReLU (the last included);
+ *     under mixed precision (--amp, §Mixed precision training) its tensors
+ *     are fp16 while the bias and the accumulation stay fp32 or wider.
+ *
  * Arithmetic: every sum is accumulated in double and rounded once to the
  * output type (fp16 by round-to-nearest-even, converter below).  Build with
  * -ffp-contract=off so that x86 and Arm hosts give identical doubles.
@@ -311,5 +316,54 @@ int oracle_emb_bwd_sgd(float* tables, const int64_t* row_base, int F, int D, int
         p = q;
     }
     free(key); free(val); free(tk); free(tv); free(g);
+    return OR_OK;
+}
+
+/* Bottom MLP forward ("DLRM For PyTorch", §Model architecture): for layers
+ * l = 0..L-1, h_{l+1}[j] = max(0, sum_k W_l[j][k] h_l[k] + b_l[j]), h_0 = x.
+ * dims[0..L] are the widths; W_all holds the layers' [dims[l+1]][dims[l]]
+ * weights one after another, b_all their biases.  Sums in double.  With
+ * half_io, x, the weights and every layer's output are rounded to binary16
+ * (the tensors of the mixed-precision recipe; bias and accumulation wider).
+ * out: double [B][dims[L]]. */
+int oracle_mlp_fwd(const float* x, int B, int L, const int* dims, const float* W_all, const float* b_all,
+                   int half_io, double* out)
+{
+    if (B < 0 || L < 1) return OR_EINVAL;
+    int wmax = 0;
+    for (int l = 0; l <= L; ++l) {
+        if (dims[l] < 1) return OR_EINVAL;
+        if (dims[l] > wmax) wmax = dims[l];
+    }
+    double* h = (double*)malloc(sizeof(double) * wmax);
+    double* nh = (double*)malloc(sizeof(double) * wmax);
+    if (!h || !nh) { free(h); free(nh); return OR_EINVAL; }
+    for (int b = 0; b < B; ++b) {
+        for (int k = 0; k < dims[0]; ++k) {
+            double v = (double)x[(int64_t)b * dims[0] + k];
+            h[k] = half_io ? oracle_f16_to_f64(oracle_f64_to_f16(v)) : v;
+        }
+        int64_t woff = 0, boff = 0;
+        for (int l = 0; l < L; ++l) {
+            const int K = dims[l], N = dims[l + 1];
+            for (int j = 0; j < N; ++j) {
+                double acc = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    double w = (double)W_all[woff + (int64_t)j * K + k];
+                    if (half_io) w = oracle_f16_to_f64(oracle_f64_to_f16(w));
+                    acc += w * h[k];
+                }
+                acc += (double)b_all[boff + j];
+                if (acc < 0.0) acc = 0.0;
+                nh[j] = half_io ? oracle_f16_to_f64(oracle_f64_to_f16(acc)) : acc;
+            }
+            for (int j = 0; j < N; ++j) h[j] = nh[j];
+            woff += (int64_t)N * K;
+            boff += N;
+        }
+        for (int j = 0; j < dims[L]; ++j) out[(int64_t)b * dims[L] + j] = h[j];
+    }
+    free(h);
+    free(nh);
     return OR_OK;
 }
