@@ -70,6 +70,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_plan_tables.argtypes = [_I, _P, _I, _P, _P]
     L.dlrm_batch_shard.argtypes = [_I64, _I, _I, _P, _P]
     L.dlrm_a2a_layout.argtypes = [_I, _P, _I64, _I, _I, _I64, _P, _P, _P, _P, _P]
+    L.dlrm_bottom_mlp_workspace_size.argtypes = [_I, _I, _P]
+    L.dlrm_bottom_mlp_workspace_size.restype = ctypes.c_size_t
+    L.dlrm_bottom_mlp_fwd.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+    L.dlrm_bottom_mlp_fwd.restype = _I
     for f in ("dlrm_plan_tables", "dlrm_batch_shard", "dlrm_a2a_layout"):
         getattr(L, f).restype = _I
     for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core", "dlrm_emb_interact_fwd",
@@ -218,3 +222,23 @@ def dlrm_a2a_layout(table_device, batch, n_ranks, rank, row_elems):
                                 *arrs, slots)
     _check("dlrm_a2a_layout", rc)
     return tuple(list(a) for a in arrs) + (list(slots[:n]),)
+
+
+# ---------------------------------------------------------------- bottom MLP
+def _dims_arr(dims):
+    return (ctypes.c_int * len(dims))(*[int(d) for d in dims])
+
+
+def dlrm_bottom_mlp_workspace_size(B, dims) -> int:
+    return int(load().dlrm_bottom_mlp_workspace_size(B, len(dims) - 1, _dims_arr(dims)))
+
+
+def dlrm_bottom_mlp_fwd(x, dims, weights, biases, out, workspace, status=None, stream=None):
+    """out (fp16 [B][dims[-1]]) = the bottom MLP of x (fp32 [B][dims[0]]); see include/dlrm_mlp.h.
+
+    weights / biases are the packed device buffers (inputs.mlp_pack lays them out)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dlrm_bottom_mlp_fwd(_ptr(x), x.shape[0], len(dims) - 1, _dims_arr(dims), _ptr(weights),
+                                    _ptr(biases), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status),
+                                    _stream(stream))
+    _check("dlrm_bottom_mlp_fwd", rc)

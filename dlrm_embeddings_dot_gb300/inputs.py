@@ -382,3 +382,29 @@ class Compact:
         self.indices = (np.concatenate(parts) if parts else np.zeros(0, np.int64)).astype(np.int32)
         self.dense = (w.dense.astype(np.float16) if dt == F16 else w.dense.astype(np.float32))[samples]
         self.grad_out = None if w.grad_out is None else w.grad_out[samples]
+
+
+def mlp_layers(dims, seed: int = 0):
+    """Xavier-uniform fp16 weights [N][K] and small fp32 biases for a bottom MLP of widths dims."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 17]))
+    W, b = [], []
+    for l in range(len(dims) - 1):
+        K, N = dims[l], dims[l + 1]
+        lim = np.sqrt(6.0 / (K + N))
+        W.append(rng.uniform(-lim, lim, size=(N, K)).astype(np.float16))
+        b.append(rng.uniform(-0.1, 0.1, size=N).astype(np.float32))
+    return W, b
+
+
+def mlp_pack(weights, biases):
+    """The packed operands of dlrm_bottom_mlp_fwd: fp16 weights, each layer
+    [N][round_up(K, 8)] with zero pad columns, one after another; fp32 biases
+    one after another."""
+    parts = []
+    for w in weights:
+        N, K = w.shape
+        Kp = (K + 7) // 8 * 8
+        pw = np.zeros((N, Kp), dtype=np.float16)
+        pw[:, :K] = w
+        parts.append(pw.reshape(-1))
+    return np.concatenate(parts), np.concatenate([np.asarray(b, np.float32) for b in biases])
