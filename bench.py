@@ -373,7 +373,7 @@ def run_ours(args) -> None:
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": ncu_traffic(kernel_names[dom]),
+            "traffic": ncu_traffic(dom if dom == "emb_bwd_sgd" else kernel_names[dom]),
             "algorithmic_bytes_per_launch": alg[dom], "launch_ms": round(op_ms[dom], 4)}
 
     line = {
