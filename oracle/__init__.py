@@ -74,6 +74,8 @@ def _declare(L) -> None:
                                       ctypes.c_int, _P, ctypes.c_int]
     L.oracle_interact_bwd.argtypes = [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, _P, _P]
+    L.oracle_round_f16.argtypes = [_P, _P, ctypes.c_int64]
+    L.oracle_round_f16.restype = None
     L.oracle_mlp_fwd.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]
     L.oracle_emb_bwd_sgd.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P,
                                      ctypes.c_int64, _P, ctypes.c_float, ctypes.c_uint, _P,
@@ -195,3 +197,29 @@ def mlp_fwd(x, weights, biases, half_io=False):
     rc = lib().oracle_mlp_fwd(_ptr(x), B, len(weights), _ptr(d), _ptr(W), _ptr(bb), int(bool(half_io)), _ptr(out))
     assert rc == 0, rc
     return out
+
+
+# ------------------------------------------------------ mixed precision (AMP)
+# "DLRM For PyTorch", §Mixed precision training: fp16 tensors for the
+# interaction, fp32 master tables, static loss scaling.  Each result below is
+# the exact (double) value of the definition, rounded once to binary16.
+
+def round_f16(x):
+    """Doubles rounded to binary16 (ties to even), as np.float16."""
+    x = _c(x, np.float64)
+    bits = np.zeros(x.shape, dtype=np.uint16)
+    lib().oracle_round_f16(_ptr(x), _ptr(bits), x.size)
+    return bits.view(np.float16)
+
+
+def emb_fwd_f16out(tables, row_base, F, D, B, indices, offsets, flags=0):
+    """Pooling of fp32 master rows, delivered as fp16 (summed in double, rounded once)."""
+    pooled, status = emb_fwd(np.asarray(tables, np.float64), row_base, F, D, B, indices, offsets, flags)
+    return round_f16(pooled), status
+
+
+def interact_bwd_f16(grad_out, dense, pooled):
+    """Interaction backward of fp16 tensors: exact sums, gradients rounded once to fp16."""
+    gd, gp = interact_bwd(np.asarray(grad_out, np.float64), np.asarray(dense, np.float64),
+                          np.asarray(pooled, np.float64))
+    return round_f16(gd), round_f16(gp)

@@ -367,3 +367,11 @@ int oracle_mlp_fwd(const float* x, int B, int L, const int* dims, const float* W
     free(nh);
     return OR_OK;
 }
+
+/* Rounds n doubles to binary16 (round to nearest, ties to even) with the
+ * converter above: the single rounding of the mixed-precision tensors
+ * ("DLRM For PyTorch", §Mixed precision training). */
+void oracle_round_f16(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_f16(x[i]);
+}
