@@ -518,6 +518,9 @@ CONFIGS = {
     "bottom-mlp": "bottom MLP 13 -> 512 -> 256 -> 128 (linear + ReLU, fp16 tensors, fp32 accumulate) on the "
                   "tensor cores, batch 65536, lognormal(0,1) dense features; and MLP + fused lookup/interaction "
                   "(the whole embedding-side forward from raw features)",
+    "train-64k-amp": "the 64K training step in mixed precision (the pages' --amp): fp32 master tables pooled to "
+                     "fp16, fp16 dense, tcgen05 interaction forward and backward, upstream gradient N(0,1e-2) "
+                     "scaled by the static loss scale 1024 in fp16, sparse SGD on the fp16 gradients with lr/1024",
     "default-fwd-uniform": "control: the default-fwd shapes with uniform indices (no Zipf reuse, so algorithmic "
                            "bytes ~ DRAM bytes)",
     "multi-hot-uniform": "control: the multi-hot shapes with uniform indices (no Zipf reuse); forward lookup, then "
@@ -562,6 +565,54 @@ def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> None:
         "device_status": int(status.item())}), flush=True)
 
 
+LOSS_SCALE = 1024.0
+
+
+def amp_step_ops(dl, w, torch, dev, stream, status, tab):
+    """The mixed-precision training step's four calls, on device buffers."""
+    F, D, B, P = w.F, w.D, w.B, w.out_cols
+    rb, idx, off = (torch.from_numpy(a).to(dev) for a in (w.row_base, w.indices, w.offsets))
+    dense = torch.from_numpy(w.dense.astype(np.float16)).to(dev)
+    g16 = torch.from_numpy((w.grad_out.astype(np.float64) * LOSS_SCALE).astype(np.float16)).to(dev)
+    pooled = torch.empty(B, F, D, dtype=torch.float16, device=dev)
+    out = torch.empty(B, P, dtype=torch.float16, device=dev)
+    gd = torch.empty(B, D, dtype=torch.float16, device=dev)
+    gp = torch.empty(B, F, D, dtype=torch.float16, device=dev)
+    ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8, device=dev)
+    lr = float(np.float32(w.lr / LOSS_SCALE))
+    return [
+        ("emb_fwd", lambda: dl.dlrm_emb_fwd(tab, rb, F, D, B, idx, off, pooled, flags=dl.DLRM_FLAG_POOLED_F16,
+                                            status=status, stream=stream)),
+        ("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)),
+        ("interact_bwd", lambda: dl.dlrm_interact_bwd_f16(g16, dense, pooled, F, D, B, P, gd, gp, status=status,
+                                                          stream=stream)),
+        ("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, B, idx, off, gp, lr, ws,
+                                                    flags=dl.DLRM_FLAG_GRAD_F16, status=status, stream=stream)),
+    ]
+
+
+def run_train_amp(args, dl, inputs, torch, dev, stream, status) -> None:
+    B = args.batch
+    w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True)
+    with torch.cuda.stream(stream):
+        tab = torch.empty(w.total_rows, w.D, dtype=torch.float32, device=dev)
+        dl.dlrm_synth_fill_uniform(tab, w.table_seed, 0, stream=stream)
+    torch.cuda.synchronize()
+    ops = amp_step_ops(dl, w, torch, dev, stream, status, tab)
+    per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
+    F, D, P, nnz = w.F, w.D, w.out_cols, w.nnz
+    alg = {"emb_fwd": nnz * (4 + 4 + D * 4) + B * F * D * 2,
+           "interact_fwd": B * (D * 2 + F * D * 2 + P * 2),
+           "interact_bwd": B * (P * 2 + D * 2 + F * D * 2 + D * 2 + F * D * 2),
+           "emb_bwd_sgd": nnz * (4 + 4 + D * 2)}
+    print(json.dumps({
+        "config": "train-64k-amp", "workload": CONFIGS["train-64k-amp"], "batch": B, "nnz": nnz,
+        "steps": args.steps, "ms_per_step": round(ms, 4), "step_samples_per_s": round(B / (ms / 1e3), 1),
+        "ops_ms": {k: round(v, 4) for k, v in per.items()},
+        "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
+        "device_status": int(status.item())}), flush=True)
+
+
 def run_config(args, name) -> None:
     """Measure one workload of the pages' configurations and print a JSON line."""
     import torch
@@ -575,6 +626,9 @@ def run_config(args, name) -> None:
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     if name == "bottom-mlp":
         run_bottom_mlp(args, dl, inputs, torch, dev, stream, status)
+        return
+    if name == "train-64k-amp":
+        run_train_amp(args, dl, inputs, torch, dev, stream, status)
         return
 
     def setup(w, tt):

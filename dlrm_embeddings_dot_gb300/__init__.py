@@ -22,6 +22,8 @@ DLRM_ERR_UNSUPPORTED = 2
 DLRM_ERR_CUDA = 3
 DLRM_ERR_WORKSPACE = 4
 DLRM_ERR_NO_FIT = 5
+DLRM_FLAG_POOLED_F16 = 2
+DLRM_FLAG_GRAD_F16 = 4
 DLRM_F32 = 0
 DLRM_F16 = 1
 DLRM_FLAG_HASH_INDICES = 1
@@ -56,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_interact_fwd_cuda_core.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I, _P]
     L.dlrm_emb_interact_fwd.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, _P, _I, ctypes.c_uint, _P, _P]
     L.dlrm_interact_bwd.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
+    L.dlrm_interact_bwd_f16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]
+    L.dlrm_interact_bwd_f16.restype = _I
     L.dlrm_emb_bwd_sgd_workspace_size.argtypes = [_I64, _I, _I64]
     L.dlrm_emb_bwd_sgd_workspace_size.restype = ctypes.c_size_t
     L.dlrm_emb_bwd_sgd.argtypes = [_P, _P, _I64, _I, _I, _I, _P, _P, _I64, _P, ctypes.c_float, _P,
@@ -154,6 +158,14 @@ def dlrm_interact_bwd(grad_out, dense, pooled, F, D, B, out_cols, grad_dense, gr
     rc = load().dlrm_interact_bwd(_ptr(grad_out), _ptr(dense), _ptr(pooled), _dtype_code(pooled), F, D, B,
                                   out_cols, _ptr(grad_dense), _ptr(grad_pooled), _stream(stream))
     _check("dlrm_interact_bwd", rc)
+
+
+def dlrm_interact_bwd_f16(grad_out, dense, pooled, F, D, B, out_cols, grad_dense, grad_pooled, status=None,
+                          stream=None):
+    """Mixed-precision interaction backward (fp16 tensors, tcgen05); see include/dlrm.h."""
+    rc = load().dlrm_interact_bwd_f16(_ptr(grad_out), _ptr(dense), _ptr(pooled), F, D, B, out_cols,
+                                      _ptr(grad_dense), _ptr(grad_pooled), _ptr(status), _stream(stream))
+    _check("dlrm_interact_bwd_f16", rc)
 
 
 def dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows) -> int:

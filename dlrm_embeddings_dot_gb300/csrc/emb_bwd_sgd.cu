@@ -267,10 +267,26 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
 }
 
 // --------------------------------------------------------- 3. segment sums
-template <int MC>
+// Four consecutive gradient elements as fp32: one 16-byte load of fp32, or an
+// 8-byte load of fp16 widened exactly.
+template <typename GT>
+__device__ __forceinline__ float4 load_grad4(const GT* p)
+{
+    if constexpr (sizeof(GT) == 4) {
+        return u4_as_f4(ldg_nc_v4(p));
+    } else {
+        uint2 r;
+        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+        return make_float4(a.x, a.y, c.x, c.y);
+    }
+}
+
+template <int MC, typename GT>
 __global__ void __launch_bounds__(256)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
-               const float* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
+               const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
                float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
                int64_t nchunks, int64_t nbags)
 {
@@ -312,7 +328,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                         v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
                         // row < nbags holds for pairs made from well-formed offsets
                         if (q + u < e && col < c4 && (int64_t)row < nbags)
-                            v[u][m] = u4_as_f4(ldg_nc_v4(grad + (int64_t)row * D + 4 * col));
+                            v[u][m] = load_grad4<GT>(grad + (int64_t)row * D + 4 * col);
                     }
                 }
 #pragma unroll
@@ -535,15 +551,15 @@ int key_bits(int64_t total_rows)
     return b;
 }
 
-template <int MC>
-dlrm_status launch_segments(const Ws& w, int64_t nnz, const float* grad, int D, float* tables,
+template <int MC, typename GT>
+dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables,
                             int64_t total_rows, float lr, int64_t nbags, cudaStream_t st)
 {
     const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
     int64_t blocks = (nchunks * kWarp + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    segment_kernel<MC><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
+    segment_kernel<MC, GT><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
                                                     w.partials, w.split_list, w.split_count, nchunks, nbags);
     dlrm_status s = check_launch("segment_kernel");
     if (s != DLRM_OK) return s;
@@ -581,7 +597,7 @@ extern "C" size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t to
 
 extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t total_rows, int F,
                                         int D, int B, const int32_t* d_indices, const int32_t* d_offsets,
-                                        int64_t nnz, const float* d_grad_pooled, float lr, void* d_workspace,
+                                        int64_t nnz, const void* d_grad_pooled, float lr, void* d_workspace,
                                         size_t workspace_bytes, unsigned flags, uint32_t* d_status, void* stream)
 {
     clear_error();
@@ -595,7 +611,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: total_rows must be in [1, 2^32 - 1)");
     if (!d_tables || !d_row_base || !d_offsets || !d_grad_pooled || (nnz > 0 && (!d_indices || !d_workspace)))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: null device pointer");
-    if (flags & ~DLRM_FLAG_HASH_INDICES)
+    if (flags & ~(DLRM_FLAG_HASH_INDICES | DLRM_FLAG_GRAD_F16))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: unknown flag bits 0x%x", flags);
     if (D % 4 != 0 || D > 1024)
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: D must be a multiple of 4, at most 1024");
@@ -647,7 +663,14 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         if (s != DLRM_OK) return s;
         cur ^= 1;
     }
-    const float* grad = d_grad_pooled;
+    if (flags & DLRM_FLAG_GRAD_F16) {
+        const __half* grad = static_cast<const __half*>(d_grad_pooled);
+        if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+        if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+        if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+        return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+    }
+    const float* grad = static_cast<const float*>(d_grad_pooled);
     if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
     if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
     if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);

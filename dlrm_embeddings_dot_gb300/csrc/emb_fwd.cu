@@ -51,6 +51,21 @@ __device__ __forceinline__ uint4 pack_chunk(const float* a)
         return f8_to_h8(a);
 }
 
+// Stores one chunk (Vec<T>::n elements) of a pooled row: as is, or fp32 -> fp16
+// rounded to nearest (the fp16 pooled output of fp32 master rows).
+template <typename T, typename TO>
+__device__ __forceinline__ void store_chunk(TO* dst, uint4 v)
+{
+    if constexpr (sizeof(T) == sizeof(TO)) {
+        *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+        const __half2 lo = __floats2half2_rn(__uint_as_float(v.x), __uint_as_float(v.y));
+        const __half2 hi = __floats2half2_rn(__uint_as_float(v.z), __uint_as_float(v.w));
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+}
+
 // Global row for index `i` of a table of n rows starting at `base`, or -1 if skipped.
 __device__ __forceinline__ int64_t resolve_row(int64_t i, int64_t base, int64_t n, bool hash,
                                                uint32_t* status)
@@ -112,11 +127,11 @@ __device__ __forceinline__ uint4 pool_bag(const T* __restrict__ tables, const in
     return pack_chunk<T>(acc);
 }
 
-template <typename T, int G>
+template <typename T, typename TO, int G>
 __global__ void __launch_bounds__(kThreads)
 emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ row_base, int F,
                      int D, int B, const int32_t* __restrict__ indices,
-                     const int32_t* __restrict__ offsets, T* __restrict__ pooled, bool hash,
+                     const int32_t* __restrict__ offsets, TO* __restrict__ pooled, bool hash,
                      uint32_t* status, int64_t nbags, int64_t nnz)
 {
     constexpr int V = Vec<T>::n;
@@ -133,7 +148,7 @@ emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ r
         const int64_t base = row_base[t], n = row_base[t + 1] - base;
         for (int ch = lane; ch < chunks; ch += G) {
             uint4 r = pool_bag<T, 4>(tables, indices, s, e, base, n, D, ch, hash, status);
-            *reinterpret_cast<uint4*>(pooled + g * D + (int64_t)ch * V) = r;
+            store_chunk<T, TO>(pooled + g * D + (int64_t)ch * V, r);
         }
     }
 }
@@ -145,11 +160,11 @@ emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ r
 // lane.  Writes go to pooled row b*F + t, a full row per group of lanes.
 // Bags that do not hold exactly one index are summed afterwards by the
 // whole warp.
-template <typename T, int G>
+template <typename T, typename TO, int G>
 __global__ void __launch_bounds__(kThreads)
 emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ row_base, int F,
                       int D, int B, const int32_t* __restrict__ indices,
-                      const int32_t* __restrict__ offsets, T* __restrict__ pooled, bool hash,
+                      const int32_t* __restrict__ offsets, TO* __restrict__ pooled, bool hash,
                       uint32_t* status, int64_t nbags, int64_t nnz)
 {
     constexpr int V = Vec<T>::n;
@@ -194,8 +209,7 @@ emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ 
                 const int src_lane = k0 + u * RPI + sub;
                 const int l = __shfl_sync(0xffffffffu, len, src_lane);
                 const int64_t o = __shfl_sync(0xffffffffu, orow, src_lane);
-                if (l >= 0 && l <= 1 && active)
-                    *reinterpret_cast<uint4*>(pooled + o * D + (int64_t)cl * V) = v[u];
+                if (l >= 0 && l <= 1 && active) store_chunk<T, TO>(pooled + o * D + (int64_t)cl * V, v[u]);
             }
         }
         // ---- bags with several indices: the whole warp, RPI bags at a time
@@ -218,7 +232,7 @@ emb_fwd_single_kernel(const T* __restrict__ tables, const int64_t* __restrict__ 
                 const int64_t base = row_base[t];
                 const uint4 r = pool_bag<T, 4>(tables, indices, s, e, base, row_base[t + 1] - base, D, cl,
                                                hash, status);
-                *reinterpret_cast<uint4*>(pooled + o * D + (int64_t)cl * V) = r;
+                store_chunk<T, TO>(pooled + o * D + (int64_t)cl * V, r);
             }
         }
     }
@@ -232,33 +246,33 @@ int64_t grid_for(int64_t groups, int G)
     return blocks < 1 ? 1 : blocks;
 }
 
-template <typename T, int G>
+template <typename T, typename TO, int G>
 void launch(const void* tables, const int64_t* row_base, int F, int D, int B,
             const int32_t* indices, const int32_t* offsets, void* pooled, bool hash,
             uint32_t* status, int64_t nbags, int64_t nnz, bool single_hot, cudaStream_t stream)
 {
     if (single_hot && D / Vec<T>::n <= G)
-        emb_fwd_single_kernel<T, G><<<(int)grid_for((nbags + kWarp - 1) / kWarp, kWarp), kThreads, 0, stream>>>(
-            (const T*)tables, row_base, F, D, B, indices, offsets, (T*)pooled, hash, status, nbags, nnz);
+        emb_fwd_single_kernel<T, TO, G><<<(int)grid_for((nbags + kWarp - 1) / kWarp, kWarp), kThreads, 0, stream>>>(
+            (const T*)tables, row_base, F, D, B, indices, offsets, (TO*)pooled, hash, status, nbags, nnz);
     else
-        emb_fwd_multi_kernel<T, G><<<(int)grid_for(nbags, G), kThreads, 0, stream>>>(
-            (const T*)tables, row_base, F, D, B, indices, offsets, (T*)pooled, hash, status, nbags, nnz);
+        emb_fwd_multi_kernel<T, TO, G><<<(int)grid_for(nbags, G), kThreads, 0, stream>>>(
+            (const T*)tables, row_base, F, D, B, indices, offsets, (TO*)pooled, hash, status, nbags, nnz);
 }
 
-template <typename T>
+template <typename T, typename TO>
 dlrm_status dispatch(const void* tables, const int64_t* row_base, int F, int D, int B,
                      const int32_t* indices, const int32_t* offsets, void* pooled, bool hash,
                      uint32_t* status, int64_t nbags, int64_t nnz, bool single_hot, cudaStream_t stream)
 {
     const int chunks = D * (int)sizeof(T) / 16;
     if (chunks <= 4)
-        launch<T, 4>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
+        launch<T, TO, 4>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
     else if (chunks <= 8)
-        launch<T, 8>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
+        launch<T, TO, 8>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
     else if (chunks <= 16)
-        launch<T, 16>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
+        launch<T, TO, 16>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
     else
-        launch<T, 32>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
+        launch<T, TO, 32>(tables, row_base, F, D, B, indices, offsets, pooled, hash, status, nbags, nnz, single_hot, stream);
     return check_launch("emb_fwd kernel");
 }
 
@@ -284,8 +298,11 @@ extern "C" dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype,
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: F*B must be below 2^31");
     if (!d_tables || !d_row_base || !d_offsets || !d_pooled || (nnz > 0 && !d_indices))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: null device pointer");
-    if (flags & ~DLRM_FLAG_HASH_INDICES)
+    if (flags & ~(DLRM_FLAG_HASH_INDICES | DLRM_FLAG_POOLED_F16))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: unknown flag bits 0x%x", flags);
+    const bool out_f16 = (flags & DLRM_FLAG_POOLED_F16) != 0;
+    if (out_f16 && dtype != DLRM_F32)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: DLRM_FLAG_POOLED_F16 needs fp32 tables");
     const int s = dtype_size(dtype);
     if (((int64_t)D * s) % 16 != 0)
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_fwd: D*%d bytes must be a multiple of 16", s);
@@ -296,9 +313,12 @@ extern "C" dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype,
     const bool hash = (flags & DLRM_FLAG_HASH_INDICES) != 0;
     const bool single_hot = nnz <= nbags + nbags / 8;   // about one index per bag
     cudaStream_t st = as_stream(stream);
+    if (dtype == DLRM_F32 && out_f16)
+        return dispatch<float, __half>(d_tables, d_row_base, F, D, B, d_indices, d_offsets, d_pooled, hash,
+                                       d_status, nbags, nnz, single_hot, st);
     if (dtype == DLRM_F32)
-        return dispatch<float>(d_tables, d_row_base, F, D, B, d_indices, d_offsets, d_pooled, hash,
-                               d_status, nbags, nnz, single_hot, st);
-    return dispatch<__half>(d_tables, d_row_base, F, D, B, d_indices, d_offsets, d_pooled, hash,
-                            d_status, nbags, nnz, single_hot, st);
+        return dispatch<float, float>(d_tables, d_row_base, F, D, B, d_indices, d_offsets, d_pooled, hash,
+                                      d_status, nbags, nnz, single_hot, st);
+    return dispatch<__half, __half>(d_tables, d_row_base, F, D, B, d_indices, d_offsets, d_pooled, hash,
+                                    d_status, nbags, nnz, single_hot, st);
 }

@@ -97,6 +97,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int c1, int c2, const void* src)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until at most N committed bulk groups of this thread still read shared memory.
@@ -135,6 +142,20 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
     d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+    d |= (uint64_t)1 << 46;                 // version
+    d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+    return d;
+}
+
+// Shared-memory descriptor, 128-byte swizzle, explicit byte offsets.  For an
+// MN-major operand (M or N contiguous) the leading offset is the stride
+// between 64-element blocks along M/N and the stride offset the stride
+// between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lead_bytes, uint32_t stride_bytes)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lead_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((stride_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;                 // version
     d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
     return d;

@@ -61,6 +61,12 @@ typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
 /* flags */
 #define DLRM_FLAG_HASH_INDICES 1u  /* fold every index into its table: idx := ((idx % N_t) + N_t) % N_t
                                       ("DLRM For PyTorch", §Command-line options, --hash_indices) */
+#define DLRM_FLAG_POOLED_F16 2u    /* dlrm_emb_fwd: fp32 tables, fp16 pooled output (each bag summed
+                                      in fp32, rounded once): the fp16 interaction input of mixed
+                                      precision ("DLRM For PyTorch", §Mixed precision training) */
+#define DLRM_FLAG_GRAD_F16 4u      /* dlrm_emb_bwd_sgd: grad_pooled is fp16 (from
+                                      dlrm_interact_bwd_f16); with a static loss scale S pass lr / S
+                                      (exact in fp32 for a power-of-two S such as the pages' 1024) */
 
 /* bits OR-ed into *d_status by kernels */
 #define DLRM_STATUS_OOB_INDEX 1u   /* an index outside [0, N_t) with hashing off: it was skipped */
@@ -85,7 +91,8 @@ typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
  *   d_tables   [total_rows][D] of dtype, 16-byte aligned
  *   d_row_base int64 [F+1], row_base[0] = 0, non-decreasing
  *   d_indices  int32 [nnz];  d_offsets int32 [F*B+1]
- *   d_pooled   [B][F][D] of dtype, 16-byte aligned (output)
+ *   d_pooled   [B][F][D] of dtype, 16-byte aligned (output); fp16 with
+ *              DLRM_FLAG_POOLED_F16 (fp32 tables only)
  * Requires F >= 1, D >= 1, B >= 0, 0 <= nnz < 2^31, D*s % 16 == 0.
  */
 dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
@@ -166,6 +173,25 @@ dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_dense,
                               void* stream);
 
 /*
+ * dlrm_interact_bwd_f16 -- the same gradient for the mixed-precision step
+ * ("DLRM For PyTorch", §Mixed precision training: fp16 tensors, static loss
+ * scaling, so G and the results carry the loss scale), on the tcgen05 tensor
+ * cores: dZ = M Z as one block-diagonal product per four samples, fp32
+ * accumulation, each result rounded once to fp16 (grad_dense = G[0..D) +
+ * dZ_0 added in fp32 first).
+ *
+ *   d_grad_out    fp16 [B][out_cols];  d_dense fp16 [B][D];  d_pooled fp16 [B][F][D]
+ *   d_grad_dense  fp16 [B][D] (output);  d_grad_pooled fp16 [B][F][D] (output)
+ * All pointers 16-byte aligned.  Requires out_cols >= W, a multiple of 8 and
+ * at most 1024, F <= 31, D a multiple of 64 up to 256 (DLRM_ERR_UNSUPPORTED
+ * otherwise).
+ * A device-side wait that times out sets DLRM_STATUS_TIMEOUT in *d_status.
+ */
+dlrm_status dlrm_interact_bwd_f16(const void* d_grad_out, const void* d_dense, const void* d_pooled, int F,
+                                  int D, int B, int out_cols, void* d_grad_dense, void* d_grad_pooled,
+                                  uint32_t* d_status, void* stream);
+
+/*
  * Workspace bytes dlrm_emb_bwd_sgd needs for nnz indices of width D over
  * total_rows rows.  Returns 0 for invalid sizes.
  */
@@ -189,7 +215,8 @@ size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
  *   d_tables       fp32 [total_rows][D], updated in place, 16-byte aligned
  *   d_row_base     int64 [F+1] with row_base[F] = total_rows
  *   total_rows     rows in the joint table, 1 <= total_rows < 2^32 - 1
- *   d_grad_pooled  fp32 [B][F][D] (from dlrm_interact_bwd), 16-byte aligned
+ *   d_grad_pooled  fp32 [B][F][D] (from dlrm_interact_bwd), 16-byte aligned;
+ *                  fp16 with DLRM_FLAG_GRAD_F16 (from dlrm_interact_bwd_f16)
  *   d_workspace    >= dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows)
  *                  bytes, 256-byte aligned.  After the stream completes, its
  *                  first nnz uint32 are the sorted row keys (0xFFFFFFFF for
@@ -201,7 +228,7 @@ size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
 dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
                              int F, int D, int B, const int32_t* d_indices,
                              const int32_t* d_offsets, int64_t nnz,
-                             const float* d_grad_pooled, float lr, void* d_workspace,
+                             const void* d_grad_pooled, float lr, void* d_workspace,
                              size_t workspace_bytes, unsigned flags, uint32_t* d_status,
                              void* stream);
 
@@ -230,7 +257,8 @@ dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t
  *    Calls that overlap on the GPU -- on different streams, or from several
  *    host threads -- race on it and must be serialised by the caller.
  * Results are identical to dlrm_emb_bwd_sgd; the sorted keys are not
- * returned.
+ * returned.  Flags as for dlrm_emb_bwd_sgd (with DLRM_FLAG_GRAD_F16 the
+ * gradient pointer holds fp16).
  */
 #define DLRM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base, int64_t total_rows,

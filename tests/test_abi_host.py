@@ -104,7 +104,7 @@ def test_sgd_workspace_and_validation(L):
     assert f(*bad) == dl.DLRM_ERR_UNSUPPORTED
     bad = list(args); bad[4] = 6                          # D % 4 != 0
     assert f(*bad) == dl.DLRM_ERR_UNSUPPORTED
-    bad = list(args); bad[13] = 4                         # unknown flag
+    bad = list(args); bad[13] = 8                         # unknown flag
     assert f(*bad) == dl.DLRM_ERR_INVALID_ARG
     ok = list(args); ok[8] = 0; ok[6] = None              # nnz = 0: nothing to do
     assert f(*ok) == dl.DLRM_OK
