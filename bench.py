@@ -169,8 +169,8 @@ def cpu_baseline(w, n_samples: int) -> dict:
 def kernels_per_step(total_rows: int) -> int:
     nbits = int(total_rows).bit_length()
     npasses = (nbits + 7) // 8
-    # emb_fwd, interact_fwd, interact_bwd, then keys + 3 per radix pass + segment + fixup
-    return 3 + 1 + 3 * npasses + 2
+    # emb_fwd, interact_fwd, interact_bwd, then keys + 3 per radix pass + segment + two fixups
+    return 3 + 1 + 3 * npasses + 3
 
 
 def run_ours(args) -> None:
@@ -318,6 +318,24 @@ def run_ours(args) -> None:
     ums = reduce_max(u0.elapsed_time(u1), world, dev)
     del tab16, pooled16, out16
 
+    # ---- the same training step in mixed precision (the pages' --amp): fp16
+    # interaction tensors on tcgen05, fp32 master tables, static loss scale
+    amp_ops = amp_step_ops(dl, w, torch, dev, stream, status, tables)
+    for _ in range(args.warmup):
+        for _, fn in amp_ops:
+            fn()
+    barrier(world)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        for _, fn in amp_ops:
+            fn()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    ams = reduce_max(a0.elapsed_time(a1), world, dev)
+    del amp_ops
+
     # ---- end to end through the public API from pinned host buffers
     h_dense = torch.from_numpy(w.dense).pin_memory()
     h_idx = torch.from_numpy(w.indices).pin_memory()
@@ -397,6 +415,12 @@ def run_ours(args) -> None:
                           "entry_point": "dlrm_emb_interact_fwd (lookup + tcgen05 interaction in one kernel)",
                           "alg_GBps": round(B * (F * (8 + D * 2) + D * 2 + P * 2) / (ums / args.steps / 1e3) / 1e9,
                                             1)}},
+        "amp_train": {"value": round(B * world * args.steps / (ams / 1e3), 1), "unit": "samples/s",
+                      "ms_per_step": round(ams / args.steps, 4),
+                      "dtype": "f16 interaction tensors (tcgen05 forward and backward), fp32 master tables",
+                      "workload": "the same 64K training step with the pages' mixed precision: pooled rows rounded "
+                                  "to fp16, upstream gradient scaled by the static loss scale 1024, SGD on fp16 "
+                                  "gradients with lr/1024"},
         "e2e": {"value": round(B * world * e_steps / (ems / 1e3), 1), "unit": "samples/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": kernels_per_step(w.total_rows) * args.steps,
@@ -424,8 +448,8 @@ def run_op(args) -> None:
     B, F, D, P = args.batch, 26, 128, 480
     g = torch.Generator(device=dev).manual_seed(0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    if args.op in ("interact_fwd", "interact_fwd16", "interact_bwd"):
-        dt = torch.float16 if args.op == "interact_fwd16" else torch.float32
+    if args.op in ("interact_fwd", "interact_fwd16", "interact_bwd", "interact_bwd16"):
+        dt = torch.float16 if args.op in ("interact_fwd16", "interact_bwd16") else torch.float32
         dense = torch.rand(B, D, generator=g, device=dev).to(dt)
         pooled = ((torch.rand(B, F, D, generator=g, device=dev) - 0.5) * 0.1).to(dt)
         out = torch.empty(B, P, dtype=dt, device=dev)
@@ -433,9 +457,15 @@ def run_op(args) -> None:
         gd = torch.empty(B, D, device=dev)
         gp = torch.empty(B, F, D, device=dev)
 
+        go16 = (go * 1024.0).to(torch.float16)
+        gd16 = torch.empty(B, D, dtype=torch.float16, device=dev)
+        gp16 = torch.empty(B, F, D, dtype=torch.float16, device=dev)
+
         def once():
             if args.op == "interact_bwd":
                 dl.dlrm_interact_bwd(go, dense, pooled, F, D, B, P, gd, gp)
+            elif args.op == "interact_bwd16":
+                dl.dlrm_interact_bwd_f16(go16, dense, pooled, F, D, B, P, gd16, gp16, status=status)
             else:
                 dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status)
     else:
@@ -751,6 +781,7 @@ def main(argv=None) -> None:
     ap.add_argument("--config", choices=sorted(CONFIGS), action="append",
                     help="measure one of the pages' workloads instead of the headline step (repeatable)")
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
+                                     "interact_bwd16",
                                      "emb_bwd_sgd", "emb_interact16"],
                     help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
     ap.add_argument("--small-tables", action="store_true",
