@@ -384,7 +384,7 @@ def run_ours(args) -> None:
         "emb_bwd_sgd": nnz * (4 + 4 + D * 4) + (unique_rows or 0) * 2 * D * 4,
     }
     dom = max(op_ms, key=op_ms.get)
-    kernel_names = {"emb_fwd": "emb_fwd_single_kernel", "interact_fwd": "interact_fwd_ffma_kernel",
+    kernel_names = {"emb_fwd": "emb_fwd_single_kernel", "interact_fwd": "interact_fwd_regs_kernel",
                     "interact_bwd": "interact_bwd_kernel",
                     "emb_bwd_sgd": f"emb_bwd_sgd ({kernels_per_step(w.total_rows) - 3} kernels)"}
     achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9

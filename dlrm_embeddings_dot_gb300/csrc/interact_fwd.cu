@@ -3,11 +3,35 @@
 // bottom-MLP output and the F pooled embeddings, strict lower triangle in
 // row-major order, concatenated after the dense vector, zero padded.
 //
-// This file holds the CUDA-core (FFMA) kernel, used for fp32 (tensor-core
-// TF32 cannot meet fp32 accuracy) and for fp16 shapes the tensor-core kernel
-// does not take, plus the entry point that picks between the two.
+// This file holds the CUDA-core kernels, used for fp32 (a single TF32
+// product cannot meet fp32 accuracy, and the three-product split measured
+// slower than these kernels) and for fp16 shapes the tensor-core kernel does
+// not take, plus the entry point that picks among them.
 //
-// FFMA kernel: one CTA of 4 warps per sample at a time.  Z = [dense; pooled
+// Where every operand float must be read from shared memory, the shared-memory
+// pipe bounds the arithmetic: a wavefront delivers 32 lane-words per clock
+// while the FMA pipes consume 128 products, so a lane needs four products per
+// float it loads (8x8 register tiles, which waste half their products on the
+// triangle).  The kernel for the common fp32 shape therefore keeps the
+// operands in registers and moves partial sums instead:
+//
+// Register kernel (fp32, D = 128, F + 1 rows of Z known at compile time): one
+// warp per sample.  Lane l holds features 4l..4l+3 of every row of Z in
+// registers and forms its four-feature partial dot products for all F(F+1)/2
+// pairs (i, j), j < i, in output order, in groups of 32 -- no wasted product.
+// Each group is finished by a transpose through a per-warp 32 x 36 shared
+// scratch: lane l stores its 32 partials as row l (four 16-byte stores, no
+// bank conflict with the 36-float pitch), and lane t adds column t in lane
+// order (32 conflict-free 4-byte reads), which leaves the dot product of the
+// group's pair t in lane t: 32 consecutive output columns, one coalesced
+// store.  (A shuffle transpose-reduce moves half the bytes but serialises a
+// select, a shuffle and an add per step and measured slower.)  A sample
+// arrives in the warp's buffer by two bulk copies (the dense row, then the F
+// pooled rows, contiguous in global memory) completing on the warp's
+// mbarrier; the next sample's copy is issued after the first group, behind a
+// warp barrier that orders the buffer's reads before the refill.
+//
+// Tile kernel (any shape): one CTA of 4 warps per sample at a time.  Z = [dense; pooled
 // rows] is staged in shared memory as fp32 (all 16-byte chunks of a sample in
 // flight at once via cp.async), rows padded to a multiple of 4 and to
 // 128-byte strides, with the 16-byte chunk index XOR-swizzled by (row / 4)
@@ -18,8 +42,12 @@
 // order w = 0..3 through shared memory.  A CTA holds one sample (about 23 KB
 // for F = 26, D = 128), so ~9 CTAs (36 warps) share an SM and hide each
 // other's staging latency.
+#include <type_traits>
+#include <utility>
+
 #include "common.cuh"
 #include "interact_tc.cuh"
+#include "tcgen05.cuh"
 
 namespace dlrm {
 namespace {
@@ -215,6 +243,184 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
     }
 }
 
+// ------------------------------------------------------------ register kernel
+constexpr int kRegWarps = 4;     // warps per CTA, one sample each at a time
+constexpr int kRegD = 128;       // 32 lanes x 4 features
+constexpr int kPitch = 36;       // floats per row of the transpose scratch
+
+template <typename Fn, int... Is>
+__device__ __forceinline__ void static_for_impl(Fn& fn, std::integer_sequence<int, Is...>)
+{
+    (fn(std::integral_constant<int, Is>{}), ...);
+}
+
+// fn(std::integral_constant<int, 0>), ..., fn(std::integral_constant<int, N-1>):
+// every index is a constant expression, so register arrays stay in registers.
+template <int N, typename Fn>
+__device__ __forceinline__ void static_for(Fn&& fn)
+{
+    static_for_impl(fn, std::make_integer_sequence<int, N>{});
+}
+
+// Pair p of the strict lower triangle in row-major order: p = i(i-1)/2 + j.
+constexpr int pair_row(int p)
+{
+    int i = 1;
+    while (i * (i + 1) / 2 <= p) ++i;
+    return i;
+}
+
+__device__ __forceinline__ float dot4(const float4& a, const float4& b)
+{
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+}
+
+// Four-feature partial dot product of pair p (zero past the last pair).
+template <int R, int p>
+__device__ __forceinline__ float slot_dot(const float4 (&z)[R])
+{
+    if constexpr (p < R * (R - 1) / 2) {
+        constexpr int i = pair_row(p);
+        constexpr int j = p - i * (i - 1) / 2;
+        return dot4(z[i], z[j]);
+    } else {
+        return 0.f;
+    }
+}
+
+// One bulk (non-tensor) copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     tc::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
+
+// Bounded wait for the phase of `parity`; false when the bound is hit, after
+// a bounded drain of the copy in flight.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity)
+{
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (clock64() - t0 < tc::kWaitCycles)
+        if (tc::mbar_try_wait(bar, parity)) return true;
+    tc::mbar_drain(bar, parity);
+    return false;
+}
+
+// Shared memory of one CTA: [kRegWarps][R rows][D floats] sample buffers,
+// [kRegWarps][32][kPitch] transpose scratch, kRegWarps mbarriers.
+template <int R>
+constexpr size_t regs_smem_bytes()
+{
+    return (size_t)kRegWarps * R * kRegD * 4 + (size_t)kRegWarps * 32 * kPitch * 4 + kRegWarps * 8;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kRegWarps * kWarp, 3)
+interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restrict__ pooled, int B,
+                         float* __restrict__ out, int P, uint32_t* __restrict__ status)
+{
+    constexpr int NP = R * (R - 1) / 2;           // pairs
+    constexpr int NG = (NP + 31) / 32;            // groups of 32 pairs
+    constexpr int D = kRegD;
+    extern __shared__ __align__(16) float4 zbuf[];
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    float4* mine = zbuf + warp * R * kWarp;       // row r, features 4l..4l+3 at [r * 32 + l]
+    float* const scratch_all = reinterpret_cast<float*>(zbuf + kRegWarps * R * kWarp);
+    float* scratch = scratch_all + warp * 32 * kPitch;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(scratch_all + kRegWarps * 32 * kPitch) + warp;
+    const int64_t stride = (int64_t)gridDim.x * kRegWarps;
+    int64_t b = (int64_t)blockIdx.x * kRegWarps + warp;
+
+    // row 0 of Z is the dense row, rows 1..F the sample's pooled rows
+    auto stage = [&](int64_t s) {
+        if (lane == 0) {
+            tc::mbar_expect_tx(bar, R * D * 4);
+            bulk_g2s(mine, dense + s * D, D * 4, bar);
+            bulk_g2s(mine + kWarp, pooled + s * (int64_t)(R - 1) * D, (R - 1) * D * 4, bar);
+        }
+    };
+    if (lane == 0) {
+        tc::mbar_init(bar, 1);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+    uint32_t phase = 0;
+    if (b < B) stage(b);
+    for (; b < B; b += stride) {
+        if (!bounded_wait(bar, phase)) {
+            if (lane == 0) set_status(status, DLRM_STATUS_TIMEOUT);
+            return;
+        }
+        phase ^= 1u;
+        float4 z[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) z[r] = mine[r * kWarp + lane];
+        float* orow = out + b * P;
+        *reinterpret_cast<float4*>(orow + 4 * lane) = z[0];
+        static_for<NG>([&](auto G) {
+            constexpr int g = decltype(G)::value;
+            float v[32];
+            static_for<32>([&](auto T) {
+                constexpr int t = decltype(T)::value;
+                v[t] = slot_dot<R, g * 32 + t>(z);
+            });
+            float* row = scratch + lane * kPitch;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(row + 4 * q) =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            __syncwarp();
+            float sum = scratch[lane];
+#pragma unroll
+            for (int r = 1; r < 32; ++r) sum += scratch[r * kPitch + lane];
+            const int col = D + g * 32 + lane;
+            if (col < P) orow[col] = sum;
+            // orders this group's scratch reads before the next group's
+            // writes; it also keeps the scheduler from hoisting later groups'
+            // products into this group (which spills registers)
+            __syncwarp();
+            if constexpr (g == 0) {
+                // the sample buffer was read before the barrier above
+                if (b + stride < B) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    stage(b + stride);
+                }
+            }
+        });
+    }
+}
+
+template <int R>
+dlrm_status launch_regs(const float* dense, const float* pooled, int B, float* out, int P, uint32_t* status,
+                        cudaStream_t stream)
+{
+    const size_t smem = regs_smem_bytes<R>();
+    auto kern = interact_fwd_regs_kernel<R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_fwd: %s", cudaGetErrorString(e));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRegWarps * kWarp, smem);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    const int64_t need = ((int64_t)B + kRegWarps - 1) / kRegWarps;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    const int blocks = (int)(need < cap ? need : cap);
+    kern<<<blocks, kRegWarps * kWarp, smem, stream>>>(dense, pooled, B, out, P, status);
+    return check_launch("interact_fwd_regs_kernel");
+}
+
+// Shapes the register kernel takes: fp32, D = 128, F in {8, 26}, rows of the
+// output 16-byte aligned, and no padding column past the last group of 32
+// pairs (the group's empty slots write the padding zeros).
+inline bool regs_supported(int F, int D, int P, const void* out)
+{
+    const int groups = (F * (F + 1) / 2 + 31) / 32;
+    return D == kRegD && (F == 8 || F == 26) && P % 4 == 0 && P <= kRegD + 32 * groups && aligned16(out);
+}
+
 template <typename T, int DT>
 dlrm_status launch_ffma_t(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
                           cudaStream_t stream)
@@ -238,8 +444,17 @@ dlrm_status launch_ffma_t(const void* dense, const void* pooled, int F, int D, i
 
 template <typename T>
 dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int B, void* out, int P,
-                        cudaStream_t stream)
+                        uint32_t* status, cudaStream_t stream)
 {
+    if constexpr (sizeof(T) == 4) {
+        if (regs_supported(F, D, P, out)) {
+            const float* d = static_cast<const float*>(dense);
+            const float* p = static_cast<const float*>(pooled);
+            float* o = static_cast<float*>(out);
+            return F == 26 ? launch_regs<27>(d, p, B, o, P, status, stream)
+                           : launch_regs<9>(d, p, B, o, P, status, stream);
+        }
+    }
     if (D == 128) return launch_ffma_t<T, 128>(dense, pooled, F, D, B, out, P, stream);
     return launch_ffma_t<T, 0>(dense, pooled, F, D, B, out, P, stream);
 }
@@ -272,8 +487,8 @@ extern "C" dlrm_status dlrm_interact_fwd(const void* d_dense, const void* d_pool
     cudaStream_t st = as_stream(stream);
     if (dtype == DLRM_F16 && tc_interact_supported(F, D, out_cols, d_dense, d_pooled, d_out))
         return tc_interact_fwd(d_dense, d_pooled, F, D, B, d_out, out_cols, d_status, st);
-    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
-    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, d_status, st);
+    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, d_status, st);
 }
 
 // CUDA-core path for any shape, exposed for tests of the tensor-core kernel.
@@ -289,6 +504,6 @@ extern "C" dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const vo
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_fwd_cuda_core: alignment");
     if (B == 0) return DLRM_OK;
     cudaStream_t st = as_stream(stream);
-    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
-    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, st);
+    if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, nullptr, st);
+    return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, nullptr, st);
 }

@@ -86,7 +86,20 @@ def test_tensor_core_shapes(cuda_lib, F, D):
     check_fwd(cc, dense, pooled, P, 2e-2)
 
 
-@pytest.mark.parametrize("F,D,P", [(3, 16, 22), (26, 128, 480), (5, 40, 60), (33, 64, 700), (26, 24, 400)])
+@pytest.mark.parametrize("B", [1, 5, 1021, 4099])
+def test_register_kernel_default_shape_fp32(cuda_lib, B):
+    """F = 26, D = 128, P = 480 fp32: the register-resident kernel (one warp
+    per sample); B past 1216 makes warps take several samples, so the
+    double-buffered staging of the next sample is exercised."""
+    rng = np.random.default_rng(100 + B)
+    dense = np.abs(rng.standard_normal((B, 128))).astype(np.float32)
+    pooled = rng.standard_normal((B, 26, 128)).astype(np.float32)
+    got = run_fwd(cuda_lib, to_dev(dense), to_dev(pooled), 480)
+    check_fwd(got, dense, pooled, 480, 1e-5)
+
+
+@pytest.mark.parametrize("F,D,P", [(3, 16, 22), (26, 128, 480), (5, 40, 60), (33, 64, 700), (26, 24, 400),
+                                   (8, 128, 164), (8, 128, 192), (26, 128, 496), (26, 128, 484)])
 @pytest.mark.parametrize("dt", [np.float32, np.float16])
 def test_cuda_core_kernel(cuda_lib, F, D, P, dt):
     if dt == np.float16 and D % 8:
