@@ -288,6 +288,28 @@ __device__ __forceinline__ float slot_dot(const float4 (&z)[R])
     }
 }
 
+__device__ __forceinline__ void cp_async16_ca(void* smem_dst, const void* gsrc)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One bulk (non-tensor) copy shared -> global in the thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(tc::smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // One bulk (non-tensor) copy global -> shared, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {
@@ -317,13 +339,48 @@ constexpr size_t regs_smem_bytes()
     return (size_t)kRegWarps * R * kRegD * 4 + (size_t)kRegWarps * 32 * kPitch * 4 + kRegWarps * 8;
 }
 
+// The interaction of one sample whose Z rows (features 4l..4l+3 in lane l)
+// are in z: the dense block and the F(F+1)/2 dot products of output row orow.
+// after_first = work to start once the first group has passed its barrier
+// (the sample buffer z came from may then be refilled).
+template <int R, typename Fn>
+__device__ __forceinline__ void regs_sample(const float4 (&z)[R], float* orow, int P, int lane, float* scratch,
+                                            Fn&& after_first)
+{
+    constexpr int NP = R * (R - 1) / 2;           // pairs
+    constexpr int NG = (NP + 31) / 32;            // groups of 32 pairs
+    constexpr int D = kRegD;
+    *reinterpret_cast<float4*>(orow + 4 * lane) = z[0];
+    static_for<NG>([&](auto G) {
+        constexpr int g = decltype(G)::value;
+        float v[32];
+        static_for<32>([&](auto T) {
+            constexpr int t = decltype(T)::value;
+            v[t] = slot_dot<R, g * 32 + t>(z);
+        });
+        float* row = scratch + lane * kPitch;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(row + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        __syncwarp();
+        float sum = scratch[lane];
+#pragma unroll
+        for (int r = 1; r < 32; ++r) sum += scratch[r * kPitch + lane];
+        const int col = D + g * 32 + lane;
+        if (col < P) orow[col] = sum;
+        // orders this group's scratch reads before the next group's writes;
+        // it also keeps the scheduler from hoisting later groups' products
+        // into this group (which spills registers)
+        __syncwarp();
+        if constexpr (g == 0) after_first();
+    });
+}
+
 template <int R>
 __global__ void __launch_bounds__(kRegWarps * kWarp, 3)
 interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restrict__ pooled, int B,
                          float* __restrict__ out, int P, uint32_t* __restrict__ status)
 {
-    constexpr int NP = R * (R - 1) / 2;           // pairs
-    constexpr int NG = (NP + 31) / 32;            // groups of 32 pairs
     constexpr int D = kRegD;
     extern __shared__ __align__(16) float4 zbuf[];
     const int lane = threadIdx.x % kWarp;
@@ -359,39 +416,173 @@ interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restric
         float4 z[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) z[r] = mine[r * kWarp + lane];
-        float* orow = out + b * P;
-        *reinterpret_cast<float4*>(orow + 4 * lane) = z[0];
-        static_for<NG>([&](auto G) {
-            constexpr int g = decltype(G)::value;
-            float v[32];
-            static_for<32>([&](auto T) {
-                constexpr int t = decltype(T)::value;
-                v[t] = slot_dot<R, g * 32 + t>(z);
-            });
-            float* row = scratch + lane * kPitch;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4*>(row + 4 * q) =
-                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            __syncwarp();
-            float sum = scratch[lane];
-#pragma unroll
-            for (int r = 1; r < 32; ++r) sum += scratch[r * kPitch + lane];
-            const int col = D + g * 32 + lane;
-            if (col < P) orow[col] = sum;
-            // orders this group's scratch reads before the next group's
-            // writes; it also keeps the scheduler from hoisting later groups'
-            // products into this group (which spills registers)
-            __syncwarp();
-            if constexpr (g == 0) {
-                // the sample buffer was read before the barrier above
-                if (b + stride < B) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    stage(b + stride);
-                }
+        const int64_t nb = b + stride;
+        regs_sample<R>(z, out + b * P, P, lane, scratch, [&] {
+            // the sample buffer was read before the group barrier
+            if (nb < B) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                stage(nb);
             }
         });
     }
+}
+
+// ------------------------------------------- lookup + register kernel in one pass
+// The same interaction, with the sample buffer filled straight from the
+// tables: lane t < F resolves bag t of the warp's next sample (bounds two
+// samples ahead, the index one sample ahead, as in the tensor-core fused
+// kernel), then every lane copies its 16-byte column of each single-index
+// bag's row with cp.async; empty bags (and rejected indices) give zero rows,
+// bags of several indices are summed in fp32 in bag order by the whole warp.
+// The pooled rows (rows 1..F of the buffer) leave by one bulk store, so the
+// lookup's output is written once and never read back.  Pooled rows and
+// interaction are bit-identical to dlrm_emb_fwd + dlrm_interact_fwd.
+struct RegGather {
+    const float* tables;
+    const int64_t* row_base;
+    const int32_t* indices;
+    const int32_t* offsets;
+    int64_t nnz;
+    bool hash;
+};
+
+// Shared memory: [kRegWarps][R rows][D floats] sample buffers and the scratch.
+template <int R>
+constexpr size_t emb_regs_smem_bytes()
+{
+    return (size_t)kRegWarps * R * kRegD * 4 + (size_t)kRegWarps * 32 * kPitch * 4;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kRegWarps * kWarp, 3)
+emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, float* __restrict__ pooled,
+                         float* __restrict__ out, int P, uint32_t* __restrict__ status)
+{
+    constexpr int F = R - 1;
+    constexpr int D = kRegD;
+    // bag -> source: a table row (32 bits: 2^32 rows of 512 bytes would not
+    // fit in memory), kRowZero (empty bag, rejected index) or kRowMulti
+    constexpr uint32_t kRowZero = 0xffffffffu, kRowMulti = 0xfffffffeu;
+    extern __shared__ __align__(16) float4 zbuf[];
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    float4* mine = zbuf + warp * R * kWarp;
+    float* scratch = reinterpret_cast<float*>(zbuf + kRegWarps * R * kWarp) + warp * 32 * kPitch;
+    const int64_t stride = (int64_t)gridDim.x * kRegWarps;
+    int64_t b = (int64_t)blockIdx.x * kRegWarps + warp;
+    int64_t tbase = 0, tn = 0;                    // lane t < F: table t's first row and row count
+    if (lane < F) {
+        tbase = ga.row_base[lane];
+        tn = ga.row_base[lane + 1] - tbase;
+    }
+    auto load_bounds = [&](int64_t smp, int& a, int& e) {
+        a = e = 0;
+        if (lane < F && smp < B) {
+            a = ldg_early_s32(ga.offsets + (int64_t)lane * B + smp);
+            e = ldg_early_s32(ga.offsets + (int64_t)lane * B + smp + 1);
+        }
+    };
+    auto clamp_bounds = [&](int& a, int& e) {     // into [0, nnz], flagging malformed lists
+        int64_t x = a, y = e;
+        if (x < 0 || y < x || y > ga.nnz) {
+            set_status(status, DLRM_STATUS_BAD_OFFSETS);
+            x = x < 0 ? 0 : (x > ga.nnz ? ga.nnz : x);
+            y = y < x ? x : (y > ga.nnz ? ga.nnz : y);
+        }
+        a = (int)x;
+        e = (int)y;
+    };
+    auto resolve = [&](int a, int e, int idx) -> uint32_t {
+        if (lane >= F || e - a == 0) return kRowZero;
+        if (e - a > 1) return kRowMulti;
+        int64_t i = idx;
+        if (ga.hash && tn > 0) {
+            i %= tn;
+            if (i < 0) i += tn;
+        } else if (ga.hash || i < 0 || i >= tn || tbase + i >= (int64_t)kRowMulti) {
+            set_status(status, DLRM_STATUS_OOB_INDEX);
+            return kRowZero;
+        }
+        return (uint32_t)(tbase + i);
+    };
+    // fill the buffer with sample smp: the dense row, then bag t's row as row t + 1
+    auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
+        cp_async16(mine + lane, dense + smp * D + 4 * lane);
+#pragma unroll
+        for (int t = 0; t < F; ++t) {
+            const uint32_t src = __shfl_sync(0xffffffffu, src_row, t);
+            float4* dst = mine + (t + 1) * kWarp + lane;
+            if (src < kRowMulti)
+                cp_async16_ca(dst, ga.tables + (size_t)src * D + 4 * lane);
+            else if (src == kRowZero)
+                *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // bags of several indices: fp32 sum in bag order, as in the lookup
+        for (uint32_t multi = __ballot_sync(0xffffffffu, src_row == kRowMulti); multi; multi &= multi - 1) {
+            const int t = __ffs(multi) - 1;
+            const int s1 = __shfl_sync(0xffffffffu, a, t), e1 = __shfl_sync(0xffffffffu, e, t);
+            const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int p = s1; p < e1; ++p) {
+                int64_t i = __ldg(ga.indices + p);
+                if (ga.hash && n > 0) {
+                    i %= n;
+                    if (i < 0) i += n;
+                } else if (ga.hash || i < 0 || i >= n) {
+                    set_status(status, DLRM_STATUS_OOB_INDEX);
+                    continue;
+                }
+                const float4 r = u4_as_f4(ldg_nc_l1_v4(ga.tables + (base + i) * D + 4 * lane));
+                acc.x += r.x;
+                acc.y += r.y;
+                acc.z += r.z;
+                acc.w += r.w;
+            }
+            mine[(t + 1) * kWarp + lane] = acc;
+        }
+        cp_async_commit();
+    };
+
+    int a0, e0, a1, e1;
+    load_bounds(b, a0, e0);
+    load_bounds(b + stride, a1, e1);
+    clamp_bounds(a0, e0);
+    if (b < B) {
+        const int idx0 = (lane < F && e0 - a0 == 1) ? __ldg(ga.indices + a0) : 0;
+        stage(b, resolve(a0, e0, idx0), a0, e0);
+    }
+    clamp_bounds(a1, e1);
+    for (; b < B; b += stride) {
+        const int64_t nb = b + stride;
+        // in flight during this sample: the next sample's index, the bounds two samples on
+        const int idx1 = (lane < F && e1 - a1 == 1) ? ldg_early_s32(ga.indices + a1) : 0;
+        int a2, e2;
+        load_bounds(nb + stride, a2, e2);
+        cp_async_wait_group<0>();
+        float4 z[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) z[r] = mine[r * kWarp + lane];
+        if (pooled) {
+            // every lane's rows (cp.async and plain stores) -> visible to the bulk store
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                bulk_s2g(pooled + b * (int64_t)F * D, mine + kWarp, F * D * 4);
+                tc::bulk_commit();
+            }
+        }
+        regs_sample<R>(z, out + b * P, P, lane, scratch, [&] {
+            if (pooled) {
+                if (lane == 0) tc::bulk_wait_read<0>();   // the bulk store has read the buffer
+                __syncwarp();
+            }
+            if (nb < B) stage(nb, resolve(a1, e1, idx1), a1, e1);
+        });
+        clamp_bounds(a2, e2);
+        a1 = a2;
+        e1 = e2;
+    }
+    if (pooled && lane == 0) tc::bulk_wait_all();
 }
 
 template <int R>
@@ -410,6 +601,24 @@ dlrm_status launch_regs(const float* dense, const float* pooled, int B, float* o
     const int blocks = (int)(need < cap ? need : cap);
     kern<<<blocks, kRegWarps * kWarp, smem, stream>>>(dense, pooled, B, out, P, status);
     return check_launch("interact_fwd_regs_kernel");
+}
+
+template <int R>
+dlrm_status launch_emb_regs(const RegGather& ga, const float* dense, int B, float* pooled, float* out, int P,
+                            uint32_t* status, cudaStream_t stream)
+{
+    const size_t smem = emb_regs_smem_bytes<R>();
+    auto kern = emb_interact_regs_kernel<R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_interact_fwd: %s", cudaGetErrorString(e));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRegWarps * kWarp, smem);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    const int64_t need = ((int64_t)B + kRegWarps - 1) / kRegWarps;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    const int blocks = (int)(need < cap ? need : cap);
+    kern<<<blocks, kRegWarps * kWarp, smem, stream>>>(ga, dense, B, pooled, out, P, status);
+    return check_launch("emb_interact_regs_kernel");
 }
 
 // Shapes the register kernel takes: fp32, D = 128, F in {8, 26}, rows of the
@@ -460,6 +669,27 @@ dlrm_status launch_ffma(const void* dense, const void* pooled, int F, int D, int
 }
 
 }  // namespace
+
+// fp32 lookup + interaction in one pass (pooled may be null); shapes as
+// regs_supported, plus 16-byte-aligned tables and pooled.
+bool regs_emb_interact_supported(int F, int D, int out_cols, const void* tables, const void* dense,
+                                 const void* pooled, const void* out)
+{
+    return regs_supported(F, D, out_cols, out) && aligned16(tables) && aligned16(dense) &&
+           (pooled == nullptr || aligned16(pooled));
+}
+
+dlrm_status regs_emb_interact_fwd(const float* tables, const int64_t* row_base, int F, int D, int B,
+                                  const int32_t* indices, const int32_t* offsets, int64_t nnz, const float* dense,
+                                  float* pooled, float* out, int out_cols, bool hash, uint32_t* status,
+                                  cudaStream_t stream)
+{
+    (void)D;
+    RegGather ga{tables, row_base, indices, offsets, nnz, hash};
+    return F == 26 ? launch_emb_regs<27>(ga, dense, B, pooled, out, out_cols, status, stream)
+                   : launch_emb_regs<9>(ga, dense, B, pooled, out, out_cols, status, stream);
+}
+
 }  // namespace dlrm
 
 using namespace dlrm;
@@ -506,4 +736,35 @@ extern "C" dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const vo
     cudaStream_t st = as_stream(stream);
     if (dtype == DLRM_F32) return launch_ffma<float>(d_dense, d_pooled, F, D, B, d_out, out_cols, nullptr, st);
     return launch_ffma<__half>(d_dense, d_pooled, F, D, B, d_out, out_cols, nullptr, st);
+}
+
+extern "C" dlrm_status dlrm_emb_interact_fwd_train(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                                   int F, int D, int B, const int32_t* d_indices,
+                                                   const int32_t* d_offsets, int64_t nnz, const void* d_dense,
+                                                   void* d_pooled, void* d_out, int out_cols, unsigned flags,
+                                                   uint32_t* d_status, void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: bad dtype");
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: need F >= 1, D >= 1, B >= 0");
+    if (nnz < 0 || nnz >= (int64_t)1 << 31 || (int64_t)F * B >= (int64_t)1 << 31)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: nnz and F*B must be below 2^31");
+    const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
+    if (out_cols < W)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: out_cols %d < D + F(F+1)/2 = %lld",
+                    out_cols, (long long)W);
+    if (!d_tables || !d_row_base || !d_offsets || !d_dense || !d_pooled || !d_out || (nnz > 0 && !d_indices))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: null device pointer");
+    if (flags & ~DLRM_FLAG_HASH_INDICES)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: unknown flag bits 0x%x", flags);
+    if (dtype != DLRM_F32 || !regs_emb_interact_supported(F, D, out_cols, d_tables, d_dense, d_pooled, d_out))
+        return fail(DLRM_ERR_UNSUPPORTED,
+                    "dlrm_emb_interact_fwd_train: needs fp32, D = 128, F in {8, 26}, out_cols a multiple of 4 "
+                    "without padding past the last group of 32 pairs, and 16-byte aligned pointers (use "
+                    "dlrm_emb_fwd + dlrm_interact_fwd otherwise)");
+    if (B == 0) return DLRM_OK;
+    return regs_emb_interact_fwd((const float*)d_tables, d_row_base, F, D, B, d_indices, d_offsets, nnz,
+                                 (const float*)d_dense, (float*)d_pooled, (float*)d_out, out_cols,
+                                 (flags & DLRM_FLAG_HASH_INDICES) != 0, d_status, as_stream(stream));
 }

@@ -580,9 +580,20 @@ extern "C" dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dt
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: null device pointer");
     if (flags & ~DLRM_FLAG_HASH_INDICES)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: unknown flag bits 0x%x", flags);
-    if (dtype != DLRM_F16 || !tc_interact_supported(F, D, out_cols, d_dense, d_dense, d_out) || !aligned16(d_tables))
+    if (dtype == DLRM_F32) {
+        if (!regs_emb_interact_supported(F, D, out_cols, d_tables, d_dense, nullptr, d_out))
+            return fail(DLRM_ERR_UNSUPPORTED,
+                        "dlrm_emb_interact_fwd: fp32 needs D = 128, F in {8, 26}, out_cols a multiple of 4 without "
+                        "padding past the last group of 32 pairs, and 16-byte aligned pointers (use dlrm_emb_fwd + "
+                        "dlrm_interact_fwd otherwise)");
+        if (B == 0) return DLRM_OK;
+        return regs_emb_interact_fwd((const float*)d_tables, d_row_base, F, D, B, d_indices, d_offsets, nnz,
+                                     (const float*)d_dense, nullptr, (float*)d_out, out_cols,
+                                     (flags & DLRM_FLAG_HASH_INDICES) != 0, d_status, as_stream(stream));
+    }
+    if (!tc_interact_supported(F, D, out_cols, d_dense, d_dense, d_out) || !aligned16(d_tables))
         return fail(DLRM_ERR_UNSUPPORTED,
-                    "dlrm_emb_interact_fwd: needs fp16, F <= 32, D a multiple of 64 up to 256, out_cols a multiple "
+                    "dlrm_emb_interact_fwd: fp16 needs F <= 32, D a multiple of 64 up to 256, out_cols a multiple "
                     "of 8 and 16-byte aligned pointers (use dlrm_emb_fwd + dlrm_interact_fwd otherwise)");
     if (B == 0) return DLRM_OK;
     GatherArgs ga;

@@ -144,17 +144,44 @@ dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const void* d_poole
  *   out[b] = dlrm_interact_fwd(dense[b], dlrm_emb_fwd(bags of sample b))
  *
  * Results are bit-identical to the two calls (bags of one index are copied,
- * larger bags are summed in fp32 in bag order and rounded once to fp16).
- * Arguments as in dlrm_emb_fwd and dlrm_interact_fwd.  Requires fp16,
- * F <= 32, D a multiple of 64 up to 256, out_cols a multiple of 8 and 16-byte
- * aligned tables, dense and out; otherwise DLRM_ERR_UNSUPPORTED (use the two
- * calls).  Status bits as in dlrm_emb_fwd, plus DLRM_STATUS_TIMEOUT.
+ * larger bags are summed in fp32 in bag order and rounded once to the table
+ * type).  Arguments as in dlrm_emb_fwd and dlrm_interact_fwd.  Shapes taken:
+ *   fp16: F <= 32, D a multiple of 64 up to 256, out_cols a multiple of 8
+ *         (tensor-core kernel);
+ *   fp32: D = 128, F in {8, 26}, out_cols a multiple of 4 and at most
+ *         D + 32 * ceil(F(F+1)/2 / 32) (480 for F = 26) (CUDA-core kernel);
+ * with 16-byte aligned tables, dense and out; otherwise DLRM_ERR_UNSUPPORTED
+ * (use the two calls).  Status bits as in dlrm_emb_fwd, plus
+ * DLRM_STATUS_TIMEOUT.
  */
 dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
                                   int F, int D, int B, const int32_t* d_indices,
                                   const int32_t* d_offsets, int64_t nnz, const void* d_dense,
                                   void* d_out, int out_cols, unsigned flags, uint32_t* d_status,
                                   void* stream);
+
+/*
+ * dlrm_emb_interact_fwd_train -- the training forward in one pass:
+ * dlrm_emb_fwd and dlrm_interact_fwd, also writing the pooled tensor that
+ * dlrm_interact_bwd and dlrm_emb_bwd_sgd take.  (The same two operations:
+ * "DLRM For PyTorch", §Model architecture.)
+ *
+ *   d_pooled[b] = dlrm_emb_fwd(bags of sample b)                (output)
+ *   d_out[b]    = dlrm_interact_fwd(dense[b], d_pooled[b])      (output)
+ *
+ * Both are bit-identical to the two calls; the pooled rows are written once
+ * and not read back from memory.  Arguments as in dlrm_emb_fwd and
+ * dlrm_interact_fwd.  Requires fp32 tables, D = 128, F in {8, 26}, out_cols a
+ * multiple of 4 and at most D + 32 * ceil(F(F+1)/2 / 32) (480 for F = 26),
+ * 16-byte aligned tables, dense, pooled and out; otherwise
+ * DLRM_ERR_UNSUPPORTED (use the two calls).  Flags: DLRM_FLAG_HASH_INDICES.
+ * Status bits as in dlrm_emb_fwd.
+ */
+dlrm_status dlrm_emb_interact_fwd_train(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                        int F, int D, int B, const int32_t* d_indices,
+                                        const int32_t* d_offsets, int64_t nnz, const void* d_dense,
+                                        void* d_pooled, void* d_out, int out_cols, unsigned flags,
+                                        uint32_t* d_status, void* stream);
 
 /*
  * dlrm_interact_bwd -- gradient of dlrm_interact_fwd.

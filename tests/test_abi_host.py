@@ -85,6 +85,30 @@ def test_interact_validation(L):
     assert h(FAKE, FAKE, 0, 2, 4, 8, FAKE, 6, None) == dl.DLRM_ERR_INVALID_ARG
 
 
+def test_fused_training_forward_validation(L):
+    f = L.dlrm_emb_interact_fwd_train
+    # tables, dtype, row_base, F, D, B, indices, offsets, nnz, dense, pooled, out, out_cols, flags, status, stream
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 478, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert "out_cols" in _err(L)
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, None, FAKE, 480, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 480, 8, None, None) == dl.DLRM_ERR_INVALID_ARG
+    # fp16 tables, other F, D, padding past the last group of pairs, misalignment: the two calls instead
+    assert f(FAKE, 1, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 25, 128, 8, FAKE, FAKE, 200, FAKE, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 64, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 484, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 482, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE_MIS, FAKE, 480, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE_MIS, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    # empty batch: nothing to do, returns before any CUDA call
+    assert f(FAKE, 0, FAKE, 26, 128, 0, None, FAKE, 0, FAKE, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_OK
+    assert f(FAKE, 0, FAKE, 8, 128, 0, None, FAKE, 0, FAKE, FAKE, FAKE, 164, 1, None, None) == dl.DLRM_OK
+    # the inference entry takes the same fp32 shapes (no pooled output)
+    g = L.dlrm_emb_interact_fwd
+    assert g(FAKE, 0, FAKE, 3, 16, 8, FAKE, FAKE, 24, FAKE, FAKE, 22, 0, None, None) == dl.DLRM_ERR_UNSUPPORTED
+    assert g(FAKE, 0, FAKE, 26, 128, 0, None, FAKE, 0, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_OK
+
+
 def test_sgd_workspace_and_validation(L):
     ws = L.dlrm_emb_bwd_sgd_workspace_size
     assert ws(-1, 128, 10) == 0 and ws(10, 3, 10) == 0 and ws(10, 128, 0) == 0

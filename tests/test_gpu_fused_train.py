@@ -1,0 +1,126 @@
+"""GPU parity of the fp32 lookup + interaction in one pass: the training
+forward dlrm_emb_interact_fwd_train (pooled rows written for the backward)
+and dlrm_emb_interact_fwd with fp32 tables (no pooled output).
+
+Both compute what dlrm_emb_fwd followed by dlrm_interact_fwd computes, with
+the same arithmetic in the same order, so pooled rows, interaction output and
+status bits are compared bit for bit with the two calls (whose oracle parity
+test_gpu_lookup and test_gpu_interaction establish); one oracle comparison on
+sampled rows is made here directly as well.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dlrm_embeddings_dot_gb300 import inputs
+from gpu_util import Compact, dev, device_tables, to_dev
+from helpers import assert_within_abs_sum
+from test_gpu_interaction import abs_products
+
+pytestmark = pytest.mark.gpu
+
+
+def two_calls(dl, tab, row_base, F, D, B, idx, off, dense, P, flags=0):
+    pooled = torch.full((B, F, D), float("nan"), device=dev())
+    out = torch.full((B, P), float("nan"), device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    dl.dlrm_emb_fwd(tab, row_base, F, D, B, idx, off, pooled, flags=flags, status=st)
+    dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=st)
+    torch.cuda.synchronize()
+    return pooled.cpu().numpy(), out.cpu().numpy(), int(st.item())
+
+
+def fused_train(dl, tab, row_base, F, D, B, idx, off, dense, P, flags=0):
+    pooled = torch.full((B, F, D), float("nan"), device=dev())
+    out = torch.full((B, P), float("nan"), device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    dl.dlrm_emb_interact_fwd_train(tab, row_base, F, D, B, idx, off, dense, pooled, out, P, flags=flags, status=st)
+    torch.cuda.synchronize()
+    return pooled.cpu().numpy(), out.cpu().numpy(), int(st.item())
+
+
+def fused_infer(dl, tab, row_base, F, D, B, idx, off, dense, P, flags=0):
+    out = torch.full((B, P), float("nan"), device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    dl.dlrm_emb_interact_fwd(tab, row_base, F, D, B, idx, off, dense, out, P, flags=flags, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(st.item())
+
+
+def _same(a, b):
+    """Bit equality (NaN patterns included)."""
+    return a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("B", [1, 5, 1021, 4099, 65536])
+def test_default_shapes_match_two_calls_and_oracle(cuda_lib, B):
+    """F = 26, D = 128, 480 columns, Zipf 1.2 single-hot fp32 (the training
+    shapes); B past 1824 gives every warp several samples, so the staging of
+    the next sample behind the current one is exercised."""
+    w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=1.2, train=True)
+    tab = device_tables(cuda_lib, w)
+    args = (tab, to_dev(w.row_base), w.F, w.D, w.B, to_dev(w.indices), to_dev(w.offsets), to_dev(w.dense),
+            w.out_cols)
+    p2, o2, s2 = two_calls(cuda_lib, *args)
+    p1, o1, s1 = fused_train(cuda_lib, *args)
+    oi, si = fused_infer(cuda_lib, *args)
+    assert s1 == s2 == si == 0
+    assert _same(p1, p2) and _same(o1, o2) and _same(oi, o2)
+    samples = np.unique(np.concatenate([np.arange(min(B, 8)), [B // 2, B - 1]]))
+    c = Compact(w, samples)
+    rp, _ = oracle.emb_fwd(c.tables, c.row_base, c.F, c.D, c.B, c.indices, c.offsets)
+    assert np.array_equal(p1[samples], rp), "single-hot fp32 pooling is a copy of the row"
+    ro = oracle.interact_fwd(c.dense, rp, w.out_cols)
+    W = w.D + w.F * (w.F + 1) // 2
+    assert np.array_equal(o1[samples][:, :w.D], c.dense)
+    assert not o1[samples][:, W:].any()
+    assert_within_abs_sum(o1[samples][:, :W], ro[:, :W], abs_products(c.dense, rp), 1e-5, "fused vs oracle")
+
+
+@pytest.mark.parametrize("F,P", [(26, 480), (8, 164), (8, 192)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_ragged_bags_hashing_and_skips(cuda_lib, F, P, flags):
+    """Empty bags, bags of several indices, indices outside the table (skipped
+    with the status bit, or folded with DLRM_FLAG_HASH_INDICES)."""
+    rng = np.random.default_rng(F * 11 + P + flags)
+    B, D = 2111, 128
+    rows = rng.integers(1, 50, size=F)
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tab = to_dev(rng.standard_normal((row_base[-1], D)).astype(np.float32))
+    counts = rng.choice([0, 1, 1, 1, 2, 5], size=F * B)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    idx = rng.integers(-60, 60, size=off[-1]).astype(np.int32)
+    dense = to_dev(rng.standard_normal((B, D)).astype(np.float32))
+    args = (tab, to_dev(row_base), F, D, B, to_dev(idx), to_dev(off), dense, P, flags)
+    p2, o2, s2 = two_calls(cuda_lib, *args)
+    p1, o1, s1 = fused_train(cuda_lib, *args)
+    oi, si = fused_infer(cuda_lib, *args)
+    assert s1 == s2 == si
+    assert (s1 & cuda_lib.DLRM_STATUS_OOB_INDEX) == (0 if flags else cuda_lib.DLRM_STATUS_OOB_INDEX)
+    assert _same(p1, p2) and _same(o1, o2) and _same(oi, o2)
+    # and directly against the oracle on a few samples
+    tables = tab.cpu().numpy()
+    ref_p, ref_s = oracle.emb_fwd(tables, row_base, F, D, B, idx, off, flags=flags)
+    absum, _ = oracle.emb_fwd(np.abs(tables), row_base, F, D, B, idx, off, flags=flags)
+    assert ref_s == s1
+    assert_within_abs_sum(p1, ref_p, absum.astype(np.float64), 1e-5, "pooled vs oracle")
+
+
+def test_malformed_offsets_are_clamped_like_the_lookup(cuda_lib):
+    rng = np.random.default_rng(5)
+    F, D, B, P = 26, 128, 300, 480
+    rows = np.full(F, 40)
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tab = to_dev(rng.standard_normal((row_base[-1], D)).astype(np.float32))
+    off = np.arange(F * B + 1, dtype=np.int32)
+    off[17] = 5                     # decreasing
+    off[400] = 10**6                # past nnz
+    idx = rng.integers(0, 40, size=F * B).astype(np.int32)
+    dense = to_dev(rng.standard_normal((B, D)).astype(np.float32))
+    args = (tab, to_dev(row_base), F, D, B, to_dev(idx), to_dev(off), dense, P)
+    p2, o2, s2 = two_calls(cuda_lib, *args)
+    p1, o1, s1 = fused_train(cuda_lib, *args)
+    assert s1 == s2 and s1 & cuda_lib.DLRM_STATUS_BAD_OFFSETS
+    assert _same(p1, p2) and _same(o1, o2)
