@@ -166,11 +166,16 @@ def cpu_baseline(w, n_samples: int) -> dict:
 
 
 # ------------------------------------------------------------- GPU benchmark
-def kernels_per_step(total_rows: int) -> int:
+def sgd_kernels(total_rows: int) -> int:
+    """Kernels of one dlrm_emb_bwd_sgd call: keys, 3 per radix pass, segment, two fixups."""
     nbits = int(total_rows).bit_length()
     npasses = (nbits + 7) // 8
-    # emb_fwd, interact_fwd, interact_bwd, then keys + 3 per radix pass + segment + two fixups
-    return 3 + 1 + 3 * npasses + 3
+    return 1 + 3 * npasses + 3
+
+
+def kernels_per_step(total_rows: int) -> int:
+    # the one-pass training forward, interact_bwd, then the sparse SGD's kernels
+    return 2 + sgd_kernels(total_rows)
 
 
 def run_ours(args) -> None:
@@ -210,26 +215,25 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     nnz = w.nnz
 
-    ev = {k: [] for k in ("emb_fwd", "interact_fwd", "interact_bwd", "emb_bwd_sgd")}
+    ev = {k: [] for k in ("emb_interact_fwd", "interact_bwd", "emb_bwd_sgd")}
 
     def step(record=False):
         marks = []
         if record:
-            marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             marks[0].record(stream)
-        dl.dlrm_emb_fwd(tables, row_base, F, D, B, idx, off, pooled, status=status, stream=stream)
+        # lookup + interaction in one pass; the pooled rows are written for the backward
+        dl.dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, idx, off, dense, pooled, out, P, status=status,
+                                       stream=stream)
         if record:
             marks[1].record(stream)
-        dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)
-        if record:
-            marks[2].record(stream)
         dl.dlrm_interact_bwd(grad_out, dense, pooled, F, D, B, P, gd, gp, stream=stream)
         if record:
-            marks[3].record(stream)
+            marks[2].record(stream)
         dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status,
                             stream=stream)
         if record:
-            marks[4].record(stream)
+            marks[3].record(stream)
             for k, (a, b) in zip(ev, zip(marks[:-1], marks[1:])):
                 ev[k].append((a, b))
 
@@ -243,6 +247,20 @@ def run_ours(args) -> None:
         step(record=True)
     torch.cuda.synchronize()
     op_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+
+    # ---- the same forward as the two separate calls (context for the one-pass forward)
+    two = []
+    for _ in range(max(5, min(args.steps, 50))):
+        m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        m[0].record(stream)
+        dl.dlrm_emb_fwd(tables, row_base, F, D, B, idx, off, pooled, status=status, stream=stream)
+        m[1].record(stream)
+        dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)
+        m[2].record(stream)
+        two.append(m)
+    torch.cuda.synchronize()
+    two_ms = {"emb_fwd": statistics.mean(m[0].elapsed_time(m[1]) for m in two),
+              "interact_fwd": statistics.mean(m[1].elapsed_time(m[2]) for m in two)}
 
     # ---- timed region (inputs > L2: the 4.1 GB tables and 0.9 GB pooled/grad tensors)
     clocks = ClockSampler(local)
@@ -378,15 +396,14 @@ def run_ours(args) -> None:
         unique_rows = int(torch.unique_consecutive(k).numel())
     s = 4  # fp32
     alg = {
-        "emb_fwd": B * F * (4 + 4 + D * s) + B * F * D * s,
-        "interact_fwd": B * (D * s + F * D * s + P * s),
+        # offsets + index + row read per lookup, pooled row written once; dense read, output written
+        "emb_interact_fwd": B * F * (4 + 4 + D * s) + B * F * D * s + B * (D * s + P * s),
         "interact_bwd": B * (P * 4 + D * s + F * D * s + D * 4 + F * D * 4),
         "emb_bwd_sgd": nnz * (4 + 4 + D * 4) + (unique_rows or 0) * 2 * D * 4,
     }
     dom = max(op_ms, key=op_ms.get)
-    kernel_names = {"emb_fwd": "emb_fwd_single_kernel", "interact_fwd": "interact_fwd_regs_kernel",
-                    "interact_bwd": "interact_bwd_kernel",
-                    "emb_bwd_sgd": f"emb_bwd_sgd ({kernels_per_step(w.total_rows) - 3} kernels)"}
+    kernel_names = {"emb_interact_fwd": "emb_interact_regs_kernel", "interact_bwd": "interact_bwd_kernel",
+                    "emb_bwd_sgd": f"emb_bwd_sgd ({sgd_kernels(w.total_rows)} kernels)"}
     achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
@@ -404,6 +421,7 @@ def run_ours(args) -> None:
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (4.1 GB tables, 0.87 GB pooled/grad tensors per step)"},
         "ops_ms": {k: round(v, 4) for k, v in op_ms.items()},
+        "fwd_two_calls_ms": {k: round(v, 4) for k, v in two_ms.items()},
         "fwd": {"value": round(B * world * args.steps / (fms / 1e3), 1), "unit": "samples/s",
                 "ms_per_step": round(fms / args.steps, 4), "dtype": "f16 storage, f32 accumulate",
                 "workload": "dlrm-default 64K forward: 26 single-hot fp16 tables, Zipf 1.05, 480 columns",
@@ -488,12 +506,17 @@ def run_op(args) -> None:
 
         dense16 = torch.from_numpy(w.dense.astype(np.float16)).to(dev) if dt == inputs.F16 else None
         out16 = torch.empty(B, P, dtype=torch.float16, device=dev) if dt == inputs.F16 else None
+        dense32 = torch.from_numpy(w.dense).to(dev) if dt == inputs.F32 else None
+        out32 = torch.empty(B, P, device=dev) if dt == inputs.F32 else None
 
         def once():
             if args.op == "emb_bwd_sgd":
                 dl.dlrm_emb_bwd_sgd(tables, rb, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status)
             elif args.op == "emb_interact16":
                 dl.dlrm_emb_interact_fwd(tables, rb, F, D, B, idx, off, dense16, out16, P, status=status)
+            elif args.op == "emb_interact_train":
+                dl.dlrm_emb_interact_fwd_train(tables, rb, F, D, B, idx, off, dense32, pooled, out32, P,
+                                               status=status)
             else:
                 dl.dlrm_emb_fwd(tables, rb, F, D, B, idx, off, pooled, status=status)
     for _ in range(args.warmup):
@@ -714,6 +737,14 @@ def run_config(args, name) -> None:
             ops.append(("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, Bw, idx, off, gp,
                                                                    w.lr, ws, status=status, stream=stream)))
         per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
+        fused_train = None
+        if train and not multi and tt == torch.float32 and F in (8, 26) and D == 128:
+            fops = [("emb_interact_fwd_train",
+                     lambda: dl.dlrm_emb_interact_fwd_train(tab, rb, F, D, Bw, idx, off, dense, pooled, out, P,
+                                                            status=status, stream=stream))] + ops[2:]
+            fper, fms = _time_ops(torch, stream, fops, args.steps, args.warmup)
+            fused_train = {"ms_per_step": round(fms, 4), "step_samples_per_s": round(Bw / (fms / 1e3), 1),
+                           "ops_ms": {k: round(v, 4) for k, v in fper.items()}}
         fused_ms = None
         if tt == torch.float16 and not train:
             fop = [("emb_interact_fwd", lambda: dl.dlrm_emb_interact_fwd(tab, rb, F, D, Bw, idx, off, dense, out, P,
@@ -730,6 +761,8 @@ def run_config(args, name) -> None:
                 "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
                 "fwd_samples_per_s": round(Bw / (fwd_ms / 1e3), 1),
                 "step_samples_per_s": round(Bw / (ms / 1e3), 1), "device_status": int(status.item())}
+        if fused_train is not None:
+            line["one_pass_forward"] = fused_train
         if fused_ms is not None:
             line["fused_fwd"] = {"ms": round(fused_ms, 4), "samples_per_s": round(Bw / (fused_ms / 1e3), 1),
                                  "alg_GBps": round(Bw * (F * (8 + D * 2) + D * 2 + P * 2) / (fused_ms / 1e3) / 1e9,
@@ -782,7 +815,7 @@ def main(argv=None) -> None:
                     help="measure one of the pages' workloads instead of the headline step (repeatable)")
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",
                                      "interact_bwd16",
-                                     "emb_bwd_sgd", "emb_interact16"],
+                                     "emb_bwd_sgd", "emb_interact16", "emb_interact_train"],
                     help="time one entry point alone on the DLRM-default shapes (used for ncu captures)")
     ap.add_argument("--small-tables", action="store_true",
                     help="with --op: tables with 10x fewer rows (log-uniform in [10, 4e5])")
