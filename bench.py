@@ -402,7 +402,7 @@ def run_ours(args) -> None:
         "emb_bwd_sgd": nnz * (4 + 4 + D * 4) + (unique_rows or 0) * 2 * D * 4,
     }
     dom = max(op_ms, key=op_ms.get)
-    kernel_names = {"emb_interact_fwd": "emb_interact_regs_kernel", "interact_bwd": "interact_bwd_kernel",
+    kernel_names = {"emb_interact_fwd": "emb_interact_regs_kernel", "interact_bwd": "interact_bwd_regs_kernel",
                     "emb_bwd_sgd": f"emb_bwd_sgd ({sgd_kernels(w.total_rows)} kernels)"}
     achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),

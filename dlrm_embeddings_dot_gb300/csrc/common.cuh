@@ -6,6 +6,8 @@
 #include <stdint.h>
 
 #include <cstdarg>
+#include <type_traits>
+#include <utility>
 #include <cstdio>
 
 #include "dlrm.h"
@@ -119,6 +121,20 @@ __device__ __forceinline__ uint4 f8_to_h8(const float* f)
 #pragma unroll
     for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
     return v;
+}
+
+template <typename Fn, int... Is>
+__device__ __forceinline__ void static_for_impl(Fn& fn, std::integer_sequence<int, Is...>)
+{
+    (fn(std::integral_constant<int, Is>{}), ...);
+}
+
+// fn(std::integral_constant<int, 0>), ..., fn(std::integral_constant<int, N-1>):
+// every index is a constant expression, so register arrays stay in registers.
+template <int N, typename Fn>
+__device__ __forceinline__ void static_for(Fn&& fn)
+{
+    static_for_impl(fn, std::make_integer_sequence<int, N>{});
 }
 
 }  // namespace dlrm

@@ -14,6 +14,7 @@
 // over j (fixed order).  Outputs are 16-byte stores, 512 contiguous bytes per
 // warp.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace dlrm {
 namespace {
@@ -169,6 +170,160 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
     }
 }
 
+// ------------------------------------------------------------ register kernel
+// fp32, D = 128, R = F + 1 rows known at compile time.  One warp per sample;
+// lane l holds features 4l..4l+3 of every row of Z in registers.  The sample
+// arrives by three bulk copies on the warp's mbarrier (dense row, the F
+// pooled rows, the upstream gradient row); the lanes expand G's triangle
+// into M (one triangle element per lane per step, through a pair table
+// built once per block), and output row i is an fp32 FMA chain over j in
+// ascending order, with M's rows read by broadcast float4 loads.  The next
+// sample's copies are issued as soon as this one's buffer has been read.
+constexpr int kRegD = 128;
+
+template <int R>
+struct RegBwd {
+    static constexpr int NP = R * (R - 1) / 2;             // triangle elements
+    static constexpr int RS = (R + 3) / 4 * 4;             // M row stride
+    static constexpr int z_bytes = R * kRegD * 4;
+    static constexpr int m_bytes = R * RS * 4;
+    // per-warp bytes for a gradient row of P floats
+    __host__ __device__ static constexpr int warp_bytes(int P) { return z_bytes + (P * 4 + 15) / 16 * 16 + m_bytes; }
+    // per-block bytes: warps, the pair table, the mbarriers
+    __host__ __device__ static constexpr int block_bytes(int P)
+    {
+        return kWarps * warp_bytes(P) + (NP * 2 + 15) / 16 * 16 + kWarps * 8;
+    }
+};
+
+template <int R>
+__global__ void __launch_bounds__(kWarps * kWarp, 3)
+interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __restrict__ dense,
+                         const float* __restrict__ pooled, int B, int P, float* __restrict__ grad_dense,
+                         float* __restrict__ grad_pooled, uint32_t* __restrict__ status)
+{
+    using L = RegBwd<R>;
+    constexpr int F = R - 1, D = kRegD, RS = L::RS, NP = L::NP;
+    extern __shared__ __align__(16) unsigned char bwd_regs_raw[];
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int wb = L::warp_bytes(P);
+    unsigned char* base = bwd_regs_raw + (size_t)warp * wb;
+    float4* zs = reinterpret_cast<float4*>(base);                       // [R][32] float4
+    float* gs = reinterpret_cast<float*>(base + L::z_bytes);             // [P]
+    float* M = reinterpret_cast<float*>(base + L::z_bytes + (P * 4 + 15) / 16 * 16);
+    uint16_t* pair_ij = reinterpret_cast<uint16_t*>(bwd_regs_raw + (size_t)kWarps * wb);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(bwd_regs_raw + (size_t)kWarps * wb + (NP * 2 + 15) / 16 * 16) + warp;
+
+    // pair table (i << 8 | j for triangle element p), M's diagonal stays zero
+    for (int p = threadIdx.x; p < NP; p += blockDim.x) {
+        int i = 1;
+        while (i * (i + 1) / 2 <= p) ++i;
+        pair_ij[p] = (uint16_t)(i << 8 | (p - i * (i - 1) / 2));
+    }
+    for (int x = lane; x < R * RS; x += kWarp) M[x] = 0.f;
+    if (lane == 0) {
+        tc::mbar_init(bar, 1);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int64_t stride = (int64_t)gridDim.x * kWarps;
+    int64_t b = (int64_t)blockIdx.x * kWarps + warp;
+    auto stage = [&](int64_t smp) {
+        if (lane == 0) {
+            tc::mbar_expect_tx(bar, R * D * 4 + P * 4);
+            tc::bulk_g2s(zs, dense + smp * D, D * 4, bar);
+            tc::bulk_g2s(zs + kWarp, pooled + smp * (int64_t)F * D, F * D * 4, bar);
+            tc::bulk_g2s(gs, grad_out + smp * P, P * 4, bar);
+        }
+    };
+    uint32_t phase = 0;
+    if (b < B) stage(b);
+    for (; b < B; b += stride) {
+        if (!tc::bounded_wait(bar, phase)) {
+            if (lane == 0) set_status(status, DLRM_STATUS_TIMEOUT);
+            return;
+        }
+        phase ^= 1u;
+        // G's triangle into both halves of M
+#pragma unroll
+        for (int k = 0; k < (NP + kWarp - 1) / kWarp; ++k) {
+            const int p = k * kWarp + lane;
+            if (p < NP) {
+                const float v = gs[D + p];
+                const int ij = pair_ij[p];
+                const int i = ij >> 8, j = ij & 0xff;
+                M[i * RS + j] = v;
+                M[j * RS + i] = v;
+            }
+        }
+        float4 z[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) z[r] = zs[r * kWarp + lane];
+        const float4 g0 = reinterpret_cast<const float4*>(gs)[lane];
+        // M complete for every lane; the staging buffer has been read
+        __syncwarp();
+        if (b + stride < B) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            stage(b + stride);
+        }
+        // a rolled loop over the rows keeps the code small (the diagonal of M
+        // is zero, so j = i adds an exact zero product)
+#pragma unroll 1
+        for (int i = 0; i < R; ++i) {
+            const float4* mrow = reinterpret_cast<const float4*>(M + i * RS);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            static_for<RS / 4>([&](auto J4) {
+                constexpr int j0 = 4 * decltype(J4)::value;
+                const float4 c = mrow[j0 / 4];
+                if constexpr (j0 + 0 < R) fma4(acc, c.x, z[j0 + 0 < R ? j0 + 0 : 0]);
+                if constexpr (j0 + 1 < R) fma4(acc, c.y, z[j0 + 1 < R ? j0 + 1 : 0]);
+                if constexpr (j0 + 2 < R) fma4(acc, c.z, z[j0 + 2 < R ? j0 + 2 : 0]);
+                if constexpr (j0 + 3 < R) fma4(acc, c.w, z[j0 + 3 < R ? j0 + 3 : 0]);
+            });
+            float* dst;
+            if (i == 0) {
+                acc.x += g0.x;
+                acc.y += g0.y;
+                acc.z += g0.z;
+                acc.w += g0.w;
+                dst = grad_dense + b * D;
+            } else {
+                dst = grad_pooled + (b * F + (i - 1)) * D;
+            }
+            reinterpret_cast<float4*>(dst)[lane] = acc;
+        }
+        __syncwarp();   // M is rebuilt for the next sample
+    }
+}
+
+template <int R>
+dlrm_status launch_regs(const float* grad_out, const float* dense, const float* pooled, int B, int P, float* gd,
+                        float* gp, uint32_t* status, cudaStream_t stream)
+{
+    const size_t smem = (size_t)RegBwd<R>::block_bytes(P);
+    auto kern = interact_bwd_regs_kernel<R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_bwd: %s", cudaGetErrorString(e));
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * kWarp, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    if (blocks > cap) blocks = cap;
+    kern<<<(int)blocks, kWarps * kWarp, smem, stream>>>(grad_out, dense, pooled, B, P, gd, gp, status);
+    return check_launch("interact_bwd_regs_kernel");
+}
+
+// Shapes the register kernel takes: fp32, D = 128, F in {8, 26}, gradient
+// rows of a multiple of 4 floats, at most 1024 columns.
+inline bool regs_bwd_supported(int F, int D, int P)
+{
+    return D == kRegD && (F == 8 || F == 26) && P % 4 == 0 && P <= 1024;
+}
+
 template <typename T, int RMAX>
 dlrm_status launch(const float* grad_out, const void* dense, const void* pooled, int F, int D, int B, int P,
                    float* gd, float* gp, cudaStream_t stream)
@@ -231,6 +386,12 @@ extern "C" dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_interact_bwd: pointers must be 16-byte aligned");
     if (B == 0) return DLRM_OK;
     cudaStream_t st = as_stream(stream);
+    if (dtype == DLRM_F32 && regs_bwd_supported(F, D, out_cols)) {
+        const float* d = static_cast<const float*>(d_dense);
+        const float* p = static_cast<const float*>(d_pooled);
+        return F == 26 ? launch_regs<27>(d_grad_out, d, p, B, out_cols, d_grad_dense, d_grad_pooled, nullptr, st)
+                       : launch_regs<9>(d_grad_out, d, p, B, out_cols, d_grad_dense, d_grad_pooled, nullptr, st);
+    }
     if (dtype == DLRM_F32)
         return dispatch<float>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);
     return dispatch<__half>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);

@@ -248,20 +248,6 @@ constexpr int kRegWarps = 4;     // warps per CTA, one sample each at a time
 constexpr int kRegD = 128;       // 32 lanes x 4 features
 constexpr int kPitch = 36;       // floats per row of the transpose scratch
 
-template <typename Fn, int... Is>
-__device__ __forceinline__ void static_for_impl(Fn& fn, std::integer_sequence<int, Is...>)
-{
-    (fn(std::integral_constant<int, Is>{}), ...);
-}
-
-// fn(std::integral_constant<int, 0>), ..., fn(std::integral_constant<int, N-1>):
-// every index is a constant expression, so register arrays stay in registers.
-template <int N, typename Fn>
-__device__ __forceinline__ void static_for(Fn&& fn)
-{
-    static_for_impl(fn, std::make_integer_sequence<int, N>{});
-}
-
 // Pair p of the strict lower triangle in row-major order: p = i(i-1)/2 + j.
 constexpr int pair_row(int p)
 {
@@ -286,42 +272,6 @@ __device__ __forceinline__ float slot_dot(const float4 (&z)[R])
     } else {
         return 0.f;
     }
-}
-
-// Adds `bytes` to the transaction count of the barrier's current phase (no arrival).
-__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// One bulk (non-tensor) copy shared -> global in the thread's bulk group.
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(tc::smem_u32(src)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// One bulk (non-tensor) copy global -> shared, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     tc::smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-                 : "memory");
-}
-
-// Bounded wait for the phase of `parity`; false when the bound is hit, after
-// a bounded drain of the copy in flight.
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity)
-{
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (clock64() - t0 < tc::kWaitCycles)
-        if (tc::mbar_try_wait(bar, parity)) return true;
-    tc::mbar_drain(bar, parity);
-    return false;
 }
 
 // Shared memory of one CTA: [kRegWarps][R rows][D floats] sample buffers,
@@ -389,8 +339,8 @@ interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restric
     auto stage = [&](int64_t s) {
         if (lane == 0) {
             tc::mbar_expect_tx(bar, R * D * 4);
-            bulk_g2s(mine, dense + s * D, D * 4, bar);
-            bulk_g2s(mine + kWarp, pooled + s * (int64_t)(R - 1) * D, (R - 1) * D * 4, bar);
+            tc::bulk_g2s(mine, dense + s * D, D * 4, bar);
+            tc::bulk_g2s(mine + kWarp, pooled + s * (int64_t)(R - 1) * D, (R - 1) * D * 4, bar);
         }
     };
     if (lane == 0) {
@@ -401,7 +351,7 @@ interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restric
     uint32_t phase = 0;
     if (b < B) stage(b);
     for (; b < B; b += stride) {
-        if (!bounded_wait(bar, phase)) {
+        if (!tc::bounded_wait(bar, phase)) {
             if (lane == 0) set_status(status, DLRM_STATUS_TIMEOUT);
             return;
         }
@@ -520,11 +470,11 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
     // own 16-byte column); lane 0 arrives once all copies are counted.
     auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
         if (lane < F && src_row < kRowMulti) {
-            mbar_expect_tx_only(bar, D * 4);
-            bulk_g2s(mine + (lane + 1) * kWarp, ga.tables + (size_t)src_row * D, D * 4, bar);
+            tc::mbar_expect_tx_only(bar, D * 4);
+            tc::bulk_g2s(mine + (lane + 1) * kWarp, ga.tables + (size_t)src_row * D, D * 4, bar);
         } else if (lane == F) {
-            mbar_expect_tx_only(bar, D * 4);
-            bulk_g2s(mine, dense + smp * D, D * 4, bar);
+            tc::mbar_expect_tx_only(bar, D * 4);
+            tc::bulk_g2s(mine, dense + smp * D, D * 4, bar);
         }
         for (uint32_t zero = __ballot_sync(0xffffffffu, lane < F && src_row == kRowZero); zero; zero &= zero - 1)
             mine[__ffs(zero) * kWarp + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -570,7 +520,7 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
         const int idx1 = (lane < F && e1 - a1 == 1) ? ldg_early_s32(ga.indices + a1) : 0;
         int a2, e2;
         load_bounds(nb + stride, a2, e2);
-        if (!bounded_wait(bar, phase)) {
+        if (!tc::bounded_wait(bar, phase)) {
             if (lane == 0) {
                 set_status(status, DLRM_STATUS_TIMEOUT);
                 if (kPooled) tc::bulk_wait_all();
@@ -586,7 +536,7 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-                bulk_s2g(pooled + b * (int64_t)F * D, mine + kWarp, F * D * 4);
+                tc::bulk_s2g(pooled + b * (int64_t)F * D, mine + kWarp, F * D * 4);
                 tc::bulk_commit();
             }
         }

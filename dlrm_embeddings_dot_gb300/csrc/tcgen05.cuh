@@ -1,6 +1,6 @@
-// tcgen05.cuh -- inline-PTX helpers for the Blackwell tensor-core kernels:
-// mbarriers with bounded waits, TMA tensor loads, tcgen05 MMA / commit / TMEM
-// loads, the 128-byte-swizzle K-major shared-memory descriptor, and the
+// tcgen05.cuh -- inline-PTX helpers for the Blackwell kernels: mbarriers
+// with bounded waits, bulk copies, TMA tensor loads, tcgen05 MMA / commit /
+// TMEM loads, the 128-byte-swizzle K-major shared-memory descriptor, and the
 // driver's tensor-map encoder.
 #pragma once
 
@@ -68,6 +68,42 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity)
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitCycles) {
     }
+}
+
+// Adds `bytes` to the transaction count of the barrier's current phase (no arrival).
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk (non-tensor) copy shared -> global in the thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// One bulk (non-tensor) copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Bounded wait for the phase of `parity`; false when the bound is hit, after
+// a bounded drain of the copy in flight.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (clock64() - t0 < kWaitCycles)
+        if (mbar_try_wait(bar, parity)) return true;
+    mbar_drain(bar, parity);
+    return false;
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,

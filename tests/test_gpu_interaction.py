@@ -141,7 +141,11 @@ def abs_bwd(G, dense, pooled):
 
 
 @pytest.mark.parametrize("F,D,P,B", [(3, 16, 22, 256), (26, 128, 480, 513), (1, 32, 40, 9),
-                                     (15, 64, 200, 33), (31, 128, 640, 17)])
+                                     (15, 64, 200, 33), (31, 128, 640, 17),
+                                     # fp32: the register kernel (F in {8, 26}, D = 128, P % 4 == 0), with
+                                     # several samples per warp past 1824, and the staged kernel for P % 4 != 0
+                                     (26, 128, 480, 4099), (26, 128, 1024, 37), (8, 128, 164, 2000),
+                                     (26, 128, 481, 70)])
 @pytest.mark.parametrize("dt", [np.float32, np.float16])
 def test_backward(cuda_lib, F, D, P, B, dt):
     rng = np.random.default_rng(F * D + B)
