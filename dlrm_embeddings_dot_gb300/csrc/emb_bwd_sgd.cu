@@ -290,6 +290,9 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
                int64_t nchunks, int64_t nbags)
 {
+    // positions per batch: their gradient rows, and the table rows of the runs
+    // that end (complete) among them, are all loaded before any is used
+    constexpr int U = MC >= 8 ? 1 : 8 / MC;
     const int lane = threadIdx.x % kWarp;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
@@ -302,71 +305,88 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
         uint32_t prev = __shfl_up_sync(0xffffffffu, key, 1);
         if (lane == 0) prev = p0 > 0 ? keys[p0 - 1] : ~key;
         const uint32_t after = (p0 + kChunk < n) ? keys[p0 + kChunk] : kSkipKey;
+        uint32_t next = __shfl_down_sync(0xffffffffu, key, 1);
+        if (lane == kWarp - 1) next = after;
         const bool valid = key != kSkipKey;
         const uint32_t heads = __ballot_sync(0xffffffffu, valid && prev != key);
         const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
         if (vmask == 0) continue;
         const int nvalid = 32 - __clz(vmask);             // valid lanes are a prefix
-        uint32_t starts = heads | 1u;                     // lane 0 starts a run piece
-        while (starts) {
-            const int s = __ffs(starts) - 1;
-            starts &= starts - 1;
-            if (s >= nvalid) break;
-            const int e = starts ? min(__ffs(starts) - 1, nvalid) : nvalid;
-            const uint32_t skey = __shfl_sync(0xffffffffu, key, s);
-            float4 acc[MC];
+        const uint32_t starts = heads | 1u;               // lane 0 starts a run piece
+        // pieces: a piece ends where the next position holds another key or
+        // the chunk's valid prefix ends.  A piece that began with a head (its
+        // run starts in this chunk) and whose run does not continue past the
+        // chunk is a whole run: its row is updated here.
+        const bool piece_end = valid && (next != key || lane == nvalid - 1);
+        const int s_me = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));
+        const bool starts_here = (heads >> s_me) & 1u;
+        const bool run_ends = lane < kWarp - 1 || after != key;
+        const uint32_t ends = __ballot_sync(0xffffffffu, piece_end);
+        const uint32_t whole = __ballot_sync(0xffffffffu, piece_end && starts_here && run_ends);
+        const uint32_t complete = __ballot_sync(0xffffffffu, piece_end && starts_here && run_ends &&
+                                                             (int64_t)key < total_rows);
+        float4 acc[MC];
 #pragma unroll
-            for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int q = s; q < e; q += 4) {
-                float4 v[4][MC];
+        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < nvalid; q0 += U) {
+            float4 v[U][MC], w[U][MC];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t row = __shfl_sync(0xffffffffu, val, (q + u) & 31);
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u;
+                const uint32_t row = __shfl_sync(0xffffffffu, val, q & 31);
+                const uint32_t qk = __shfl_sync(0xffffffffu, key, q & 31);
+                const bool done = q < nvalid && ((complete >> (q & 31)) & 1u);
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    const int col = lane + m * kWarp;
+                    v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    // row < nbags holds for pairs made from well-formed offsets
+                    if (q < nvalid && col < c4 && (int64_t)row < nbags)
+                        v[u][m] = load_grad4<GT>(grad + (int64_t)row * D + 4 * col);
+                    if (done && col < c4) w[u][m] = *reinterpret_cast<const float4*>(tables + (int64_t)qk * D + 4 * col);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u;
+                if (q >= nvalid) break;
+#pragma unroll
+                for (int m = 0; m < MC; ++m) {
+                    acc[m].x += v[u][m].x;
+                    acc[m].y += v[u][m].y;
+                    acc[m].z += v[u][m].z;
+                    acc[m].w += v[u][m].w;
+                }
+                if (!((ends >> q) & 1u)) continue;
+                const uint32_t qk = __shfl_sync(0xffffffffu, key, q);
+                if ((complete >> q) & 1u) {
 #pragma unroll
                     for (int m = 0; m < MC; ++m) {
                         const int col = lane + m * kWarp;
-                        v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        // row < nbags holds for pairs made from well-formed offsets
-                        if (q + u < e && col < c4 && (int64_t)row < nbags)
-                            v[u][m] = load_grad4<GT>(grad + (int64_t)row * D + 4 * col);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (q + u < e)
-#pragma unroll
-                        for (int m = 0; m < MC; ++m) {
-                            acc[m].x += v[u][m].x;
-                            acc[m].y += v[u][m].y;
-                            acc[m].z += v[u][m].z;
-                            acc[m].w += v[u][m].w;
+                        if (col < c4) {
+                            float4 x = w[u][m];
+                            x.x = fmaf(-lr, acc[m].x, x.x);
+                            x.y = fmaf(-lr, acc[m].y, x.y);
+                            x.z = fmaf(-lr, acc[m].z, x.z);
+                            x.w = fmaf(-lr, acc[m].w, x.w);
+                            *reinterpret_cast<float4*>(tables + (int64_t)qk * D + 4 * col) = x;
                         }
-            }
-            const bool starts_here = (heads >> s) & 1u;
-            const bool ends_here = e < 32 || after != skey;
-            if (starts_here && ends_here) {
-                if ((int64_t)skey >= total_rows) continue;   // cannot happen for keys made above
-#pragma unroll
-                for (int m = 0; m < MC; ++m) {
-                    const int col = lane + m * kWarp;
-                    if (col < c4) {
-                        float4* w = reinterpret_cast<float4*>(tables + (int64_t)skey * D + 4 * col);
-                        float4 x = *w;
-                        x.x = fmaf(-lr, acc[m].x, x.x);
-                        x.y = fmaf(-lr, acc[m].y, x.y);
-                        x.z = fmaf(-lr, acc[m].z, x.z);
-                        x.w = fmaf(-lr, acc[m].w, x.w);
-                        *w = x;
                     }
-                }
-            } else {
-                const int64_t slot = 2 * c + (starts_here ? 1 : 0);
+                } else if (!((whole >> q) & 1u)) {
+                    // a piece of a run that crosses a chunk edge: its partial sum
+                    // (a whole run whose key is out of range cannot be made above)
+                    const bool piece_starts_here = __shfl_sync(0xffffffffu, starts_here, q);
+                    const int64_t slot = 2 * c + (piece_starts_here ? 1 : 0);
 #pragma unroll
-                for (int m = 0; m < MC; ++m) {
-                    const int col = lane + m * kWarp;
-                    if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
+                    for (int m = 0; m < MC; ++m) {
+                        const int col = lane + m * kWarp;
+                        if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
+                    }
+                    if (piece_starts_here && lane == 0) split_list[atomicAdd(split_count, 1u)] = (uint32_t)c;
                 }
-                if (starts_here && lane == 0) split_list[atomicAdd(split_count, 1u)] = (uint32_t)c;
+#pragma unroll
+                for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     }
@@ -557,8 +577,13 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
 {
     const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
     int64_t blocks = (nchunks * kWarp + 255) / 256;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segment_kernel<MC, GT>, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
     const int64_t cap = (int64_t)num_sms() * 8;
-    if (blocks > cap) blocks = cap;
+    const int64_t resident = (int64_t)num_sms() * per_sm;   // one wave of the grid-stride loop
+    if (blocks > resident) blocks = resident;
     segment_kernel<MC, GT><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
                                                     w.partials, w.split_list, w.split_count, nchunks, nbags);
     dlrm_status s = check_launch("segment_kernel");
