@@ -36,6 +36,36 @@ inline dlrm_status check_launch(const char* what)
     return DLRM_OK;
 }
 
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel on the stream drains.  Every kernel launched this
+// way calls pdl_wait() before touching global memory, so it still sees all of
+// the previous kernel's writes and makes none the previous kernel could see.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+inline dlrm_status check_launch_pdl(cudaError_t e, const char* what)
+{
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DLRM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    }
+    return check_launch(what);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int dtype_size(dlrm_dtype dt) { return dt == DLRM_F16 ? 2 : 4; }
 inline bool dtype_ok(dlrm_dtype dt) { return dt == DLRM_F32 || dt == DLRM_F16; }
@@ -45,6 +75,15 @@ int num_sms();   // SM count of the current device (cached per device)
 
 // -------------------------------------------------------------- device side
 constexpr int kWarp = 32;
+
+// Programmatic dependent launch: wait for the previous grid on the stream to
+// complete (its writes visible), then let the next grid be scheduled.  Both
+// are no-ops for a grid launched without the attribute.
+__device__ __forceinline__ void pdl_wait_and_release()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit)
 {

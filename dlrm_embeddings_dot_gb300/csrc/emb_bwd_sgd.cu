@@ -83,8 +83,10 @@ template <int G>
 __global__ void __launch_bounds__(256)
 keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* __restrict__ indices,
             const int32_t* __restrict__ offsets, bool hash, uint32_t* status, uint32_t* __restrict__ keys,
-            uint32_t* __restrict__ vals, int64_t nbags, int64_t nnz)
+            uint32_t* __restrict__ vals, int64_t nbags, int64_t nnz, uint32_t* __restrict__ split_count)
 {
+    pdl_wait_and_release();
+    if (blockIdx.x == 0 && threadIdx.x < 2) split_count[threadIdx.x] = 0;   // counters of the segment pass
     const int lane = threadIdx.x % G;
     const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
     const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kSortThreads)
 radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t mask, uint32_t* __restrict__ hist,
               int64_t ntiles)
 {
+    pdl_wait_and_release();
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
     __syncthreads();
@@ -180,6 +183,7 @@ radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t 
 __global__ void __launch_bounds__(kSortThreads)
 radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ totals)
 {
+    pdl_wait_and_release();
     __shared__ uint32_t warp_sums[kSortThreads / kWarp];
     __shared__ uint32_t chunk_total;
     uint32_t* row = hist + (int64_t)blockIdx.x * ntiles;
@@ -211,6 +215,7 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
                 uint32_t mask, const uint32_t* __restrict__ hist, const uint32_t* __restrict__ totals,
                 int64_t ntiles)
 {
+    pdl_wait_and_release();
     constexpr int kW = kSortThreads / kWarp;
     __shared__ uint32_t wcnt[kW][256];
     __shared__ uint32_t dbase[256];
@@ -290,6 +295,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
                int64_t nchunks, int64_t nbags)
 {
+    pdl_wait_and_release();
     // positions per batch: their gradient rows, and the table rows of the runs
     // that end (complete) among them, are all loaded before any is used
     constexpr int U = MC >= 8 ? 1 : 8 / MC;
@@ -438,6 +444,7 @@ fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restri
              uint32_t* __restrict__ long_list, uint32_t* __restrict__ long_count, int D,
              float* __restrict__ tables, int64_t total_rows, float lr)
 {
+    pdl_wait_and_release();
     const int lane = threadIdx.x % kWarp;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
@@ -492,6 +499,7 @@ fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __r
                   const uint32_t* __restrict__ long_count, int D, float* __restrict__ tables, int64_t total_rows,
                   float lr)
 {
+    pdl_wait_and_release();
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
     __shared__ int64_t s_cend;
@@ -584,15 +592,19 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
     const int64_t cap = (int64_t)num_sms() * 8;
     const int64_t resident = (int64_t)num_sms() * per_sm;   // one wave of the grid-stride loop
     if (blocks > resident) blocks = resident;
-    segment_kernel<MC, GT><<<(int)blocks, 256, 0, st>>>(w.keys[0], w.vals[0], nnz, grad, D, tables, total_rows, lr,
-                                                    w.partials, w.split_list, w.split_count, nchunks, nbags);
-    dlrm_status s = check_launch("segment_kernel");
+    dlrm_status s = check_launch_pdl(launch_pdl(segment_kernel<MC, GT>, (int)blocks, 256, 0, st,
+                                                (const uint32_t*)w.keys[0], (const uint32_t*)w.vals[0], nnz, grad, D,
+                                                tables, total_rows, lr, w.partials, w.split_list, w.split_count,
+                                                nchunks, nbags),
+                                     "segment_kernel");
     if (s != DLRM_OK) return s;
     int64_t fblocks = (nchunks * kWarp + 255) / 256;
     if (fblocks > cap) fblocks = cap;
-    fixup_kernel<MC><<<(int)fblocks, 256, 0, st>>>(w.keys[0], nnz, w.partials, w.split_list, w.split_count,
-                                                   w.long_list, w.split_count + 1, D, tables, total_rows, lr);
-    s = check_launch("fixup_kernel");
+    s = check_launch_pdl(launch_pdl(fixup_kernel<MC>, (int)fblocks, 256, 0, st, (const uint32_t*)w.keys[0], nnz,
+                                    (const float*)w.partials, (const uint32_t*)w.split_list,
+                                    (const uint32_t*)w.split_count, w.long_list, w.split_count + 1, D, tables,
+                                    total_rows, lr),
+                         "fixup_kernel");
     if (s != DLRM_OK) return s;
     const int64_t lblocks = nchunks < (int64_t)num_sms() * 2 ? nchunks : (int64_t)num_sms() * 2;
     const size_t smem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
@@ -601,10 +613,11 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
                                              (int)smem);
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
     }
-    fixup_long_kernel<MC><<<(int)lblocks, kFixThreads, smem, st>>>(w.keys[0], nnz, w.partials, w.split_list,
-                                                                   w.long_list, w.split_count + 1, D, tables,
-                                                                   total_rows, lr);
-    return check_launch("fixup_long_kernel");
+    return check_launch_pdl(launch_pdl(fixup_long_kernel<MC>, (int)lblocks, kFixThreads, smem, st,
+                                       (const uint32_t*)w.keys[0], nnz, (const float*)w.partials,
+                                       (const uint32_t*)w.split_list, (const uint32_t*)w.long_list,
+                                       (const uint32_t*)(w.split_count + 1), D, tables, total_rows, lr),
+                            "fixup_long_kernel");
 }
 
 }  // namespace
@@ -654,8 +667,6 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     const int nbits = key_bits(total_rows);
     const int npasses = (nbits + 7) / 8;
     int cur = npasses & 1;   // the last pass lands in buffer 0
-    cudaError_t ce = cudaMemsetAsync(w.split_count, 0, 2 * sizeof(uint32_t), st);
-    if (ce != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(ce));
 
     const int64_t nbags = (int64_t)F * B;
     const bool multi = nnz > 2 * nbags;
@@ -665,13 +676,12 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         int64_t blocks = (nbags * G + 255) / 256;
         const int64_t cap = (int64_t)num_sms() * 8;
         if (blocks > cap) blocks = cap;
-        if (multi)
-            keys_kernel<32><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
-                                                         w.keys[cur], w.vals[cur], nbags, nnz);
-        else
-            keys_kernel<1><<<(int)blocks, 256, 0, st>>>(d_row_base, F, B, d_indices, d_offsets, hash, d_status,
-                                                        w.keys[cur], w.vals[cur], nbags, nnz);
-        dlrm_status s = check_launch("keys_kernel");
+        const cudaError_t e =
+            multi ? launch_pdl(keys_kernel<32>, (int)blocks, 256, 0, st, d_row_base, F, B, d_indices, d_offsets, hash,
+                               d_status, w.keys[cur], w.vals[cur], nbags, nnz, w.split_count)
+                  : launch_pdl(keys_kernel<1>, (int)blocks, 256, 0, st, d_row_base, F, B, d_indices, d_offsets, hash,
+                               d_status, w.keys[cur], w.vals[cur], nbags, nnz, w.split_count);
+        dlrm_status s = check_launch_pdl(e, "keys_kernel");
         if (s != DLRM_OK) return s;
     }
     const int64_t ntiles = (nnz + kTile - 1) / kTile;
@@ -679,12 +689,14 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         const int shift = 8 * pass;
         const int bits = nbits - shift < 8 ? nbits - shift : 8;
         const uint32_t mask = (1u << bits) - 1u;
-        radix_upsweep<<<(int)ntiles, kSortThreads, 0, st>>>(w.keys[cur], nnz, shift, mask, w.hist, ntiles);
-        radix_scan<<<256, kSortThreads, 0, st>>>(w.hist, ntiles, w.totals);
-        radix_downsweep<<<(int)ntiles, kSortThreads, 0, st>>>(w.keys[cur], w.vals[cur], w.keys[cur ^ 1],
-                                                              w.vals[cur ^ 1], nnz, shift, mask, w.hist, w.totals,
-                                                              ntiles);
-        dlrm_status s = check_launch("radix sort pass");
+        cudaError_t e = launch_pdl(radix_upsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur], nnz,
+                                   shift, mask, w.hist, ntiles);
+        if (e == cudaSuccess) e = launch_pdl(radix_scan, 256, kSortThreads, 0, st, w.hist, ntiles, w.totals);
+        if (e == cudaSuccess)
+            e = launch_pdl(radix_downsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur],
+                           (const uint32_t*)w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], nnz, shift, mask,
+                           (const uint32_t*)w.hist, (const uint32_t*)w.totals, ntiles);
+        dlrm_status s = check_launch_pdl(e, "radix sort pass");
         if (s != DLRM_OK) return s;
         cur ^= 1;
     }

@@ -202,6 +202,7 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
                          const float* __restrict__ pooled, int B, int P, float* __restrict__ grad_dense,
                          float* __restrict__ grad_pooled, uint32_t* __restrict__ status)
 {
+    pdl_wait_and_release();
     using L = RegBwd<R>;
     constexpr int F = R - 1, D = kRegD, RS = L::RS, NP = L::NP;
     extern __shared__ __align__(16) unsigned char bwd_regs_raw[];
@@ -313,8 +314,9 @@ dlrm_status launch_regs(const float* grad_out, const float* dense, const float* 
     int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    kern<<<(int)blocks, kWarps * kWarp, smem, stream>>>(grad_out, dense, pooled, B, P, gd, gp, status);
-    return check_launch("interact_bwd_regs_kernel");
+    return check_launch_pdl(launch_pdl(kern, (int)blocks, kWarps * kWarp, smem, stream, grad_out, dense, pooled, B, P,
+                                       gd, gp, status),
+                            "interact_bwd_regs_kernel");
 }
 
 // Shapes the register kernel takes: fp32, D = 128, F in {8, 26}, gradient

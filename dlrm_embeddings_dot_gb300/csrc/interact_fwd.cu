@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(kRegWarps * kWarp, 3)
 interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restrict__ pooled, int B,
                          float* __restrict__ out, int P, uint32_t* __restrict__ status)
 {
+    pdl_wait_and_release();
     constexpr int D = kRegD;
     extern __shared__ __align__(16) float4 zbuf[];
     const int lane = threadIdx.x % kWarp;
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(kRegWarps * kWarp, 3)
 emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, float* __restrict__ pooled,
                          float* __restrict__ out, int P, uint32_t* __restrict__ status)
 {
+    pdl_wait_and_release();
     constexpr int kAfter = kPooled ? (R * (R - 1) / 2 + 31) / 32 / 2 : 0;
     constexpr int F = R - 1;
     constexpr int D = kRegD;
@@ -571,8 +573,8 @@ dlrm_status launch_regs(const float* dense, const float* pooled, int B, float* o
     const int64_t need = ((int64_t)B + kRegWarps - 1) / kRegWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     const int blocks = (int)(need < cap ? need : cap);
-    kern<<<blocks, kRegWarps * kWarp, smem, stream>>>(dense, pooled, B, out, P, status);
-    return check_launch("interact_fwd_regs_kernel");
+    return check_launch_pdl(launch_pdl(kern, blocks, kRegWarps * kWarp, smem, stream, dense, pooled, B, out, P, status),
+                            "interact_fwd_regs_kernel");
 }
 
 template <int R, bool kPooled>
@@ -589,8 +591,9 @@ dlrm_status launch_emb_regs(const RegGather& ga, const float* dense, int B, floa
     const int64_t need = ((int64_t)B + kRegWarps - 1) / kRegWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     const int blocks = (int)(need < cap ? need : cap);
-    kern<<<blocks, kRegWarps * kWarp, smem, stream>>>(ga, dense, B, pooled, out, P, status);
-    return check_launch("emb_interact_regs_kernel");
+    return check_launch_pdl(launch_pdl(kern, blocks, kRegWarps * kWarp, smem, stream, ga, dense, B, pooled, out, P,
+                                       status),
+                            "emb_interact_regs_kernel");
 }
 
 // Shapes the register kernel takes: fp32, D = 128, F in {8, 26}, rows of the
