@@ -77,11 +77,16 @@ int num_sms();   // SM count of the current device (cached per device)
 constexpr int kWarp = 32;
 
 // Programmatic dependent launch: wait for the previous grid on the stream to
-// complete (its writes visible), then let the next grid be scheduled.  Both
-// are no-ops for a grid launched without the attribute.
+// complete (its writes visible).  A no-op for a grid launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ... and let the next grid be scheduled at once (its blocks wait in
+// pdl_wait until this grid completes).  Kernels that need the SM's L1 for
+// themselves leave this out: the next grid is then scheduled as they exit.
 __device__ __forceinline__ void pdl_wait_and_release()
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 

@@ -95,6 +95,7 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     const T* __restrict__ pooled, int F, int D, int B, int P,
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
+    pdl_wait_and_release();
     constexpr int RS = (RMAX + 3) / 4 * 4;       // smem row stride of M (multiple of 4)
     extern __shared__ __align__(16) unsigned char bwd_smem_raw[];
     const int lane = threadIdx.x % kWarp;
@@ -344,9 +345,9 @@ dlrm_status launch(const float* grad_out, const void* dense, const void* pooled,
     int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    kern<<<(int)blocks, kWarps * kWarp, smem, stream>>>(grad_out, (const T*)dense, (const T*)pooled, F, D, B, P,
-                                                        gd, gp);
-    return check_launch("interact_bwd_kernel");
+    return check_launch_pdl(launch_pdl(kern, (int)blocks, kWarps * kWarp, smem, stream, grad_out, (const T*)dense,
+                                       (const T*)pooled, F, D, B, P, gd, gp),
+                            "interact_bwd_kernel");
 }
 
 template <typename T>

@@ -70,6 +70,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
                        __half* __restrict__ grad_dense, int F, int D, int B, int P, int KH, int NS,
                        uint32_t tmem_cols, uint32_t* status)
 {
+    pdl_wait_and_release();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int z_bytes = KH * kZBlockBytes;
@@ -393,7 +394,8 @@ extern "C" dlrm_status dlrm_interact_bwd_f16(const void* d_grad_out, const void*
     cudaError_t e = cudaFuncSetAttribute(interact_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_bwd_f16: %s", cudaGetErrorString(e));
-    interact_bwd_tc_kernel<<<grid, kThreads, smem, as_stream(stream)>>>(
-        mp, md, mg, (const __half*)d_grad_out, (__half*)d_grad_dense, F, D, B, out_cols, KH, ns, tmem_cols, d_status);
-    return check_launch("interact_bwd_tc_kernel");
+    return check_launch_pdl(launch_pdl(interact_bwd_tc_kernel, grid, kThreads, smem, as_stream(stream), mp, md, mg,
+                                       (const __half*)d_grad_out, (__half*)d_grad_dense, F, D, B, out_cols, KH, ns,
+                                       tmem_cols, d_status),
+                            "interact_bwd_tc_kernel");
 }

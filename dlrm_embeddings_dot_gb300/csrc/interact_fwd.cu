@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 8)
 interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D_rt,
                          int B, T* __restrict__ out, int P)
 {
+    pdl_wait_and_release();
     extern __shared__ __align__(16) float smem[];
     const int D = DT ? DT : D_rt;
     const FfmaGeom geo = ffma_geom(F, D, P);
@@ -622,8 +623,9 @@ dlrm_status launch_ffma_t(const void* dense, const void* pooled, int F, int D, i
     int64_t blocks = B;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    kern<<<(int)blocks, kFfmaThreads, smem, stream>>>((const T*)dense, (const T*)pooled, F, D, B, (T*)out, P);
-    return check_launch("interact_fwd_ffma_kernel");
+    return check_launch_pdl(launch_pdl(kern, (int)blocks, kFfmaThreads, smem, stream, (const T*)dense, (const T*)pooled,
+                                       F, D, B, (T*)out, P),
+                            "interact_fwd_ffma_kernel");
 }
 
 template <typename T>

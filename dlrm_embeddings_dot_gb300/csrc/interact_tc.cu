@@ -103,6 +103,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
                    uint32_t* status, GatherArgs ga)
 {
+    pdl_wait_and_release();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const Layout L = make_layout(KH, P, NS);
@@ -491,9 +492,9 @@ dlrm_status launch_kernel(int grid, int threads, const Layout& L, const CUtensor
     cudaError_t e = cudaFuncSetAttribute(interact_tc_kernel<kFused, kCpr>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-    interact_tc_kernel<kFused, kCpr><<<grid, threads, L.smem, stream>>>(mp, md, (const __half*)dense, (__half*)out, F,
-                                                                        D, B, P, KH, ns, status, ga);
-    return check_launch("interact_tc_kernel");
+    return check_launch_pdl(launch_pdl(interact_tc_kernel<kFused, kCpr>, grid, threads, L.smem, stream, mp, md,
+                                       (const __half*)dense, (__half*)out, F, D, B, P, KH, ns, status, ga),
+                            "interact_tc_kernel");
 }
 
 // Tensor maps + launch of the tcgen05 kernel.  pooled == nullptr selects the

@@ -54,6 +54,7 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                  const __grid_constant__ CUtensorMap map_out, const float* __restrict__ bias, int M, int N, int K,
                  int BN, int NS, uint32_t tmem_cols, uint32_t* status)
 {
+    pdl_wait_and_release();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int a_bytes = kBM * 128, stage_bytes = a_bytes + BN * 128;
@@ -232,6 +233,7 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 // x (fp32 [M][K]) -> fp16 [M][Kp], pad columns zero.
 __global__ void cast_pad_kernel(const float* __restrict__ x, int64_t M, int K, int Kp, __half* __restrict__ x16)
 {
+    pdl_wait_and_release();
     const int64_t n = M * Kp;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / Kp;
@@ -286,8 +288,9 @@ dlrm_status launch_layer(const __half* a, int lda, const __half* w, const float*
     const int grid = tiles < num_sms() ? tiles : num_sms();
     cudaError_t e = cudaFuncSetAttribute(mlp_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_bottom_mlp_fwd: %s", cudaGetErrorString(e));
-    mlp_layer_kernel<<<grid, kThreads, smem, st>>>(ma, mw, mo, bias, M, N, lda, BN, ns, tmem_cols, status);
-    return check_launch("mlp_layer_kernel");
+    return check_launch_pdl(launch_pdl(mlp_layer_kernel, grid, kThreads, smem, st, ma, mw, mo, bias, M, N, lda, BN, ns,
+                                       tmem_cols, status),
+                            "mlp_layer_kernel");
 }
 
 // Workspace: x as fp16 [B][round_up8(dims[0])], then each hidden layer's
@@ -342,7 +345,8 @@ extern "C" dlrm_status dlrm_bottom_mlp_fwd(const float* d_x, int B, int n_layers
         const int64_t n = (int64_t)B * Kp0;
         int64_t blocks = (n + 255) / 256;
         if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
-        cast_pad_kernel<<<(int)blocks, 256, 0, st>>>(d_x, B, dims[0], Kp0, x16);
+        const cudaError_t e = launch_pdl(cast_pad_kernel, (int)blocks, 256, 0, st, d_x, (int64_t)B, dims[0], Kp0, x16);
+        if (e != cudaSuccess) return check_launch_pdl(e, "cast_pad_kernel");
         dlrm_status s = check_launch("cast_pad_kernel");
         if (s != DLRM_OK) return s;
     }
