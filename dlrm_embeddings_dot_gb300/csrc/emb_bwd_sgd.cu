@@ -16,15 +16,17 @@
 //     keys inside its chunk.  A run wholly inside the chunk updates its row
 //     at once (w = fmaf(-lr, g, w)); a run crossing a chunk edge leaves one
 //     partial sum per chunk it touches.
-//  4. fixup: one warp per run that crossed a chunk edge finds the run's last
-//     chunk (32 chunks per probe), adds its partial sums in chunk order and
-//     updates the row; runs of more than 64 pieces are handed to one block
+//     The chunk where such a run starts finds the run's last chunk (an
+//     exponential probe of chunk heads, then 32-ary refinement) and files
+//     the run with its number of pieces.
+//  4. fixup (one kernel): runs of more than 64 pieces are summed by one block
 //     each (16 warps add 16 contiguous slices of pieces, then the 16 sums in
-//     slice order).  A lane keeps up to 4 partial-sum loads in flight.
+//     slice order), the others by one warp each, pieces in chunk order; a
+//     lane keeps up to 4 partial-sum loads in flight.
 // Every order of summation is fixed by the data, so results are bitwise
 // reproducible.  Workspace layout (256-byte aligned pieces):
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
-//   partials[2 * nchunks][D] | split_list[nchunks] | long_list[nchunks] |
+//   partials[2 * nchunks][D] | split_list[nchunks] | long_list[nchunks] (64-bit) |
 //   counters
 // The sort ends in keysA/valsA, which the caller may read after the call.
 #include <mutex>
@@ -46,9 +48,9 @@ struct Ws {
     uint32_t* hist;
     uint32_t* totals;
     float* partials;
-    uint32_t* split_list;
-    uint32_t* split_count;   // [0] split runs, [1] long split runs
-    uint32_t* long_list;
+    uint64_t* split_list;    // runs crossing a chunk edge: first chunk << 32 | pieces, up to kLongPieces pieces
+    uint32_t* split_count;   // [0] entries of split_list, [1] entries of long_list
+    uint64_t* long_list;     // the same for runs of more pieces
     size_t bytes;
 };
 
@@ -71,8 +73,8 @@ Ws carve(void* base, int64_t nnz, int D)
     w.hist = (uint32_t*)take(4 * 256 * (size_t)ntiles);
     w.totals = (uint32_t*)take(4 * 256);
     w.partials = (float*)take(4 * 2 * (size_t)nchunks * D);
-    w.split_list = (uint32_t*)take(4 * (size_t)nchunks);
-    w.long_list = (uint32_t*)take(4 * (size_t)nchunks);
+    w.split_list = (uint64_t*)take(8 * (size_t)nchunks);
+    w.long_list = (uint64_t*)take(8 * (size_t)nchunks);
     w.split_count = (uint32_t*)take(8);
     w.bytes = off;
     return w;
@@ -271,6 +273,37 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
     }
 }
 
+// ----------------------------------------------------------------- 4. fixup
+constexpr int kLongPieces = 64;   // runs with more chunk pieces are summed by a whole block
+constexpr int kFixRegs = 4;       // float4 partial-sum loads a lane has in flight
+
+// Last chunk touched by the run of key K that starts in chunk c0 and continues
+// past it.  Keys are sorted, so the run touches chunk c iff the first key of c
+// is K, and the chunks it touches are c0..L.  Chunk c0 + 2 is probed first
+// (one broadcast load); past it, one round probes c0 + 2^j for j = 0..31 (so
+// 2^j <= L - c0 < 2^(j+1) for the last true j), then each round probes 32
+// evenly spaced chunks of the remaining interval.
+__device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ keys, int64_t n, int64_t nchunks,
+                                                  int64_t c0, uint32_t K, int lane)
+{
+    auto touches = [&](int64_t c) { return c < nchunks && c * kChunk < n && keys[c * kChunk] == K; };
+    if (!touches(c0 + 2)) return c0 + 1;      // most runs that cross an edge end in the next chunk
+    const uint32_t m = __ballot_sync(0xffffffffu, touches(c0 + ((int64_t)1 << lane)));
+    const int j = __popc(m) - 1;              // chunk c0 + 1 is touched, so j >= 0
+    int64_t lo = c0 + ((int64_t)1 << j);      // touched
+    int64_t hi = c0 + ((int64_t)2 << j);      // not touched (or past the end)
+    while (hi - lo > 1) {
+        const int64_t step = (hi - lo + kWarp - 1) / kWarp;
+        const int64_t c = lo + step * (lane + 1);
+        const uint32_t t = __ballot_sync(0xffffffffu, c < hi && touches(c));
+        const int k = __popc(t);              // probes lo + step, ..., lo + k*step are touched
+        const int64_t nlo = lo + step * k;
+        hi = nlo + step < hi ? nlo + step : hi;
+        lo = nlo;
+    }
+    return lo;
+}
+
 // --------------------------------------------------------- 3. segment sums
 // Four consecutive gradient elements as fp32: one 16-byte load of fp32, or an
 // 8-byte load of fp16 widened exactly.
@@ -292,8 +325,8 @@ template <int MC, typename GT>
 __global__ void __launch_bounds__(256)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
                const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
-               float* __restrict__ partials, uint32_t* __restrict__ split_list, uint32_t* split_count,
-               int64_t nchunks, int64_t nbags)
+               float* __restrict__ partials, uint64_t* __restrict__ split_list, uint32_t* split_count,
+               uint64_t* __restrict__ long_list, int64_t nchunks, int64_t nbags)
 {
     pdl_wait_and_release();
     // positions per batch: their gradient rows, and the table rows of the runs
@@ -334,6 +367,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint32_t file_key = kSkipKey;   // key of a run that starts here and crosses the chunk's end
         for (int q0 = 0; q0 < nvalid; q0 += U) {
             float4 v[U][MC], w[U][MC];
 #pragma unroll
@@ -389,30 +423,22 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                         const int col = lane + m * kWarp;
                         if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
                     }
-                    if (piece_starts_here && lane == 0) split_list[atomicAdd(split_count, 1u)] = (uint32_t)c;
+                    if (piece_starts_here) file_key = qk;   // filed after the chunk (at most one per chunk)
                 }
 #pragma unroll
                 for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-    }
-}
-
-// ----------------------------------------------------------------- 4. fixup
-constexpr int kLongPieces = 64;   // runs with more chunk pieces go to a block-per-run pass
-constexpr int kFixRegs = 4;       // float4 partial-sum loads a lane has in flight
-
-// Last chunk a run that starts in chunk c0 (and continues past it) touches:
-// chunks c0+1, c0+2, ... are probed 32 at a time (keys are sorted, so the run
-// touches chunk c iff the first key of c is K).
-__device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ keys, int64_t n, int64_t c0,
-                                                  uint32_t K, int lane)
-{
-    for (int64_t base = c0 + 1;; base += kWarp) {
-        const int64_t c = base + lane;
-        const bool touches = c * kChunk < n && keys[c * kChunk] == K;
-        const uint32_t m = __ballot_sync(0xffffffffu, touches);
-        if (m != 0xffffffffu) return base + (__ffs(~m) - 1) - 1;
+        if (file_key != kSkipKey) {   // this chunk files the run it starts, with its number of pieces
+            const int64_t pieces = run_last_chunk(keys, n, nchunks, c, file_key, lane) - c + 1;
+            if (lane == 0) {
+                const uint64_t e = (uint64_t)c << 32 | (uint64_t)pieces;
+                if (pieces > kLongPieces)
+                    long_list[atomicAdd(split_count + 1, 1u)] = e;
+                else
+                    split_list[atomicAdd(split_count, 1u)] = e;
+            }
+        }
     }
 }
 
@@ -435,114 +461,66 @@ __device__ __forceinline__ void apply_sgd(float* __restrict__ tables, int64_t ro
     }
 }
 
-// One warp per split run: pieces (partial sums) added in chunk order.  Runs
-// of more than kLongPieces pieces are appended to a list for fixup_long_kernel.
+// Slot of piece j of the run that starts in chunk c0 (the first piece is the
+// starting chunk's "continues" slot, the others are chunk-start slots).
+__device__ __forceinline__ int64_t piece_slot(int64_t c0, int64_t j) { return j == 0 ? 2 * c0 + 1 : 2 * (c0 + j); }
+
+// Pieces [j0, j1) of the run starting in chunk c0, added in order into acc.
 template <int MC>
-__global__ void __launch_bounds__(256)
-fixup_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
-             const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ split_count,
-             uint32_t* __restrict__ long_list, uint32_t* __restrict__ long_count, int D,
-             float* __restrict__ tables, int64_t total_rows, float lr)
+__device__ __forceinline__ void add_pieces(const float* __restrict__ partials, int64_t c0, int64_t j0, int64_t j1,
+                                           int D, int lane, float4 (&acc)[MC])
 {
-    pdl_wait_and_release();
-    const int lane = threadIdx.x % kWarp;
-    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
-    const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
     const int c4 = D / 4;
-    const uint32_t count = *split_count;
-    for (int64_t i = warp_id; i < count; i += nwarps) {
-        const int64_t c0 = split_list[i];
-        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
-        const int64_t pieces = run_last_chunk(keys, n, c0, K, lane) - c0 + 1;
-        if (pieces > kLongPieces) {
-            if (lane == 0) long_list[atomicAdd(long_count, 1u)] = (uint32_t)i;
-            continue;
+    constexpr int kFixBatch = kFixRegs / MC > 0 ? kFixRegs / MC : 1;   // pieces in flight
+    for (int64_t j = j0; j < j1; j += kFixBatch) {
+        float4 v[kFixBatch][MC];
+#pragma unroll
+        for (int u = 0; u < kFixBatch; ++u) {
+            const int64_t slot = piece_slot(c0, j + u);
+#pragma unroll
+            for (int m = 0; m < MC; ++m) {
+                const int col = lane + m * kWarp;
+                v[u][m] = (j + u < j1 && col < c4) ? reinterpret_cast<const float4*>(partials + slot * D)[col]
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        float4 acc[MC];
 #pragma unroll
-        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int kFixBatch = kFixRegs / MC > 0 ? kFixRegs / MC : 1;   // pieces in flight
-        for (int64_t j = 0; j < pieces; j += kFixBatch) {
-            float4 v[kFixBatch][MC];
-#pragma unroll
-            for (int u = 0; u < kFixBatch; ++u) {
-                const int64_t slot = (j + u) == 0 ? 2 * c0 + 1 : 2 * (c0 + j + u);
+        for (int u = 0; u < kFixBatch; ++u)
+            if (j + u < j1)
 #pragma unroll
                 for (int m = 0; m < MC; ++m) {
-                    const int col = lane + m * kWarp;
-                    v[u][m] = (j + u < pieces && col < c4) ? reinterpret_cast<const float4*>(partials + slot * D)[col]
-                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    acc[m].x += v[u][m].x;
+                    acc[m].y += v[u][m].y;
+                    acc[m].z += v[u][m].z;
+                    acc[m].w += v[u][m].w;
                 }
-            }
-#pragma unroll
-            for (int u = 0; u < kFixBatch; ++u)
-                if (j + u < pieces)
-#pragma unroll
-                    for (int m = 0; m < MC; ++m) {
-                        acc[m].x += v[u][m].x;
-                        acc[m].y += v[u][m].y;
-                        acc[m].z += v[u][m].z;
-                        acc[m].w += v[u][m].w;
-                    }
-        }
-        if ((int64_t)K < total_rows) apply_sgd<MC>(tables, K, D, lr, lane, acc);
     }
 }
 
-// One block per long split run: warp w adds the w-th of kW contiguous slices
-// of the run's pieces in order (kFixBatch loads in flight), then warp 0 adds
-// the kW slice sums in slice order and applies the update.
+// Runs that cross chunk edges.  Block i < (long runs) takes long run i: warp w
+// adds the w-th of kW contiguous slices of its pieces, then warp 0 adds the
+// kW slice sums in slice order and updates the row.  Then every warp takes
+// short runs (pieces in order, one warp per run).
 template <int MC>
 __global__ void __launch_bounds__(kFixThreads)
-fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __restrict__ partials,
-                  const uint32_t* __restrict__ split_list, const uint32_t* __restrict__ long_list,
-                  const uint32_t* __restrict__ long_count, int D, float* __restrict__ tables, int64_t total_rows,
-                  float lr)
+fixup_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ partials,
+             const uint64_t* __restrict__ split_list, const uint64_t* __restrict__ long_list,
+             const uint32_t* __restrict__ counts, int D, float* __restrict__ tables, int64_t total_rows, float lr)
 {
     pdl_wait_and_release();
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
-    __shared__ int64_t s_cend;
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const int c4 = D / 4;
-    const uint32_t count = *long_count;
-    for (uint32_t i = blockIdx.x; i < count; i += gridDim.x) {
-        const int64_t c0 = split_list[long_list[i]];
+    const uint32_t nshort = counts[0], nlong = counts[1];
+    for (uint32_t i = blockIdx.x; i < nlong; i += gridDim.x) {
+        const uint64_t e = long_list[i];
+        const int64_t c0 = (int64_t)(e >> 32), pieces = (int64_t)(e & 0xffffffffu);
         const uint32_t K = keys[c0 * kChunk + kChunk - 1];
-        if (warp == 0) {
-            const int64_t ce = run_last_chunk(keys, n, c0, K, lane);
-            if (lane == 0) s_cend = ce;
-        }
-        __syncthreads();
-        const int64_t pieces = s_cend - c0 + 1;
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int64_t j0 = pieces * warp / kW, j1 = pieces * (warp + 1) / kW;
-        constexpr int kFixBatch = kFixRegs / MC > 0 ? kFixRegs / MC : 1;   // pieces in flight
-        for (int64_t j = j0; j < j1; j += kFixBatch) {
-            float4 v[kFixBatch][MC];
-#pragma unroll
-            for (int u = 0; u < kFixBatch; ++u) {
-                const int64_t slot = (j + u) == 0 ? 2 * c0 + 1 : 2 * (c0 + j + u);
-#pragma unroll
-                for (int m = 0; m < MC; ++m) {
-                    const int col = lane + m * kWarp;
-                    v[u][m] = (j + u < j1 && col < c4) ? reinterpret_cast<const float4*>(partials + slot * D)[col]
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kFixBatch; ++u)
-                if (j + u < j1)
-#pragma unroll
-                    for (int m = 0; m < MC; ++m) {
-                        acc[m].x += v[u][m].x;
-                        acc[m].y += v[u][m].y;
-                        acc[m].z += v[u][m].z;
-                        acc[m].w += v[u][m].w;
-                    }
-        }
+        add_pieces<MC>(partials, c0, pieces * warp / kW, pieces * (warp + 1) / kW, D, lane, acc);
 #pragma unroll
         for (int m = 0; m < MC; ++m) {
             const int col = lane + m * kWarp;
@@ -570,6 +548,17 @@ fixup_long_kernel(const uint32_t* __restrict__ keys, int64_t n, const float* __r
         }
         __syncthreads();
     }
+    const int64_t gw = (int64_t)blockIdx.x * kW + warp, nw = (int64_t)gridDim.x * kW;
+    for (int64_t i = gw; i < nshort; i += nw) {
+        const uint64_t e = split_list[i];
+        const int64_t c0 = (int64_t)(e >> 32), pieces = (int64_t)(e & 0xffffffffu);
+        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
+        float4 acc[MC];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        add_pieces<MC>(partials, c0, 0, pieces, D, lane, acc);
+        if ((int64_t)K < total_rows) apply_sgd<MC>(tables, K, D, lr, lane, acc);
+    }
 }
 
 int key_bits(int64_t total_rows)
@@ -589,35 +578,27 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segment_kernel<MC, GT>, 256, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
-    const int64_t cap = (int64_t)num_sms() * 8;
     const int64_t resident = (int64_t)num_sms() * per_sm;   // one wave of the grid-stride loop
     if (blocks > resident) blocks = resident;
     dlrm_status s = check_launch_pdl(launch_pdl(segment_kernel<MC, GT>, (int)blocks, 256, 0, st,
                                                 (const uint32_t*)w.keys[0], (const uint32_t*)w.vals[0], nnz, grad, D,
                                                 tables, total_rows, lr, w.partials, w.split_list, w.split_count,
-                                                nchunks, nbags),
+                                                w.long_list, nchunks, nbags),
                                      "segment_kernel");
     if (s != DLRM_OK) return s;
-    int64_t fblocks = (nchunks * kWarp + 255) / 256;
-    if (fblocks > cap) fblocks = cap;
-    s = check_launch_pdl(launch_pdl(fixup_kernel<MC>, (int)fblocks, 256, 0, st, (const uint32_t*)w.keys[0], nnz,
-                                    (const float*)w.partials, (const uint32_t*)w.split_list,
-                                    (const uint32_t*)w.split_count, w.long_list, w.split_count + 1, D, tables,
-                                    total_rows, lr),
-                         "fixup_kernel");
-    if (s != DLRM_OK) return s;
-    const int64_t lblocks = nchunks < (int64_t)num_sms() * 2 ? nchunks : (int64_t)num_sms() * 2;
     const size_t smem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(fixup_long_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(fixup_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
     }
-    return check_launch_pdl(launch_pdl(fixup_long_kernel<MC>, (int)lblocks, kFixThreads, smem, st,
-                                       (const uint32_t*)w.keys[0], nnz, (const float*)w.partials,
-                                       (const uint32_t*)w.split_list, (const uint32_t*)w.long_list,
-                                       (const uint32_t*)(w.split_count + 1), D, tables, total_rows, lr),
-                            "fixup_long_kernel");
+    int64_t fblocks = (int64_t)num_sms() * 4;
+    const int64_t fneed = (nchunks * kWarp + kFixThreads - 1) / kFixThreads;   // one warp per chunk at most
+    if (fblocks > fneed) fblocks = fneed;
+    return check_launch_pdl(launch_pdl(fixup_kernel<MC>, (int)fblocks, kFixThreads, smem, st, (const uint32_t*)w.keys[0],
+                                       (const float*)w.partials, (const uint64_t*)w.split_list,
+                                       (const uint64_t*)w.long_list, (const uint32_t*)w.split_count, D, tables,
+                                       total_rows, lr),
+                            "fixup_kernel");
 }
 
 }  // namespace
