@@ -57,6 +57,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.dlrm_interact_fwd.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P]
     L.dlrm_interact_fwd_cuda_core.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I, _P]
     L.dlrm_emb_interact_fwd.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, _P, _I, ctypes.c_uint, _P, _P]
+    L.dlrm_emb_interact_bwd.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, _P, _I, _P, _P, ctypes.c_uint, _P,
+                                        _P]
     L.dlrm_emb_interact_fwd_train.argtypes = [_P, _I, _P, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _I, ctypes.c_uint,
                                               _P, _P]
     L.dlrm_interact_bwd.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
@@ -83,7 +85,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for f in ("dlrm_plan_tables", "dlrm_batch_shard", "dlrm_a2a_layout"):
         getattr(L, f).restype = _I
     for f in ("dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_fwd_cuda_core", "dlrm_emb_interact_fwd",
-              "dlrm_emb_interact_fwd_train", "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
+              "dlrm_emb_interact_fwd_train", "dlrm_emb_interact_bwd", "dlrm_interact_bwd", "dlrm_emb_bwd_sgd", "dlrm_emb_bwd_sgd_noalloc", "dlrm_synth_fill_uniform"):
         getattr(L, f).restype = _I
     if path is None:
         _lib = L
@@ -163,6 +165,15 @@ def dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, indices, offsets, den
                                             _ptr(indices), _ptr(offsets), indices.numel(), _ptr(dense),
                                             _ptr(pooled), _ptr(out), out_cols, flags, _ptr(status), _stream(stream))
     _check("dlrm_emb_interact_fwd_train", rc)
+
+
+def dlrm_emb_interact_bwd(tables, row_base, F, D, B, indices, offsets, grad_out, dense, out_cols, grad_dense,
+                          grad_pooled, flags=0, status=None, stream=None):
+    """Interaction backward with the pooled rows gathered from the tables; see ``include/dlrm.h``."""
+    rc = load().dlrm_emb_interact_bwd(_ptr(tables), _dtype_code(tables), _ptr(row_base), F, D, B, _ptr(indices),
+                                      _ptr(offsets), indices.numel(), _ptr(grad_out), _ptr(dense), out_cols,
+                                      _ptr(grad_dense), _ptr(grad_pooled), flags, _ptr(status), _stream(stream))
+    _check("dlrm_emb_interact_bwd", rc)
 
 
 def dlrm_interact_bwd(grad_out, dense, pooled, F, D, B, out_cols, grad_dense, grad_pooled, stream=None):

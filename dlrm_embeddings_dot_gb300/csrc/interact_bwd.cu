@@ -14,6 +14,8 @@
 // over j (fixed order).  Outputs are 16-byte stores, 512 contiguous bytes per
 // warp.
 #include "common.cuh"
+#include "interact_tc.cuh"
+#include "reg_gather.cuh"
 #include "tcgen05.cuh"
 
 namespace dlrm {
@@ -197,10 +199,17 @@ struct RegBwd {
     }
 };
 
-template <int R>
+// kGather: Z's pooled rows are gathered from the tables (ga) instead of read
+// from a stored pooled tensor (pooled is then unused); the values are the
+// same bits the lookup produced, so are the results.
+// Gathered rows arrive by per-lane cp.async (the backward has room in the
+// shared-memory pipe; 26 bulk copies per sample measured 3 % slower).
+constexpr bool kRowsAsync = true;
+
+template <int R, bool kGather>
 __global__ void __launch_bounds__(kWarps * kWarp, 3)
 interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __restrict__ dense,
-                         const float* __restrict__ pooled, int B, int P, float* __restrict__ grad_dense,
+                         const float* __restrict__ pooled, RegGather ga, int B, int P, float* __restrict__ grad_dense,
                          float* __restrict__ grad_pooled, uint32_t* __restrict__ status)
 {
     pdl_wait_and_release();
@@ -232,17 +241,45 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
 
     const int64_t stride = (int64_t)gridDim.x * kWarps;
     int64_t b = (int64_t)blockIdx.x * kWarps + warp;
-    auto stage = [&](int64_t smp) {
-        if (lane == 0) {
+    const BagLanes<F, D> bags(ga, B, lane, status);
+    // sample smp's Z rows and gradient row, all counted on the warp's mbarrier
+    auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
+        if constexpr (kGather) {
+            bags.template gather<kRowsAsync>(zs, src_row, a, e, bar);
+            if (lane == F) {
+                tc::mbar_expect_tx_only(bar, D * 4);
+                tc::bulk_g2s(zs, dense + smp * D, D * 4, bar);
+            } else if (lane == F + 1) {
+                tc::mbar_expect_tx_only(bar, P * 4);
+                tc::bulk_g2s(gs, grad_out + smp * P, P * 4, bar);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar);
+        } else if (lane == 0) {
             tc::mbar_expect_tx(bar, R * D * 4 + P * 4);
             tc::bulk_g2s(zs, dense + smp * D, D * 4, bar);
             tc::bulk_g2s(zs + kWarp, pooled + smp * (int64_t)F * D, F * D * 4, bar);
             tc::bulk_g2s(gs, grad_out + smp * P, P * 4, bar);
         }
     };
+    // bags: bounds two samples ahead, the index one sample ahead (used a
+    // sample after it was requested)
+    int a1 = 0, e1 = 0, a2 = 0, e2 = 0, idx1 = 0;
+    if constexpr (kGather) {
+        int a0, e0;
+        bags.load_bounds(b, a0, e0);
+        bags.load_bounds(b + stride, a1, e1);
+        bags.load_bounds(b + 2 * stride, a2, e2);
+        bags.clamp(a0, e0);
+        if (b < B) stage(b, bags.resolve(a0, e0, bags.early_index(a0, e0)), a0, e0);
+        bags.clamp(a1, e1);
+        idx1 = bags.early_index(a1, e1);
+    } else {
+        if (b < B) stage(b, 0, 0, 0);
+    }
     uint32_t phase = 0;
-    if (b < B) stage(b);
     for (; b < B; b += stride) {
+        if constexpr (kGather && kRowsAsync) asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (!tc::bounded_wait(bar, phase)) {
             if (lane == 0) set_status(status, DLRM_STATUS_TIMEOUT);
             return;
@@ -268,7 +305,20 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
         __syncwarp();
         if (b + stride < B) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            stage(b + stride);
+            if constexpr (kGather)
+                stage(b + stride, bags.resolve(a1, e1, idx1), a1, e1);
+            else
+                stage(b + stride, 0, 0, 0);
+        }
+        if constexpr (kGather) {   // advance the bag pipeline by one sample
+            int a3, e3;
+            bags.load_bounds(b + 3 * stride, a3, e3);
+            bags.clamp(a2, e2);
+            idx1 = bags.early_index(a2, e2);
+            a1 = a2;
+            e1 = e2;
+            a2 = a3;
+            e2 = e3;
         }
         // a rolled loop over the rows keeps the code small (the diagonal of M
         // is zero, so j = i adds an exact zero product)
@@ -300,12 +350,12 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
     }
 }
 
-template <int R>
-dlrm_status launch_regs(const float* grad_out, const float* dense, const float* pooled, int B, int P, float* gd,
-                        float* gp, uint32_t* status, cudaStream_t stream)
+template <int R, bool kGather>
+dlrm_status launch_regs(const float* grad_out, const float* dense, const float* pooled, const RegGather& ga, int B,
+                        int P, float* gd, float* gp, uint32_t* status, cudaStream_t stream)
 {
     const size_t smem = (size_t)RegBwd<R>::block_bytes(P);
-    auto kern = interact_bwd_regs_kernel<R>;
+    auto kern = interact_bwd_regs_kernel<R, kGather>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_bwd: %s", cudaGetErrorString(e));
     int per_sm = 0;
@@ -315,8 +365,8 @@ dlrm_status launch_regs(const float* grad_out, const float* dense, const float* 
     int64_t blocks = ((int64_t)B + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * per_sm;
     if (blocks > cap) blocks = cap;
-    return check_launch_pdl(launch_pdl(kern, (int)blocks, kWarps * kWarp, smem, stream, grad_out, dense, pooled, B, P,
-                                       gd, gp, status),
+    return check_launch_pdl(launch_pdl(kern, (int)blocks, kWarps * kWarp, smem, stream, grad_out, dense, pooled, ga, B,
+                                       P, gd, gp, status),
                             "interact_bwd_regs_kernel");
 }
 
@@ -392,10 +442,50 @@ extern "C" dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_
     if (dtype == DLRM_F32 && regs_bwd_supported(F, D, out_cols)) {
         const float* d = static_cast<const float*>(d_dense);
         const float* p = static_cast<const float*>(d_pooled);
-        return F == 26 ? launch_regs<27>(d_grad_out, d, p, B, out_cols, d_grad_dense, d_grad_pooled, nullptr, st)
-                       : launch_regs<9>(d_grad_out, d, p, B, out_cols, d_grad_dense, d_grad_pooled, nullptr, st);
+        const RegGather none{};
+        return F == 26 ? launch_regs<27, false>(d_grad_out, d, p, none, B, out_cols, d_grad_dense, d_grad_pooled,
+                                                nullptr, st)
+                       : launch_regs<9, false>(d_grad_out, d, p, none, B, out_cols, d_grad_dense, d_grad_pooled,
+                                               nullptr, st);
     }
     if (dtype == DLRM_F32)
         return dispatch<float>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);
     return dispatch<__half>(d_grad_out, d_dense, d_pooled, F, D, B, out_cols, d_grad_dense, d_grad_pooled, st);
+}
+
+extern "C" dlrm_status dlrm_emb_interact_bwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                            int F, int D, int B, const int32_t* d_indices, const int32_t* d_offsets,
+                                            int64_t nnz, const float* d_grad_out, const void* d_dense, int out_cols,
+                                            float* d_grad_dense, float* d_grad_pooled, unsigned flags,
+                                            uint32_t* d_status, void* stream)
+{
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: bad dtype");
+    if (F < 1 || D < 1 || B < 0)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: need F >= 1, D >= 1, B >= 0");
+    if (nnz < 0 || nnz >= (int64_t)1 << 31 || (int64_t)F * B >= (int64_t)1 << 31)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: nnz and F*B must be below 2^31");
+    const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
+    if (out_cols < W)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: out_cols %d < D + F(F+1)/2 = %lld", out_cols,
+                    (long long)W);
+    if (!d_tables || !d_row_base || !d_offsets || !d_grad_out || !d_dense || !d_grad_dense || !d_grad_pooled ||
+        (nnz > 0 && !d_indices))
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: null device pointer");
+    if (flags & ~DLRM_FLAG_HASH_INDICES)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: unknown flag bits 0x%x", flags);
+    if (dtype != DLRM_F32 || !regs_bwd_supported(F, D, out_cols) || !aligned16(d_tables) || !aligned16(d_grad_out) ||
+        !aligned16(d_dense) || !aligned16(d_grad_dense) || !aligned16(d_grad_pooled))
+        return fail(DLRM_ERR_UNSUPPORTED,
+                    "dlrm_emb_interact_bwd: needs fp32, D = 128, F in {8, 26}, out_cols a multiple of 4 up to 1024 "
+                    "and 16-byte aligned pointers (use dlrm_emb_fwd + dlrm_interact_bwd otherwise)");
+    if (B == 0) return DLRM_OK;
+    const RegGather ga{(const float*)d_tables, d_row_base, d_indices, d_offsets, nnz,
+                       (flags & DLRM_FLAG_HASH_INDICES) != 0};
+    const float* d = static_cast<const float*>(d_dense);
+    cudaStream_t st = as_stream(stream);
+    return F == 26 ? launch_regs<27, true>(d_grad_out, d, nullptr, ga, B, out_cols, d_grad_dense, d_grad_pooled,
+                                           d_status, st)
+                   : launch_regs<9, true>(d_grad_out, d, nullptr, ga, B, out_cols, d_grad_dense, d_grad_pooled,
+                                          d_status, st);
 }

@@ -47,6 +47,7 @@
 
 #include "common.cuh"
 #include "interact_tc.cuh"
+#include "reg_gather.cuh"
 #include "tcgen05.cuh"
 
 namespace dlrm {
@@ -384,15 +385,6 @@ interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restric
 // The pooled rows (rows 1..F of the buffer) leave by one bulk store, so the
 // lookup's output is written once and never read back.  Pooled rows and
 // interaction are bit-identical to dlrm_emb_fwd + dlrm_interact_fwd.
-struct RegGather {
-    const float* tables;
-    const int64_t* row_base;
-    const int32_t* indices;
-    const int32_t* offsets;
-    int64_t nnz;
-    bool hash;
-};
-
 // Shared memory: the same layout as the register kernel's.
 template <int R>
 constexpr size_t emb_regs_smem_bytes()
@@ -413,9 +405,6 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
     constexpr int kAfter = kPooled ? (R * (R - 1) / 2 + 31) / 32 / 2 : 0;
     constexpr int F = R - 1;
     constexpr int D = kRegD;
-    // bag -> source: a table row (32 bits: 2^32 rows of 512 bytes would not
-    // fit in memory), kRowZero (empty bag, rejected index) or kRowMulti
-    constexpr uint32_t kRowZero = 0xffffffffu, kRowMulti = 0xfffffffeu;
     extern __shared__ __align__(16) float4 zbuf[];
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
@@ -431,98 +420,31 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
     }
     __syncwarp();
     uint32_t phase = 0;
-    int64_t tbase = 0, tn = 0;                    // lane t < F: table t's first row and row count
-    if (lane < F) {
-        tbase = ga.row_base[lane];
-        tn = ga.row_base[lane + 1] - tbase;
-    }
-    auto load_bounds = [&](int64_t smp, int& a, int& e) {
-        a = e = 0;
-        if (lane < F && smp < B) {
-            a = ldg_early_s32(ga.offsets + (int64_t)lane * B + smp);
-            e = ldg_early_s32(ga.offsets + (int64_t)lane * B + smp + 1);
-        }
-    };
-    auto clamp_bounds = [&](int& a, int& e) {     // into [0, nnz], flagging malformed lists
-        int64_t x = a, y = e;
-        if (x < 0 || y < x || y > ga.nnz) {
-            set_status(status, DLRM_STATUS_BAD_OFFSETS);
-            x = x < 0 ? 0 : (x > ga.nnz ? ga.nnz : x);
-            y = y < x ? x : (y > ga.nnz ? ga.nnz : y);
-        }
-        a = (int)x;
-        e = (int)y;
-    };
-    auto resolve = [&](int a, int e, int idx) -> uint32_t {
-        if (lane >= F || e - a == 0) return kRowZero;
-        if (e - a > 1) return kRowMulti;
-        int64_t i = idx;
-        if (ga.hash && tn > 0) {
-            i %= tn;
-            if (i < 0) i += tn;
-        } else if (ga.hash || i < 0 || i >= tn || tbase + i >= (int64_t)kRowMulti) {
-            set_status(status, DLRM_STATUS_OOB_INDEX);
-            return kRowZero;
-        }
-        return (uint32_t)(tbase + i);
-    };
-    // fill the buffer with sample smp: the dense row, then bag t's row as row
-    // t + 1.  Lane t < F copies its single-index bag's row and lane F the
-    // dense row, each one 512-byte bulk copy counted on the warp's mbarrier;
-    // zero rows and sums of several rows are stored by the lanes (each its
-    // own 16-byte column); lane 0 arrives once all copies are counted.
+    const BagLanes<F, D> bags(ga, B, lane, status);
+    // fill the buffer with sample smp: the bags' rows as rows 1..F, the dense
+    // row (lane F's bulk copy) as row 0; lane 0 arrives once all are counted
     auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
-        if (lane < F && src_row < kRowMulti) {
-            tc::mbar_expect_tx_only(bar, D * 4);
-            tc::bulk_g2s(mine + (lane + 1) * kWarp, ga.tables + (size_t)src_row * D, D * 4, bar);
-        } else if (lane == F) {
+        bags.gather(mine, src_row, a, e, bar);
+        if (lane == F) {
             tc::mbar_expect_tx_only(bar, D * 4);
             tc::bulk_g2s(mine, dense + smp * D, D * 4, bar);
-        }
-        for (uint32_t zero = __ballot_sync(0xffffffffu, lane < F && src_row == kRowZero); zero; zero &= zero - 1)
-            mine[__ffs(zero) * kWarp + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-        // bags of several indices: fp32 sum in bag order, as in the lookup
-        for (uint32_t multi = __ballot_sync(0xffffffffu, src_row == kRowMulti); multi; multi &= multi - 1) {
-            const int t = __ffs(multi) - 1;
-            const int s1 = __shfl_sync(0xffffffffu, a, t), e1 = __shfl_sync(0xffffffffu, e, t);
-            const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = s1; p < e1; ++p) {
-                int64_t i = __ldg(ga.indices + p);
-                if (ga.hash && n > 0) {
-                    i %= n;
-                    if (i < 0) i += n;
-                } else if (ga.hash || i < 0 || i >= n) {
-                    set_status(status, DLRM_STATUS_OOB_INDEX);
-                    continue;
-                }
-                const float4 r = u4_as_f4(ldg_nc_l1_v4(ga.tables + (base + i) * D + 4 * lane));
-                acc.x += r.x;
-                acc.y += r.y;
-                acc.z += r.z;
-                acc.w += r.w;
-            }
-            mine[(t + 1) * kWarp + lane] = acc;
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar);
     };
 
     int a0, e0, a1, e1;
-    load_bounds(b, a0, e0);
-    load_bounds(b + stride, a1, e1);
-    clamp_bounds(a0, e0);
-    if (b < B) {
-        const int idx0 = (lane < F && e0 - a0 == 1) ? __ldg(ga.indices + a0) : 0;
-        stage(b, resolve(a0, e0, idx0), a0, e0);
-    }
-    clamp_bounds(a1, e1);
+    bags.load_bounds(b, a0, e0);
+    bags.load_bounds(b + stride, a1, e1);
+    bags.clamp(a0, e0);
+    if (b < B) stage(b, bags.resolve(a0, e0, bags.early_index(a0, e0)), a0, e0);
+    bags.clamp(a1, e1);
     for (; b < B; b += stride) {
         const int64_t nb = b + stride;
         // in flight during this sample: the next sample's index, the bounds two samples on
-        const int idx1 = (lane < F && e1 - a1 == 1) ? ldg_early_s32(ga.indices + a1) : 0;
+        const int idx1 = bags.early_index(a1, e1);
         int a2, e2;
-        load_bounds(nb + stride, a2, e2);
+        bags.load_bounds(nb + stride, a2, e2);
         if (!tc::bounded_wait(bar, phase)) {
             if (lane == 0) {
                 set_status(status, DLRM_STATUS_TIMEOUT);
@@ -550,10 +472,10 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
             }
             if (nb < B) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                stage(nb, resolve(a1, e1, idx1), a1, e1);
+                stage(nb, bags.resolve(a1, e1, idx1), a1, e1);
             }
         });
-        clamp_bounds(a2, e2);
+        bags.clamp(a2, e2);
         a1 = a2;
         e1 = e2;
     }

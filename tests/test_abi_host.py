@@ -109,6 +109,27 @@ def test_fused_training_forward_validation(L):
     assert g(FAKE, 0, FAKE, 26, 128, 0, None, FAKE, 0, FAKE, FAKE, 480, 0, None, None) == dl.DLRM_OK
 
 
+def test_gathering_backward_validation(L):
+    f = L.dlrm_emb_interact_bwd
+    # tables, dtype, row_base, F, D, B, indices, offsets, nnz, grad_out, dense, out_cols, gd, gp, flags, status, stream
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 478, FAKE, FAKE, 0, None, None) == \
+        dl.DLRM_ERR_INVALID_ARG
+    assert "out_cols" in _err(L)
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 480, None, FAKE, 0, None, None) == \
+        dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 480, FAKE, FAKE, 2, None, None) == \
+        dl.DLRM_ERR_INVALID_ARG
+    assert f(FAKE, 1, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 480, FAKE, FAKE, 0, None, None) == \
+        dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 25, 128, 8, FAKE, FAKE, 200, FAKE, FAKE, 480, FAKE, FAKE, 0, None, None) == \
+        dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 481, FAKE, FAKE, 0, None, None) == \
+        dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, 208, FAKE, FAKE, 480, FAKE, FAKE_MIS, 0, None, None) == \
+        dl.DLRM_ERR_UNSUPPORTED
+    assert f(FAKE, 0, FAKE, 26, 128, 0, None, FAKE, 0, FAKE, FAKE, 480, FAKE, FAKE, 0, None, None) == dl.DLRM_OK
+
+
 def test_sgd_workspace_and_validation(L):
     ws = L.dlrm_emb_bwd_sgd_workspace_size
     assert ws(-1, 128, 10) == 0 and ws(10, 3, 10) == 0 and ws(10, 128, 0) == 0

@@ -1,6 +1,7 @@
 """GPU parity of the fp32 lookup + interaction in one pass: the training
 forward dlrm_emb_interact_fwd_train (pooled rows written for the backward)
-and dlrm_emb_interact_fwd with fp32 tables (no pooled output).
+and dlrm_emb_interact_fwd with fp32 tables (no pooled output); and of the
+backward that gathers the pooled rows again, dlrm_emb_interact_bwd.
 
 Both compute what dlrm_emb_fwd followed by dlrm_interact_fwd computes, with
 the same arithmetic in the same order, so pooled rows, interaction output and
@@ -124,3 +125,84 @@ def test_malformed_offsets_are_clamped_like_the_lookup(cuda_lib):
     p1, o1, s1 = fused_train(cuda_lib, *args)
     assert s1 == s2 and s1 & cuda_lib.DLRM_STATUS_BAD_OFFSETS
     assert _same(p1, p2) and _same(o1, o2)
+
+
+def bwd_two_calls(dl, tab, row_base, F, D, B, idx, off, dense, go, P, flags=0):
+    pooled = torch.empty(B, F, D, device=dev())
+    gd = torch.full((B, D), float("nan"), device=dev())
+    gp = torch.full((B, F, D), float("nan"), device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    dl.dlrm_emb_fwd(tab, row_base, F, D, B, idx, off, pooled, flags=flags, status=st)
+    dl.dlrm_interact_bwd(go, dense, pooled, F, D, B, P, gd, gp)
+    torch.cuda.synchronize()
+    return gd.cpu().numpy(), gp.cpu().numpy(), int(st.item())
+
+
+def bwd_gather(dl, tab, row_base, F, D, B, idx, off, dense, go, P, flags=0):
+    gd = torch.full((B, D), float("nan"), device=dev())
+    gp = torch.full((B, F, D), float("nan"), device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    dl.dlrm_emb_interact_bwd(tab, row_base, F, D, B, idx, off, go, dense, P, gd, gp, flags=flags, status=st)
+    torch.cuda.synchronize()
+    return gd.cpu().numpy(), gp.cpu().numpy(), int(st.item())
+
+
+@pytest.mark.parametrize("B", [1, 5, 1021, 4099, 65536])
+def test_gathering_backward_matches_two_calls(cuda_lib, B):
+    """dlrm_emb_interact_bwd == dlrm_interact_bwd(dlrm_emb_fwd(...)) bit for bit at the training
+    shapes; past 1824 samples every warp takes several, so the bag pipeline (bounds two samples
+    ahead, index one ahead) is exercised; sampled rows against the oracle as well."""
+    w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=1.2, train=True)
+    tab = device_tables(cuda_lib, w)
+    args = (tab, to_dev(w.row_base), w.F, w.D, w.B, to_dev(w.indices), to_dev(w.offsets), to_dev(w.dense),
+            to_dev(w.grad_out), w.out_cols)
+    d2, p2, s2 = bwd_two_calls(cuda_lib, *args)
+    d1, p1, s1 = bwd_gather(cuda_lib, *args)
+    assert s1 == s2 == 0
+    assert _same(d1, d2) and _same(p1, p2)
+    samples = np.unique(np.concatenate([np.arange(min(B, 6)), [B - 1]]))
+    c = Compact(w, samples)
+    rp, _ = oracle.emb_fwd(c.tables, c.row_base, c.F, c.D, c.B, c.indices, c.offsets)
+    rd, rg = oracle.interact_bwd(w.grad_out[samples], c.dense, rp)
+    from test_gpu_interaction import abs_bwd
+    sd, sp = abs_bwd(w.grad_out[samples].astype(np.float64), c.dense, rp)
+    assert_within_abs_sum(d1[samples], rd, sd, 1e-5, "grad_dense vs oracle")
+    assert_within_abs_sum(p1[samples], rg, sp, 1e-5, "grad_pooled vs oracle")
+
+
+@pytest.mark.parametrize("F,P", [(26, 480), (8, 164), (26, 1024)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_gathering_backward_ragged_bags(cuda_lib, F, P, flags):
+    rng = np.random.default_rng(F * 13 + P + flags)
+    B, D = 2111, 128
+    rows = rng.integers(1, 50, size=F)
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tab = to_dev(rng.standard_normal((row_base[-1], D)).astype(np.float32))
+    counts = rng.choice([0, 1, 1, 1, 2, 5], size=F * B)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    idx = rng.integers(-60, 60, size=off[-1]).astype(np.int32)
+    dense = to_dev(rng.standard_normal((B, D)).astype(np.float32))
+    go = to_dev((rng.standard_normal((B, P)) * 1e-2).astype(np.float32))
+    args = (tab, to_dev(row_base), F, D, B, to_dev(idx), to_dev(off), dense, go, P, flags)
+    d2, p2, s2 = bwd_two_calls(cuda_lib, *args)
+    d1, p1, s1 = bwd_gather(cuda_lib, *args)
+    assert s1 == s2
+    assert _same(d1, d2) and _same(p1, p2)
+
+
+def test_gathering_backward_malformed_offsets(cuda_lib):
+    rng = np.random.default_rng(6)
+    F, D, B, P = 26, 128, 300, 480
+    row_base = np.concatenate([[0], np.cumsum(np.full(F, 40))]).astype(np.int64)
+    tab = to_dev(rng.standard_normal((row_base[-1], D)).astype(np.float32))
+    off = np.arange(F * B + 1, dtype=np.int32)
+    off[17] = 5
+    off[400] = 10**6
+    idx = rng.integers(0, 40, size=F * B).astype(np.int32)
+    dense = to_dev(rng.standard_normal((B, D)).astype(np.float32))
+    go = to_dev((rng.standard_normal((B, P)) * 1e-2).astype(np.float32))
+    args = (tab, to_dev(row_base), F, D, B, to_dev(idx), to_dev(off), dense, go, P)
+    d2, p2, s2 = bwd_two_calls(cuda_lib, *args)
+    d1, p1, s1 = bwd_gather(cuda_lib, *args)
+    assert s1 == s2 and s1 & cuda_lib.DLRM_STATUS_BAD_OFFSETS
+    assert _same(d1, d2) and _same(p1, p2)
