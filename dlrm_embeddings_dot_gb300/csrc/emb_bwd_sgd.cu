@@ -322,7 +322,7 @@ __device__ __forceinline__ float4 load_grad4(const GT* p)
 }
 
 template <int MC, typename GT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
                const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
                float* __restrict__ partials, uint64_t* __restrict__ split_list, uint32_t* split_count,
@@ -330,8 +330,9 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
 {
     pdl_wait_and_release();
     // positions per batch: their gradient rows, and the table rows of the runs
-    // that end (complete) among them, are all loaded before any is used
-    constexpr int U = MC >= 8 ? 1 : 8 / MC;
+    // that end (complete) among them, are all loaded before any is used (6 per
+    // batch at three blocks per SM measured best at the 64K training shapes)
+    constexpr int U = MC >= 8 ? 1 : (6 / MC > 0 ? 6 / MC : 1);
     const int lane = threadIdx.x % kWarp;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
