@@ -39,7 +39,7 @@ namespace {
 constexpr uint32_t kSkipKey = 0xFFFFFFFFu;
 constexpr int kSortThreads = 256;
 constexpr int kItems = 4;                      // keys per thread (1,024-key tiles measured best: 2 to 16 tried)
-constexpr int kTile = kSortThreads * kItems;   // 2048 keys per tile
+constexpr int kTile = kSortThreads * kItems;   // 1024 keys per tile
 constexpr int kChunk = 32;                     // positions per segment chunk
 constexpr int kFixThreads = 512;
 
