@@ -245,7 +245,7 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
     // sample smp's Z rows and gradient row, all counted on the warp's mbarrier
     auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
         if constexpr (kGather) {
-            bags.template gather<kRowsAsync>(zs, src_row, a, e, bar);
+            bags.template gather<kRowsAsync, 2>(zs, src_row, a, e, bar);
             if (lane == F) {
                 tc::mbar_expect_tx_only(bar, D * 4);
                 tc::bulk_g2s(zs, dense + smp * D, D * 4, bar);

@@ -332,19 +332,37 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                     const int row = sm * kSlot + t;
                     for (int c = lane; c < cpr; c += kWarp) {
                         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int p = s1; p < e1; ++p) {
-                            int64_t i = __ldg(ga.indices + p);
-                            if (ga.hash && n > 0) {
-                                i %= n;
-                                if (i < 0) i += n;
-                            } else if (ga.hash || i < 0 || i >= n) {
-                                set_status(status, DLRM_STATUS_OOB_INDEX);
-                                continue;
-                            }
-                            float f[8];
-                            h8_to_f8(ldg_nc_v4(ga.tables + (base + i) * D + 8 * c), f);
+                        constexpr int kMultiU = 4;   // positions in flight, added in bag order
+                        for (int p0 = s1; p0 < e1; p0 += kMultiU) {
+                            int64_t row[kMultiU];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) acc[u] += f[u];
+                            for (int u = 0; u < kMultiU; ++u) row[u] = p0 + u < e1 ? __ldg(ga.indices + p0 + u) : -1;
+                            uint4 r[kMultiU];
+#pragma unroll
+                            for (int u = 0; u < kMultiU; ++u) {
+                                int64_t i = row[u];
+                                row[u] = -1;
+                                if (p0 + u < e1) {
+                                    if (ga.hash && n > 0) {
+                                        i %= n;
+                                        if (i < 0) i += n;
+                                        row[u] = base + i;
+                                    } else if (ga.hash || i < 0 || i >= n) {
+                                        set_status(status, DLRM_STATUS_OOB_INDEX);
+                                    } else {
+                                        row[u] = base + i;
+                                    }
+                                }
+                                r[u] = row[u] >= 0 ? ldg_nc_v4(ga.tables + row[u] * D + 8 * c) : make_uint4(0, 0, 0, 0);
+                            }
+#pragma unroll
+                            for (int u = 0; u < kMultiU; ++u)
+                                if (row[u] >= 0) {
+                                    float f[8];
+                                    h8_to_f8(r[u], f);
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v) acc[v] += f[v];
+                                }
                         }
                         const uint4 w = f8_to_h8(acc);
                         const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);

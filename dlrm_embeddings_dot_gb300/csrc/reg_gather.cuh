@@ -89,8 +89,11 @@ struct BagLanes {
 
     // kCopyAsync: every lane copies its 16-byte column of each single-index row
     // with cp.async (completion: cp.async.wait_group by the same lane, which
-    // reads only the columns it copied) instead of lane t's bulk copy of row t
-    template <bool kCopyAsync = false>
+    // reads only the columns it copied) instead of lane t's bulk copy of row t.
+    // kMultiU: positions of a several-index bag in flight (indices, then rows),
+    // added in bag order; few enough that the caller's live registers are not
+    // spilled
+    template <bool kCopyAsync = false, int kMultiU = 4>
     __device__ __forceinline__ void gather(float4* buf, uint32_t src_row, int a, int e, uint64_t* bar) const
     {
         if constexpr (kCopyAsync) {
@@ -116,20 +119,38 @@ struct BagLanes {
             const int s1 = __shfl_sync(0xffffffffu, a, t), e1 = __shfl_sync(0xffffffffu, e, t);
             const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = s1; p < e1; ++p) {
-                int64_t i = __ldg(ga.indices + p);
-                if (ga.hash && n > 0) {
-                    i %= n;
-                    if (i < 0) i += n;
-                } else if (ga.hash || i < 0 || i >= n) {
-                    set_status(status, DLRM_STATUS_OOB_INDEX);
-                    continue;
+            for (int p0 = s1; p0 < e1; p0 += kMultiU) {
+                int idx[kMultiU];
+#pragma unroll
+                for (int u = 0; u < kMultiU; ++u) idx[u] = p0 + u < e1 ? __ldg(ga.indices + p0 + u) : 0;
+                uint32_t row[kMultiU];   // kRowZero: skipped or past the bag
+                float4 r[kMultiU];
+#pragma unroll
+                for (int u = 0; u < kMultiU; ++u) {
+                    int64_t i = idx[u];
+                    row[u] = kRowZero;
+                    if (p0 + u < e1) {
+                        if (ga.hash && n > 0) {
+                            i %= n;
+                            if (i < 0) i += n;
+                            row[u] = (uint32_t)(base + i);
+                        } else if (ga.hash || i < 0 || i >= n) {
+                            set_status(status, DLRM_STATUS_OOB_INDEX);
+                        } else {
+                            row[u] = (uint32_t)(base + i);
+                        }
+                    }
+                    r[u] = row[u] != kRowZero ? u4_as_f4(ldg_nc_l1_v4(ga.tables + (size_t)row[u] * D + 4 * lane))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const float4 r = u4_as_f4(ldg_nc_l1_v4(ga.tables + (base + i) * D + 4 * lane));
-                acc.x += r.x;
-                acc.y += r.y;
-                acc.z += r.z;
-                acc.w += r.w;
+#pragma unroll
+                for (int u = 0; u < kMultiU; ++u)
+                    if (row[u] != kRowZero) {
+                        acc.x += r[u].x;
+                        acc.y += r[u].y;
+                        acc.z += r[u].z;
+                        acc.w += r[u].w;
+                    }
             }
             buf[(t + 1) * kWarp + lane] = acc;
         }
