@@ -305,24 +305,36 @@ __device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ k
 }
 
 // --------------------------------------------------------- 3. segment sums
-// Four consecutive gradient elements as fp32: one 16-byte load of fp32, or an
-// 8-byte load of fp16 widened exactly.
+// A gradient chunk of four elements as loaded: fp32 as one float4, fp16 as
+// the 8 loaded bytes (half the registers, so twice the loads fit in flight),
+// widened exactly to fp32 where it is added.
 template <typename GT>
-__device__ __forceinline__ float4 load_grad4(const GT* p)
+struct GradRaw { using T = float4; };
+template <>
+struct GradRaw<__half> { using T = uint2; };
+
+template <typename GT>
+__device__ __forceinline__ typename GradRaw<GT>::T load_grad_raw(const GT* p)
 {
     if constexpr (sizeof(GT) == 4) {
         return u4_as_f4(ldg_nc_v4(p));
     } else {
         uint2 r;
         asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
-        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
-        return make_float4(a.x, a.y, c.x, c.y);
+        return r;
     }
 }
 
+__device__ __forceinline__ float4 widen(float4 v) { return v; }
+__device__ __forceinline__ float4 widen(uint2 r)
+{
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+    return make_float4(a.x, a.y, c.x, c.y);
+}
+
 template <int MC, typename GT>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, MC >= 8 ? 2 : 3)   // rows past 512 elements: registers for 8 float4 sums
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
                const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
                float* __restrict__ partials, uint64_t* __restrict__ split_list, uint32_t* split_count,
@@ -330,9 +342,11 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
 {
     pdl_wait_and_release();
     // positions per batch: their gradient rows, and the table rows of the runs
-    // that end (complete) among them, are all loaded before any is used (6 per
-    // batch at three blocks per SM measured best at the 64K training shapes)
-    constexpr int U = MC >= 8 ? 1 : (6 / MC > 0 ? 6 / MC : 1);
+    // that end (complete) among them, are all loaded before any is used (at
+    // three blocks per SM and the 64K training shapes, 6 measured best for fp32
+    // gradients; 8 for fp16, 243 against 281 us at 6)
+    constexpr int U0 = sizeof(GT) == 2 && MC <= 2 ? 8 : 6;
+    constexpr int U = MC >= 8 ? 1 : (U0 / MC > 0 ? U0 / MC : 1);
     const int lane = threadIdx.x % kWarp;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
@@ -370,7 +384,8 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
         uint32_t file_key = kSkipKey;   // key of a run that starts here and crosses the chunk's end
         for (int q0 = 0; q0 < nvalid; q0 += U) {
-            float4 v[U][MC], w[U][MC];
+            typename GradRaw<GT>::T v[U][MC];
+            float4 w[U][MC];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int q = q0 + u;
@@ -380,11 +395,11 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
 #pragma unroll
                 for (int m = 0; m < MC; ++m) {
                     const int col = lane + m * kWarp;
-                    v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u][m] = typename GradRaw<GT>::T{};
                     w[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
                     // row < nbags holds for pairs made from well-formed offsets
                     if (q < nvalid && col < c4 && (int64_t)row < nbags)
-                        v[u][m] = load_grad4<GT>(grad + (int64_t)row * D + 4 * col);
+                        v[u][m] = load_grad_raw<GT>(grad + (int64_t)row * D + 4 * col);
                     if (done && col < c4) w[u][m] = *reinterpret_cast<const float4*>(tables + (int64_t)qk * D + 4 * col);
                 }
             }
@@ -394,10 +409,11 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                 if (q >= nvalid) break;
 #pragma unroll
                 for (int m = 0; m < MC; ++m) {
-                    acc[m].x += v[u][m].x;
-                    acc[m].y += v[u][m].y;
-                    acc[m].z += v[u][m].z;
-                    acc[m].w += v[u][m].w;
+                    const float4 g = widen(v[u][m]);
+                    acc[m].x += g.x;
+                    acc[m].y += g.y;
+                    acc[m].z += g.z;
+                    acc[m].w += g.w;
                 }
                 if (!((ends >> q) & 1u)) continue;
                 const uint32_t qk = __shfl_sync(0xffffffffu, key, q);
