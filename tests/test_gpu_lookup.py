@@ -139,3 +139,70 @@ def test_malformed_offsets_are_clamped_and_flagged(cuda_lib):
     torch.cuda.synchronize()
     assert int(status.item()) & cuda_lib.DLRM_STATUS_BAD_OFFSETS
     assert torch.isfinite(pooled).all()
+
+
+# Rows one load instruction moves whole (32 lanes x 16 bytes): the single-hot
+# kernel sums the bags of several indices of each 32-bag group as one list of
+# positions, for every batch.
+WHOLE_ROW = [(inputs.F32, 128), (inputs.F16, 256)]
+
+
+@pytest.mark.parametrize("dt,D", WHOLE_ROW)
+@pytest.mark.parametrize("flags", [0, 1])
+def test_whole_row_mixed_bags_hashing_and_skips(cuda_lib, dt, D, flags):
+    """Empty, single and several-index bags (up to 40: a bag's positions span
+    several rounds of 32), indices outside the table skipped and flagged, or
+    folded into it with DLRM_FLAG_HASH_INDICES; 633 bags, a ragged last group."""
+    rng = np.random.default_rng(D + flags)
+    F, B = 3, 211
+    rows = np.array([10, 3, 50])
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tables = rng.uniform(-1, 1, size=(row_base[-1], D)).astype(np.float16 if dt == inputs.F16 else np.float32)
+    counts = rng.choice([0, 1, 1, 2, 3, 7, 40], size=F * B)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    idx = rng.integers(-60, 60, size=offsets[-1]).astype(np.int32)
+    got, status = run_lookup(cuda_lib, to_dev(tables), row_base, F, D, B, idx, offsets, flags=flags)
+    ref, rs = oracle.emb_fwd(tables, row_base, F, D, B, idx, offsets, flags=flags)
+    absum, _ = oracle.emb_fwd(np.abs(tables).astype(np.float64), row_base, F, D, B, idx, offsets, flags=flags)
+    assert status == rs == (0 if flags else oracle.STATUS_OOB)
+    assert_within_abs_sum(got, ref, absum, 1e-5 if dt == inputs.F32 else 2e-2, "pooled")
+    for g in np.flatnonzero(counts <= 1):   # copies of the row, or zeros
+        t, b = g // B, g % B
+        assert np.array_equal(got[b, t], ref[b, t])
+
+
+@pytest.mark.parametrize("dt,D", WHOLE_ROW)
+def test_whole_row_malformed_offsets(cuda_lib, dt, D):
+    """Negative, decreasing and past-nnz offsets: each bag is clamped on its
+    own (start into [0, nnz], end into [start, nnz]) and the status bit set;
+    the result equals the oracle on the CSR rebuilt from the clamped bags."""
+    rng = np.random.default_rng(11 + D)
+    F, B = 2, 100
+    rows = np.array([30, 20])
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tables = rng.uniform(-1, 1, size=(row_base[-1], D)).astype(np.float16 if dt == inputs.F16 else np.float32)
+    counts = rng.choice([1, 2, 5], size=F * B)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    nnz = int(off[-1])
+    idx = rng.integers(0, 20, size=nnz).astype(np.int32)
+    off[17] = 3            # bag 16 ends before it starts, bag 17 starts early
+    off[40] = nnz + 50     # past the index list
+    off[77] = -5           # negative
+    pooled = torch.full((B, F, D), float("nan"), dtype=torch_dtype(dt), device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    cuda_lib.dlrm_emb_fwd(to_dev(tables), to_dev(row_base), F, D, B, to_dev(idx), to_dev(off.astype(np.int32)),
+                          pooled, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & cuda_lib.DLRM_STATUS_BAD_OFFSETS
+    s = np.clip(off[:-1], 0, nnz)
+    e = np.minimum(np.maximum(off[1:], s), nnz)
+    cidx = np.concatenate([idx[a:b] for a, b in zip(s, e)]).astype(np.int32)
+    coff = np.concatenate([[0], np.cumsum(e - s)])
+    ref, rs = oracle.emb_fwd(tables, row_base, F, D, B, cidx, coff)
+    absum, _ = oracle.emb_fwd(np.abs(tables).astype(np.float64), row_base, F, D, B, cidx, coff)
+    assert rs == 0
+    got = pooled.cpu().numpy()
+    assert_within_abs_sum(got, ref, absum, 1e-5 if dt == inputs.F32 else 2e-2, "pooled")
+    for g in np.flatnonzero(e - s <= 1):
+        t, b = g // B, g % B
+        assert np.array_equal(got[b, t], ref[b, t])
