@@ -157,22 +157,21 @@ emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ r
     }
 }
 
-// The bags of several indices among a warp's 32 (lane k: bag k's length, first
-// position, table and pooled row), one row per load instruction.  Their
-// positions form one list in bag order: each lane takes one of 32 positions at
-// a time, finds its bag (the last lane whose list offset is at most the
-// position), loads and resolves its index; the warp then adds the rows kFlatU
-// at a time, each bag's in position order from zero in fp32 exactly as
-// pool_bag does, and stores a bag's sum when the next bag begins.  Index loads
-// are coalesced and a row waits for one index load, not a bag's worth.
+// The bags of several indices among the warp's 32 bags g0 + k (lane k holds
+// bag k's length), one row per load instruction.  Their positions form one
+// list in bag order: each lane takes one of 32 positions at a time, finds its
+// bag (the last lane whose list offset is at most the position), loads and
+// resolves its index; the warp then adds the rows kFlatU at a time, each bag's
+// in position order from zero in fp32 exactly as pool_bag does, and stores a
+// bag's sum when the next bag begins.  Index loads are coalesced and a row
+// waits for one index load, not a bag's worth.
 constexpr int kFlatU = 4;
 
 template <typename T, typename TO>
 __device__ __forceinline__ void pool_flat(const T* __restrict__ tables, const int64_t* __restrict__ row_base,
                                           const int32_t* __restrict__ indices, const int32_t* __restrict__ offsets,
-                                          TO* __restrict__ pooled, int F, int D, int B, int64_t g0, int64_t nbags,
-                                          int64_t nnz, int lane, int cl, bool active, int len, bool hash,
-                                          uint32_t* status)
+                                          TO* __restrict__ pooled, int F, int D, int B, int64_t g0, int64_t nnz,
+                                          int lane, int cl, bool active, int len, bool hash, uint32_t* status)
 {
     constexpr int V = Vec<T>::n;
     const int cnt = len > 1 ? len : 0;
@@ -185,7 +184,6 @@ __device__ __forceinline__ void pool_flat(const T* __restrict__ tables, const in
         start = (int)s;
         tbl = (int)(g / B);
     }
-    (void)nbags;
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
@@ -249,7 +247,7 @@ __device__ __forceinline__ void pool_flat(const T* __restrict__ tables, const in
 // RPI = 32/G rows per load instruction and U such instructions in flight per
 // lane.  Writes go to pooled row b*F + t, a full row per group of lanes.
 // Bags that do not hold exactly one index are summed afterwards by the
-// whole warp.
+// whole warp (pool_flat where a load instruction moves a whole row).
 template <typename T, typename TO, int G>
 __device__ __forceinline__ void single_hot_body(const T* __restrict__ tables, const int64_t* __restrict__ row_base,
                                                 int F, int D, int B, const int32_t* __restrict__ indices,
@@ -305,8 +303,8 @@ __device__ __forceinline__ void single_hot_body(const T* __restrict__ tables, co
         uint32_t multi = __ballot_sync(0xffffffffu, len > 1);
         if constexpr (RPI == 1) {
             if (multi)
-                pool_flat<T, TO>(tables, row_base, indices, offsets, pooled, F, D, B, g0, nbags, nnz, lane, cl, active,
-                                 len, hash, status);
+                pool_flat<T, TO>(tables, row_base, indices, offsets, pooled, F, D, B, g0, nnz, lane, cl, active, len,
+                                 hash, status);
         } else {
             // (several rows per load instruction) the whole warp, RPI bags at a time
             while (multi) {
