@@ -625,7 +625,7 @@ using namespace dlrm;
 
 extern "C" size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows)
 {
-    if (nnz < 0 || nnz >= ((int64_t)1 << 31) || D < 1 || D % 4 != 0 || D > 1024 || total_rows < 1 ||
+    if (nnz < 0 || nnz > DLRM_MAX_NNZ || D < 1 || D % 4 != 0 || D > 1024 || total_rows < 1 ||
         total_rows >= 0xFFFFFFFFll)
         return 0;
     return carve(nullptr, nnz, D).bytes;
@@ -639,8 +639,8 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     clear_error();
     if (F < 1 || D < 1 || B < 0)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: need F >= 1, D >= 1, B >= 0");
-    if (nnz < 0 || nnz >= ((int64_t)1 << 31))
-        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: nnz must be in [0, 2^31)");
+    if (nnz < 0 || nnz > DLRM_MAX_NNZ)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: nnz must be in [0, DLRM_MAX_NNZ]");
     if ((int64_t)F * B >= ((int64_t)1 << 31))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: F*B must be below 2^31");
     if (total_rows < 1 || total_rows >= 0xFFFFFFFFll)

@@ -417,8 +417,8 @@ extern "C" dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype,
     if (F < 1 || D < 1 || B < 0)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: need F >= 1, D >= 1, B >= 0 (got %d, %d, %d)",
                     F, D, B);
-    if (nnz < 0 || nnz >= (int64_t)1 << 31)
-        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: nnz must be in [0, 2^31)");
+    if (nnz < 0 || nnz > DLRM_MAX_NNZ)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: nnz must be in [0, DLRM_MAX_NNZ]");
     if ((int64_t)F * B >= (int64_t)1 << 31)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: F*B must be below 2^31");
     if (!d_tables || !d_row_base || !d_offsets || !d_pooled || (nnz > 0 && !d_indices))

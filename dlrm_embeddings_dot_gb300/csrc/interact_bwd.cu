@@ -463,8 +463,8 @@ extern "C" dlrm_status dlrm_emb_interact_bwd(const void* d_tables, dlrm_dtype dt
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: need F >= 1, D >= 1, B >= 0");
-    if (nnz < 0 || nnz >= (int64_t)1 << 31 || (int64_t)F * B >= (int64_t)1 << 31)
-        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: nnz and F*B must be below 2^31");
+    if (nnz < 0 || nnz > DLRM_MAX_NNZ || (int64_t)F * B >= (int64_t)1 << 31)
+        return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: need nnz <= DLRM_MAX_NNZ and F*B < 2^31");
     const int64_t W = (int64_t)D + (int64_t)F * (F + 1) / 2;
     if (out_cols < W)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: out_cols %d < D + F(F+1)/2 = %lld", out_cols,

@@ -68,6 +68,11 @@ typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
                                       dlrm_interact_bwd_f16); with a static loss scale S pass lr / S
                                       (exact in fp32 for a power-of-two S such as the pages' 1024) */
 
+/* The most indices (nnz) any entry point takes, 2^31 - 65: index positions, and the kernels'
+   32-bit position counters that step up to 32 past them, stay below 2^31.  Larger nnz is
+   DLRM_ERR_INVALID_ARG. */
+#define DLRM_MAX_NNZ 2147483583LL
+
 /* bits OR-ed into *d_status by kernels */
 #define DLRM_STATUS_OOB_INDEX 1u   /* an index outside [0, N_t) with hashing off: it was skipped */
 #define DLRM_STATUS_TIMEOUT   2u   /* a bounded on-chip wait gave up; the output is incomplete */
@@ -93,7 +98,7 @@ typedef enum { DLRM_F32 = 0, DLRM_F16 = 1 } dlrm_dtype;
  *   d_indices  int32 [nnz];  d_offsets int32 [F*B+1]
  *   d_pooled   [B][F][D] of dtype, 16-byte aligned (output); fp16 with
  *              DLRM_FLAG_POOLED_F16 (fp32 tables only)
- * Requires F >= 1, D >= 1, B >= 0, 0 <= nnz < 2^31, D*s % 16 == 0.
+ * Requires F >= 1, D >= 1, B >= 0, 0 <= nnz <= DLRM_MAX_NNZ, D*s % 16 == 0.
  */
 dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
                          int F, int D, int B, const int32_t* d_indices,

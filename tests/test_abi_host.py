@@ -36,6 +36,42 @@ def _declared():
     return names
 
 
+def test_binding_constants_match_the_header():
+    """Every integer macro and enum value of include/dlrm.h that the binding also defines has
+    the same value."""
+    src = open(os.path.join(ROOT, "include", "dlrm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    macros = {m.group(1): int(m.group(2), 0)
+              for m in re.finditer(r"#define\s+(DLRM_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)(?:u|LL|ll|U)?\b", src)}
+    macros.update({m.group(1): int(m.group(2))
+                   for m in re.finditer(r"\b(DLRM_[A-Z0-9_]+)\s*=\s*(\d+)\s*[,}]", src)})
+    assert {"DLRM_MAX_NNZ", "DLRM_FLAG_HASH_INDICES", "DLRM_STATUS_BAD_OFFSETS", "DLRM_OK",
+            "DLRM_ERR_INVALID_ARG", "DLRM_F16"} <= set(macros)
+    shared = [n for n in macros if hasattr(dl, n)]
+    assert len(shared) >= 8
+    for n in shared:
+        assert getattr(dl, n) == macros[n], n
+    assert dl.DLRM_MAX_NNZ == 2**31 - 65
+
+
+def test_nnz_past_the_bound_is_rejected(L):
+    """nnz above DLRM_MAX_NNZ (index positions plus the kernels' position steps must stay
+    below 2^31) is an argument error at every entry point that takes it."""
+    big = dl.DLRM_MAX_NNZ + 1
+    assert L.dlrm_emb_fwd(FAKE, 0, FAKE, 1, 4, 2, FAKE, FAKE, big, FAKE, 0, None, None) == dl.DLRM_ERR_INVALID_ARG
+    assert "DLRM_MAX_NNZ" in _err(L)
+    assert L.dlrm_emb_interact_fwd_train(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, big, FAKE, FAKE, FAKE, 480, 0, None,
+                                         None) == dl.DLRM_ERR_INVALID_ARG
+    assert L.dlrm_emb_interact_fwd(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, big, FAKE, FAKE, 480, 0, None,
+                                   None) == dl.DLRM_ERR_INVALID_ARG
+    assert L.dlrm_emb_interact_bwd(FAKE, 0, FAKE, 26, 128, 8, FAKE, FAKE, big, FAKE, FAKE, 480, FAKE, FAKE, 0, None,
+                                   None) == dl.DLRM_ERR_INVALID_ARG
+    assert L.dlrm_emb_bwd_sgd_workspace_size(big, 128, 5000) == 0
+    assert L.dlrm_emb_bwd_sgd_workspace_size(dl.DLRM_MAX_NNZ, 128, 5000) > 0
+    assert L.dlrm_emb_bwd_sgd(FAKE, FAKE, 50, 2, 16, 50, FAKE, FAKE, big, FAKE, ctypes.c_float(0.1), FAKE, 1 << 40, 0,
+                              None, None) == dl.DLRM_ERR_INVALID_ARG
+
+
 def test_every_declared_symbol_is_exported(L):
     names = _declared()
     assert {"dlrm_emb_fwd", "dlrm_interact_fwd", "dlrm_interact_bwd", "dlrm_emb_bwd_sgd",
