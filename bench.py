@@ -167,10 +167,11 @@ def cpu_baseline(w, n_samples: int) -> dict:
 
 # ------------------------------------------------------------- GPU benchmark
 def sgd_kernels(total_rows: int) -> int:
-    """Kernels of one dlrm_emb_bwd_sgd call: keys, 3 per radix pass, segment, fixup."""
+    """Kernels of one dlrm_emb_bwd_sgd call: keys (which also counts the first radix digit), scan and
+    scatter of the first pass, count + scan + scatter of each later pass, segment, fixup."""
     nbits = int(total_rows).bit_length()
     npasses = (nbits + 7) // 8
-    return 1 + 3 * npasses + 2
+    return 1 + 2 + 3 * (npasses - 1) + 2
 
 
 def kernels_per_step(total_rows: int) -> int:

@@ -31,6 +31,7 @@ DLRM_STATUS_OOB_INDEX = 1
 DLRM_STATUS_TIMEOUT = 2
 DLRM_STATUS_BAD_OFFSETS = 4
 DLRM_MAX_NNZ = 2**31 - 65
+DLRM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

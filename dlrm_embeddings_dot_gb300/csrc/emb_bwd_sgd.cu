@@ -11,23 +11,24 @@
 //     8 bits per pass, reduce-then-scan (no inter-block waiting):
 //     per-tile digit histograms -> per-digit scan over tiles -> stable
 //     scatter with warp-level ranking (match.any) in position order.
-//  3. segments: the sorted array is cut into chunks of 32 positions; a warp
-//     sums, in ascending position order, the grad rows of each run of equal
-//     keys inside its chunk.  A run wholly inside the chunk updates its row
-//     at once (w = fmaf(-lr, g, w)); a run crossing a chunk edge leaves one
-//     partial sum per chunk it touches.
-//     The chunk where such a run starts finds the run's last chunk (an
-//     exponential probe of chunk heads, then 32-ary refinement) and files
-//     the run with its number of pieces.
-//  4. fixup (one kernel): runs of more than 64 pieces are summed by one block
-//     each (16 warps add 16 contiguous slices of pieces, then the 16 sums in
-//     slice order), the others by one warp each, pieces in chunk order; a
-//     lane keeps up to 4 partial-sum loads in flight.
+//  3. segments: the sorted array is cut into items of kSubs sub-chunks of P
+//     positions (P = 32 for rows of up to 512 bytes).  A warp takes items from a
+//     counter; for each sub-chunk every lane copies its position's gradient row
+//     into shared memory with one bulk copy (so one warp instruction moves 32
+//     rows, and the copies of the next sub-chunk are in flight while this one is
+//     summed).  Each run of equal keys is summed in ascending position order; a
+//     run that starts and ends inside the item updates its row
+//     (w = fmaf(-lr, g, w)) with the table row loaded while the run is summed;
+//     a run crossing an item edge leaves one partial sum per item it touches,
+//     and the item where it starts finds the run's last item and files the run
+//     with its number of pieces.
+//  4. fixup: each filed run's pieces are added in item order (a block of 16
+//     warps over 16 contiguous slices for runs of many pieces, a warp for the
+//     others) and the row is updated.
 // Every order of summation is fixed by the data, so results are bitwise
 // reproducible.  Workspace layout (256-byte aligned pieces):
-//   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] |
-//   partials[2 * nchunks][D] | split_list[nchunks] | long_list[nchunks] (64-bit) |
-//   counters
+//   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] | counters |
+//   partials[2 * nitems][D] | split_list[nitems] | long_list[nitems]
 // The sort ends in keysA/valsA, which the caller may read after the call.
 #include <mutex>
 
@@ -40,25 +41,43 @@ constexpr uint32_t kSkipKey = 0xFFFFFFFFu;
 constexpr int kSortThreads = 256;
 constexpr int kItems = 4;                      // keys per thread (1,024-key tiles measured best: 2 to 16 tried)
 constexpr int kTile = kSortThreads * kItems;   // 1024 keys per tile
-constexpr int kChunk = 32;                     // positions per segment chunk
+
+// segment pass
+constexpr int kSubs = 8;                 // sub-chunks per item
 constexpr int kFixThreads = 512;
+constexpr int kLongPieces = 8;           // runs of more pieces are summed by a whole block
+
+// counters
+constexpr int kCtrSplit = 0;   // entries of split_list
+constexpr int kCtrLong = 1;    // entries of long_list
+constexpr int kCtrItem = 2;    // next segment item
+constexpr int kNumCounters = 4;
+
+int key_bits(int64_t total_rows)
+{
+    int b = 0;
+    while (b < 32 && ((uint64_t)1 << b) <= (uint64_t)total_rows) ++b;   // 2^b > total_rows
+    return b;
+}
 
 struct Ws {
     uint32_t *keys[2], *vals[2];
     uint32_t* hist;
     uint32_t* totals;
+    uint32_t* counters;
     float* partials;
-    uint64_t* split_list;    // runs crossing a chunk edge: first chunk << 32 | pieces, up to kLongPieces pieces
-    uint32_t* split_count;   // [0] entries of split_list, [1] entries of long_list
-    uint64_t* long_list;     // the same for runs of more pieces
+    uint64_t* split_list;
+    uint64_t* long_list;
+    int64_t ntiles, nitems;
     size_t bytes;
 };
 
 Ws carve(void* base, int64_t nnz, int D)
 {
     Ws w;
-    const int64_t ntiles = (nnz + kTile - 1) / kTile;
-    const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
+    w.ntiles = (nnz + kTile - 1) / kTile;
+    const int64_t it = (int64_t)kWarp * kSubs;
+    w.nitems = (nnz + it - 1) / it;
     uint8_t* p = static_cast<uint8_t*>(base);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -70,59 +89,136 @@ Ws carve(void* base, int64_t nnz, int D)
     w.vals[0] = (uint32_t*)take(4 * (size_t)nnz);
     w.keys[1] = (uint32_t*)take(4 * (size_t)nnz);
     w.vals[1] = (uint32_t*)take(4 * (size_t)nnz);
-    w.hist = (uint32_t*)take(4 * 256 * (size_t)ntiles);
+    w.hist = (uint32_t*)take(4 * 256 * (size_t)w.ntiles);
     w.totals = (uint32_t*)take(4 * 256);
-    w.partials = (float*)take(4 * 2 * (size_t)nchunks * D);
-    w.split_list = (uint64_t*)take(8 * (size_t)nchunks);
-    w.long_list = (uint64_t*)take(8 * (size_t)nchunks);
-    w.split_count = (uint32_t*)take(8);
+    w.counters = (uint32_t*)take(4 * kNumCounters);
+    w.partials = (float*)take(4 * 2 * (size_t)w.nitems * D);
+    w.split_list = (uint64_t*)take(8 * (size_t)w.nitems);
+    w.long_list = (uint64_t*)take(8 * (size_t)w.nitems);
     w.bytes = off;
     return w;
 }
 
+__device__ __forceinline__ uint32_t ldg_early_u32(const uint32_t* p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// 16 bytes of a table row, loaded where written (the row is stored later by
+// the same thread, so this is an ordinary coherent load, kept in order with
+// the thread's other memory accesses).
+__device__ __forceinline__ float4 ldg_row_early(const float* p)
+{
+    float4 r;
+    asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p)
+                 : "memory");
+    return r;
+}
+
 // ------------------------------------------------------------------ 1. keys
+// Block b owns bags [b * bpb, (b + 1) * bpb) (feature-major: bag g = t*B + b),
+// writes the keys of their positions and counts the first radix digit
+// (key & mask) of every key it writes: row b of the first pass's histogram.
+// For well-formed offsets the block's positions are the contiguous range
+// offsets[b * bpb] .. offsets[(b + 1) * bpb], the first pass's tile b.
+// G = 1: a thread per bag, kKeyBags bags per thread in flight (bags of about
+// one index); G = 32: a warp per bag.
+constexpr int kKeyBags = 4;
+
 template <int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kSortThreads)
 keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* __restrict__ indices,
             const int32_t* __restrict__ offsets, bool hash, uint32_t* status, uint32_t* __restrict__ keys,
-            uint32_t* __restrict__ vals, int64_t nbags, int64_t nnz, uint32_t* __restrict__ split_count)
+            uint32_t* __restrict__ vals, int64_t nbags, int64_t nnz, int64_t bpb, uint32_t mask,
+            uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ counters)
 {
+    __shared__ uint32_t h[256];
+    h[threadIdx.x] = 0;
     pdl_wait_and_release();
-    if (blockIdx.x == 0 && threadIdx.x < 2) split_count[threadIdx.x] = 0;   // counters of the segment pass
-    const int lane = threadIdx.x % G;
-    const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-    const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
-    for (int64_t g = group; g < nbags; g += ngroups) {   // g = t*B + b (feature-major, like offsets)
-        const int t = (int)((uint32_t)g / (uint32_t)B);   // F * B < 2^31
-        const int b = (int)g - t * B;
-        const int64_t base = row_base[t], n = row_base[t + 1] - base;
-        const uint32_t val = (uint32_t)((int64_t)b * F + t);
-        int64_t s = offsets[g], e = offsets[g + 1];
+    if (blockIdx.x == 0 && threadIdx.x < kNumCounters) counters[threadIdx.x] = 0;   // counters of the segment pass
+    __syncthreads();
+    const int lane = threadIdx.x % kWarp;
+    const int64_t g0 = (int64_t)blockIdx.x * bpb;
+    const int64_t g1 = g0 + bpb < nbags ? g0 + bpb : nbags;
+
+    auto bounds = [&](int64_t& s, int64_t& e) {
         if (s < 0 || e < s || e > nnz) {   // malformed CSR: clamp, flag, stay in bounds
             set_status(status, DLRM_STATUS_BAD_OFFSETS);
             s = s < 0 ? 0 : (s > nnz ? nnz : s);
             e = e < s ? s : (e > nnz ? nnz : e);
         }
-        for (int64_t p = s + lane; p < e; p += G) {
-            int64_t i = indices[p];
-            uint32_t key = kSkipKey;
-            if (hash) {
-                if (n > 0) {
-                    i %= n;
-                    if (i < 0) i += n;
-                    key = (uint32_t)(base + i);
-                } else {
-                    set_status(status, DLRM_STATUS_OOB_INDEX);
-                }
-            } else if (i >= 0 && i < n) {
+    };
+    // one position of a bag of table (base, n): its key, stored with the bag's value and counted
+    auto emit = [&](int64_t p, int32_t raw, int64_t base, int64_t n, uint32_t val) {
+        int64_t i = raw;
+        uint32_t key = kSkipKey;
+        if (hash) {
+            if (n > 0) {
+                i %= n;
+                if (i < 0) i += n;
                 key = (uint32_t)(base + i);
             } else {
                 set_status(status, DLRM_STATUS_OOB_INDEX);
             }
-            keys[p] = key;
-            vals[p] = val;
+        } else if (i >= 0 && i < n) {
+            key = (uint32_t)(base + i);
+        } else {
+            set_status(status, DLRM_STATUS_OOB_INDEX);
+        }
+        keys[p] = key;
+        vals[p] = val;
+        // Zipf-skewed keys repeat digits: one shared atomic per distinct digit per warp
+        const uint32_t d = key & mask;
+        const uint32_t peers = __match_any_sync(__activemask(), d);
+        if ((peers & ((1u << lane) - 1u)) == 0) atomicAdd(&h[d], (uint32_t)__popc(peers));
+    };
+
+    if constexpr (G == 1) {
+        for (int64_t gb = g0 + threadIdx.x; gb < g1; gb += (int64_t)kKeyBags * kSortThreads) {
+            int64_t s[kKeyBags], e[kKeyBags];
+            int32_t first[kKeyBags];
+#pragma unroll
+            for (int u = 0; u < kKeyBags; ++u) {
+                const int64_t g = gb + (int64_t)u * kSortThreads;
+                s[u] = e[u] = 0;
+                if (g < g1) {
+                    s[u] = ldg_early_s32(offsets + g);
+                    e[u] = ldg_early_s32(offsets + g + 1);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kKeyBags; ++u) {
+                bounds(s[u], e[u]);
+                first[u] = e[u] > s[u] ? ldg_early_s32(indices + s[u]) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kKeyBags; ++u) {
+                const int64_t g = gb + (int64_t)u * kSortThreads;
+                if (g < g1 && e[u] > s[u]) {
+                    const int t = (int)((uint32_t)g / (uint32_t)B);   // F * B < 2^31
+                    const int b = (int)g - t * B;
+                    const int64_t base = row_base[t], n = row_base[t + 1] - base;
+                    const uint32_t val = (uint32_t)((int64_t)b * F + t);
+                    emit(s[u], first[u], base, n, val);
+                    for (int64_t p = s[u] + 1; p < e[u]; ++p) emit(p, indices[p], base, n, val);
+                }
+            }
+        }
+    } else {
+        for (int64_t g = g0 + threadIdx.x / kWarp; g < g1; g += kSortThreads / kWarp) {
+            const int t = (int)((uint32_t)g / (uint32_t)B);
+            const int b = (int)g - t * B;
+            const int64_t base = row_base[t], n = row_base[t + 1] - base;
+            const uint32_t val = (uint32_t)((int64_t)b * F + t);
+            int64_t s = offsets[g], e = offsets[g + 1];
+            bounds(s, e);
+            for (int64_t p = s + lane; p < e; p += kWarp) emit(p, indices[p], base, n, val);
         }
     }
+    __syncthreads();
+    hist[(int64_t)threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
 }
 
 // ------------------------------------------------------- block scan helper
@@ -211,11 +307,15 @@ radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ t
     if (threadIdx.x == 0) totals[blockIdx.x] = carry;
 }
 
+// One block per tile.  The first pass's tile b is the key kernel's block b:
+// positions offsets[b * bpb] .. offsets[(b + 1) * bpb] (clamped), taken in
+// sub-tiles of kTile keys, each digit's output offset advancing by the
+// sub-tile's count; later passes' tiles are fixed ranges of kTile positions.
 __global__ void __launch_bounds__(kSortThreads)
 radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
                 uint32_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out, int64_t n, int shift,
                 uint32_t mask, const uint32_t* __restrict__ hist, const uint32_t* __restrict__ totals,
-                int64_t ntiles)
+                int64_t ntiles, const int32_t* __restrict__ offsets, int64_t bpb, int64_t nbags)
 {
     pdl_wait_and_release();
     constexpr int kW = kSortThreads / kWarp;
@@ -224,72 +324,86 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
     __shared__ uint32_t warp_sums[kW];
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const uint32_t lt = (1u << lane) - 1u;
+    int64_t lo, hi;
+    if (offsets) {
+        const int64_t g0 = (int64_t)blockIdx.x * bpb;
+        const int64_t g1 = g0 + bpb < nbags ? g0 + bpb : nbags;
+        auto clampp = [&](int64_t x) { return x < 0 ? 0 : (x > n ? n : x); };
+        lo = g0 < nbags ? clampp(offsets[g0]) : n;
+        hi = g0 < nbags ? clampp(offsets[g1]) : n;
+        if (hi < lo) hi = lo;
+    } else {
+        lo = (int64_t)blockIdx.x * kTile;
+        hi = lo + kTile < n ? lo + kTile : n;
+    }
 
     // global start of each digit in this tile
     const uint32_t ex = block_excl_scan(totals[threadIdx.x], warp_sums, nullptr);
     dbase[threadIdx.x] = ex + hist[(int64_t)threadIdx.x * ntiles + blockIdx.x];
+    for (int64_t sub = lo; sub < hi; sub += kTile) {
 #pragma unroll
-    for (int w = 0; w < kW; ++w) wcnt[w][threadIdx.x] = 0;
-    __syncthreads();
+        for (int w = 0; w < kW; ++w) wcnt[w][threadIdx.x] = 0;
+        __syncthreads();
 
-    uint32_t key[kItems], val[kItems], local[kItems];
-    const int64_t wbase = (int64_t)blockIdx.x * kTile + (int64_t)warp * kWarp * kItems;
+        uint32_t key[kItems], val[kItems], local[kItems];
+        const int64_t wbase = sub + (int64_t)warp * kWarp * kItems;
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        const int64_t p = wbase + r * kWarp + lane;
-        const bool valid = p < n;
-        key[r] = valid ? keys_in[p] : 0;
-        val[r] = valid ? vals_in[p] : 0;
-        const uint32_t d = (key[r] >> shift) & mask;
-        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 0x100u);
-        const uint32_t prior = valid ? wcnt[warp][d] : 0;
-        __syncwarp();
-        if (valid && (peers & lt) == 0) wcnt[warp][d] = prior + __popc(peers);
-        __syncwarp();
-        local[r] = prior + __popc(peers & lt);
-    }
-    __syncthreads();
-    {   // exclusive scan over warps, per digit
-        uint32_t s = 0;
-#pragma unroll
-        for (int w = 0; w < kW; ++w) {
-            const uint32_t c = wcnt[w][threadIdx.x];
-            wcnt[w][threadIdx.x] = s;
-            s += c;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        const int64_t p = wbase + r * kWarp + lane;
-        if (p < n) {
+        for (int r = 0; r < kItems; ++r) {
+            const int64_t p = wbase + r * kWarp + lane;
+            const bool valid = p < hi;
+            key[r] = valid ? keys_in[p] : 0;
+            val[r] = valid ? vals_in[p] : 0;
             const uint32_t d = (key[r] >> shift) & mask;
-            const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
-            if (pos < n) {   // always true for consistent histograms; guards the write
-                keys_out[pos] = key[r];
-                vals_out[pos] = val[r];
+            const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 0x100u);
+            const uint32_t prior = valid ? wcnt[warp][d] : 0;
+            __syncwarp();
+            if (valid && (peers & lt) == 0) wcnt[warp][d] = prior + __popc(peers);
+            __syncwarp();
+            local[r] = prior + __popc(peers & lt);
+        }
+        __syncthreads();
+        uint32_t subtotal = 0;   // this sub-tile's count of digit threadIdx.x
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {   // exclusive scan over warps, per digit
+            const uint32_t c = wcnt[w][threadIdx.x];
+            wcnt[w][threadIdx.x] = subtotal;
+            subtotal += c;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int64_t p = wbase + r * kWarp + lane;
+            if (p < hi) {
+                const uint32_t d = (key[r] >> shift) & mask;
+                const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
+                if (pos < n) {   // always true for consistent histograms; guards the write
+                    keys_out[pos] = key[r];
+                    vals_out[pos] = val[r];
+                }
             }
         }
+        __syncthreads();
+        dbase[threadIdx.x] += subtotal;
     }
 }
 
-// ----------------------------------------------------------------- 4. fixup
-constexpr int kLongPieces = 64;   // runs with more chunk pieces are summed by a whole block
-constexpr int kFixRegs = 4;       // float4 partial-sum loads a lane has in flight
 
-// Last chunk touched by the run of key K that starts in chunk c0 and continues
-// past it.  Keys are sorted, so the run touches chunk c iff the first key of c
-// is K, and the chunks it touches are c0..L.  Chunk c0 + 2 is probed first
-// (one broadcast load); past it, one round probes c0 + 2^j for j = 0..31 (so
+// ----------------------------------------------------------------- 4. fixup
+constexpr int kFixRegs = 4;   // float4 partial-sum loads a lane keeps in flight
+
+// Last item touched by the run of key K that starts in item c0 and continues
+// past it.  Keys are sorted, so the run touches item c iff the first key of c
+// is K, and the items it touches are c0..L.  Item c0 + 2 is probed first (one
+// broadcast load); past it, one round probes c0 + 2^j for j = 0..31 (so
 // 2^j <= L - c0 < 2^(j+1) for the last true j), then each round probes 32
-// evenly spaced chunks of the remaining interval.
-__device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ keys, int64_t n, int64_t nchunks,
-                                                  int64_t c0, uint32_t K, int lane)
+// evenly spaced items of the remaining interval.
+__device__ __forceinline__ int64_t run_last_item(const uint32_t* __restrict__ keys, int64_t n, int64_t nitems,
+                                                 int64_t IT, int64_t c0, uint32_t K, int lane)
 {
-    auto touches = [&](int64_t c) { return c < nchunks && c * kChunk < n && keys[c * kChunk] == K; };
-    if (!touches(c0 + 2)) return c0 + 1;      // most runs that cross an edge end in the next chunk
+    auto touches = [&](int64_t c) { return c < nitems && c * IT < n && keys[c * IT] == K; };
+    if (!touches(c0 + 2)) return c0 + 1;      // most runs that cross an edge end in the next item
     const uint32_t m = __ballot_sync(0xffffffffu, touches(c0 + ((int64_t)1 << lane)));
-    const int j = __popc(m) - 1;              // chunk c0 + 1 is touched, so j >= 0
+    const int j = __popc(m) - 1;              // item c0 + 1 is touched, so j >= 0
     int64_t lo = c0 + ((int64_t)1 << j);      // touched
     int64_t hi = c0 + ((int64_t)2 << j);      // not touched (or past the end)
     while (hi - lo > 1) {
@@ -302,161 +416,6 @@ __device__ __forceinline__ int64_t run_last_chunk(const uint32_t* __restrict__ k
         lo = nlo;
     }
     return lo;
-}
-
-// --------------------------------------------------------- 3. segment sums
-// A gradient chunk of four elements as loaded: fp32 as one float4, fp16 as
-// the 8 loaded bytes (half the registers, so twice the loads fit in flight),
-// widened exactly to fp32 where it is added.
-template <typename GT>
-struct GradRaw { using T = float4; };
-template <>
-struct GradRaw<__half> { using T = uint2; };
-
-template <typename GT>
-__device__ __forceinline__ typename GradRaw<GT>::T load_grad_raw(const GT* p)
-{
-    if constexpr (sizeof(GT) == 4) {
-        return u4_as_f4(ldg_nc_v4(p));
-    } else {
-        uint2 r;
-        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-        return r;
-    }
-}
-
-__device__ __forceinline__ float4 widen(float4 v) { return v; }
-__device__ __forceinline__ float4 widen(uint2 r)
-{
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
-    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
-    return make_float4(a.x, a.y, c.x, c.y);
-}
-
-template <int MC, typename GT>
-__global__ void __launch_bounds__(256, MC >= 8 ? 2 : 3)   // rows past 512 elements: registers for 8 float4 sums
-segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
-               const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
-               float* __restrict__ partials, uint64_t* __restrict__ split_list, uint32_t* split_count,
-               uint64_t* __restrict__ long_list, int64_t nchunks, int64_t nbags)
-{
-    pdl_wait_and_release();
-    // positions per batch: their gradient rows, and the table rows of the runs
-    // that end (complete) among them, are all loaded before any is used (at
-    // three blocks per SM and the 64K training shapes, 6 measured best for fp32
-    // gradients; 8 for fp16, 243 against 281 us at 6)
-    constexpr int U0 = sizeof(GT) == 2 && MC <= 2 ? 8 : 6;
-    constexpr int U = MC >= 8 ? 1 : (U0 / MC > 0 ? U0 / MC : 1);
-    const int lane = threadIdx.x % kWarp;
-    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
-    const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
-    const int c4 = D / 4;   // float4 columns per row
-    for (int64_t c = warp_id; c < nchunks; c += nwarps) {
-        const int64_t p0 = c * kChunk;
-        const int64_t p = p0 + lane;
-        const uint32_t key = p < n ? keys[p] : kSkipKey;
-        const uint32_t val = p < n ? vals[p] : 0;
-        uint32_t prev = __shfl_up_sync(0xffffffffu, key, 1);
-        if (lane == 0) prev = p0 > 0 ? keys[p0 - 1] : ~key;
-        const uint32_t after = (p0 + kChunk < n) ? keys[p0 + kChunk] : kSkipKey;
-        uint32_t next = __shfl_down_sync(0xffffffffu, key, 1);
-        if (lane == kWarp - 1) next = after;
-        const bool valid = key != kSkipKey;
-        const uint32_t heads = __ballot_sync(0xffffffffu, valid && prev != key);
-        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-        if (vmask == 0) continue;
-        const int nvalid = 32 - __clz(vmask);             // valid lanes are a prefix
-        const uint32_t starts = heads | 1u;               // lane 0 starts a run piece
-        // pieces: a piece ends where the next position holds another key or
-        // the chunk's valid prefix ends.  A piece that began with a head (its
-        // run starts in this chunk) and whose run does not continue past the
-        // chunk is a whole run: its row is updated here.
-        const bool piece_end = valid && (next != key || lane == nvalid - 1);
-        const int s_me = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));
-        const bool starts_here = (heads >> s_me) & 1u;
-        const bool run_ends = lane < kWarp - 1 || after != key;
-        const uint32_t ends = __ballot_sync(0xffffffffu, piece_end);
-        const uint32_t whole = __ballot_sync(0xffffffffu, piece_end && starts_here && run_ends);
-        const uint32_t complete = __ballot_sync(0xffffffffu, piece_end && starts_here && run_ends &&
-                                                             (int64_t)key < total_rows);
-        float4 acc[MC];
-#pragma unroll
-        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        uint32_t file_key = kSkipKey;   // key of a run that starts here and crosses the chunk's end
-        for (int q0 = 0; q0 < nvalid; q0 += U) {
-            typename GradRaw<GT>::T v[U][MC];
-            float4 w[U][MC];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = q0 + u;
-                const uint32_t row = __shfl_sync(0xffffffffu, val, q & 31);
-                const uint32_t qk = __shfl_sync(0xffffffffu, key, q & 31);
-                const bool done = q < nvalid && ((complete >> (q & 31)) & 1u);
-#pragma unroll
-                for (int m = 0; m < MC; ++m) {
-                    const int col = lane + m * kWarp;
-                    v[u][m] = typename GradRaw<GT>::T{};
-                    w[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    // row < nbags holds for pairs made from well-formed offsets
-                    if (q < nvalid && col < c4 && (int64_t)row < nbags)
-                        v[u][m] = load_grad_raw<GT>(grad + (int64_t)row * D + 4 * col);
-                    if (done && col < c4) w[u][m] = *reinterpret_cast<const float4*>(tables + (int64_t)qk * D + 4 * col);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = q0 + u;
-                if (q >= nvalid) break;
-#pragma unroll
-                for (int m = 0; m < MC; ++m) {
-                    const float4 g = widen(v[u][m]);
-                    acc[m].x += g.x;
-                    acc[m].y += g.y;
-                    acc[m].z += g.z;
-                    acc[m].w += g.w;
-                }
-                if (!((ends >> q) & 1u)) continue;
-                const uint32_t qk = __shfl_sync(0xffffffffu, key, q);
-                if ((complete >> q) & 1u) {
-#pragma unroll
-                    for (int m = 0; m < MC; ++m) {
-                        const int col = lane + m * kWarp;
-                        if (col < c4) {
-                            float4 x = w[u][m];
-                            x.x = fmaf(-lr, acc[m].x, x.x);
-                            x.y = fmaf(-lr, acc[m].y, x.y);
-                            x.z = fmaf(-lr, acc[m].z, x.z);
-                            x.w = fmaf(-lr, acc[m].w, x.w);
-                            *reinterpret_cast<float4*>(tables + (int64_t)qk * D + 4 * col) = x;
-                        }
-                    }
-                } else if (!((whole >> q) & 1u)) {
-                    // a piece of a run that crosses a chunk edge: its partial sum
-                    // (a whole run whose key is out of range cannot be made above)
-                    const bool piece_starts_here = __shfl_sync(0xffffffffu, starts_here, q);
-                    const int64_t slot = 2 * c + (piece_starts_here ? 1 : 0);
-#pragma unroll
-                    for (int m = 0; m < MC; ++m) {
-                        const int col = lane + m * kWarp;
-                        if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
-                    }
-                    if (piece_starts_here) file_key = qk;   // filed after the chunk (at most one per chunk)
-                }
-#pragma unroll
-                for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        if (file_key != kSkipKey) {   // this chunk files the run it starts, with its number of pieces
-            const int64_t pieces = run_last_chunk(keys, n, nchunks, c, file_key, lane) - c + 1;
-            if (lane == 0) {
-                const uint64_t e = (uint64_t)c << 32 | (uint64_t)pieces;
-                if (pieces > kLongPieces)
-                    long_list[atomicAdd(split_count + 1, 1u)] = e;
-                else
-                    split_list[atomicAdd(split_count, 1u)] = e;
-            }
-        }
-    }
 }
 
 template <int MC>
@@ -478,11 +437,11 @@ __device__ __forceinline__ void apply_sgd(float* __restrict__ tables, int64_t ro
     }
 }
 
-// Slot of piece j of the run that starts in chunk c0 (the first piece is the
-// starting chunk's "continues" slot, the others are chunk-start slots).
+// Slot of piece j of the run that starts in item c0 (the first piece is the
+// starting item's trailing slot, the others are the later items' leading slots).
 __device__ __forceinline__ int64_t piece_slot(int64_t c0, int64_t j) { return j == 0 ? 2 * c0 + 1 : 2 * (c0 + j); }
 
-// Pieces [j0, j1) of the run starting in chunk c0, added in order into acc.
+// Pieces [j0, j1) of the run starting in item c0, added in order into acc.
 template <int MC>
 __device__ __forceinline__ void add_pieces(const float* __restrict__ partials, int64_t c0, int64_t j0, int64_t j1,
                                            int D, int lane, float4 (&acc)[MC])
@@ -514,7 +473,7 @@ __device__ __forceinline__ void add_pieces(const float* __restrict__ partials, i
     }
 }
 
-// Runs that cross chunk edges.  Block i < (long runs) takes long run i: warp w
+// Runs that cross item edges.  Block i < (long runs) takes long run i: warp w
 // adds the w-th of kW contiguous slices of its pieces, then warp 0 adds the
 // kW slice sums in slice order and updates the row.  Then every warp takes
 // short runs (pieces in order, one warp per run).
@@ -522,18 +481,19 @@ template <int MC>
 __global__ void __launch_bounds__(kFixThreads)
 fixup_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ partials,
              const uint64_t* __restrict__ split_list, const uint64_t* __restrict__ long_list,
-             const uint32_t* __restrict__ counts, int D, float* __restrict__ tables, int64_t total_rows, float lr)
+             const uint32_t* __restrict__ counters, int64_t IT, int D, float* __restrict__ tables,
+             int64_t total_rows, float lr)
 {
     pdl_wait_and_release();
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const int c4 = D / 4;
-    const uint32_t nshort = counts[0], nlong = counts[1];
+    const uint32_t nshort = counters[kCtrSplit], nlong = counters[kCtrLong];
     for (uint32_t i = blockIdx.x; i < nlong; i += gridDim.x) {
         const uint64_t e = long_list[i];
         const int64_t c0 = (int64_t)(e >> 32), pieces = (int64_t)(e & 0xffffffffu);
-        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
+        const uint32_t K = keys[c0 * IT + IT - 1];
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -569,7 +529,7 @@ fixup_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ partia
     for (int64_t i = gw; i < nshort; i += nw) {
         const uint64_t e = split_list[i];
         const int64_t c0 = (int64_t)(e >> 32), pieces = (int64_t)(e & 0xffffffffu);
-        const uint32_t K = keys[c0 * kChunk + kChunk - 1];
+        const uint32_t K = keys[c0 * IT + IT - 1];
         float4 acc[MC];
 #pragma unroll
         for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -578,43 +538,258 @@ fixup_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ partia
     }
 }
 
-int key_bits(int64_t total_rows)
+// --------------------------------------------------------- 3. segment sums
+__device__ __forceinline__ void add4(float4& a, const float4& b)
 {
-    int b = 0;
-    while (b < 32 && ((uint64_t)1 << b) <= (uint64_t)total_rows) ++b;   // 2^b > total_rows
-    return b;
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+// A gradient chunk of four elements as loaded: fp32 as one float4, fp16 as
+// the 8 loaded bytes (half the registers), widened exactly to fp32 where it
+// is added.
+template <typename GT>
+struct GradRaw { using T = float4; };
+template <>
+struct GradRaw<__half> { using T = uint2; };
+
+template <typename GT>
+__device__ __forceinline__ typename GradRaw<GT>::T load_grad_raw(const GT* p)
+{
+    if constexpr (sizeof(GT) == 4) {
+        return u4_as_f4(ldg_nc_v4(p));
+    } else {
+        uint2 r;
+        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+        return r;
+    }
+}
+
+__device__ __forceinline__ float4 widen(float4 v) { return v; }
+__device__ __forceinline__ float4 widen(uint2 r)
+{
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+    return make_float4(a.x, a.y, c.x, c.y);
+}
+
+// Positions per batch: their gradient rows, and the table rows of the runs
+// that complete among them, are all loaded before any is added.
+template <int MC, typename GT>
+constexpr int seg_batch()
+{
+    return MC >= 8 ? 1 : (sizeof(GT) == 2 ? 8 : 6) / MC > 0 ? (sizeof(GT) == 2 ? 8 : 6) / MC : 1;
+}
+
+// Warps are independent: each takes items of IT = 32 * kSubs positions from a
+// counter and walks their 32-position sub-chunks (lane q holds position q's
+// key and gradient row number; the next sub-chunk's are loaded meanwhile).
+// Rows are added column-wise: lane l holds four-element columns l, l + 32, ...
+template <int MC, typename GT>
+__global__ void __launch_bounds__(256, MC >= 2 ? 2 : 3)
+segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
+               const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
+               float* __restrict__ partials, uint64_t* __restrict__ split_list, uint64_t* __restrict__ long_list,
+               uint32_t* __restrict__ counters, int64_t nitems, int64_t nbags)
+{
+    constexpr int U = seg_batch<MC, GT>();
+    constexpr int64_t IT = (int64_t)kWarp * kSubs;
+    const int lane = threadIdx.x % kWarp;
+    const int c4 = D / 4;
+    pdl_wait_and_release();
+
+    auto fetch_item = [&]() -> int64_t {
+        uint32_t v = 0;
+        if (lane == 0) v = atomicAdd(&counters[kCtrItem], 1u);
+        return (int64_t)__shfl_sync(0xffffffffu, v, 0);
+    };
+    auto load_sub = [&](int64_t item, int j, uint32_t& k, uint32_t& v) {
+        const int64_t p = item * IT + (int64_t)j * kWarp + lane;
+        k = kSkipKey;
+        v = 0;
+        if (item < nitems && p < n) {
+            k = ldg_early_u32(keys + p);
+            v = ldg_early_u32(vals + p);
+        }
+    };
+    auto load_edges = [&](int64_t item, uint32_t& before, uint32_t& after) {
+        before = after = kSkipKey;
+        if (item < nitems) {
+            if (item > 0) before = ldg_early_u32(keys + item * IT - 1);
+            if ((item + 1) * IT < n) after = ldg_early_u32(keys + (item + 1) * IT);
+        }
+    };
+
+    int64_t item = fetch_item();
+    int64_t pending = item < nitems ? fetch_item() : nitems;
+    uint32_t k_cur, v_cur, before, after;
+    load_sub(item, 0, k_cur, v_cur);
+    load_edges(item, before, after);
+    while (item < nitems) {
+        float4 acc[MC];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool cs = false;            // the run continuing into this sub-chunk began inside the item
+        uint32_t last_key = before;
+        uint32_t k_nxt = kSkipKey, v_nxt = 0, before_nxt = kSkipKey, after_nxt = kSkipKey;
+        for (int j = 0; j < kSubs; ++j) {
+            // next sub-chunk (or the next item's first) in flight while this one is summed
+            if (j + 1 < kSubs) {
+                load_sub(item, j + 1, k_nxt, v_nxt);
+            } else {
+                load_sub(pending, 0, k_nxt, v_nxt);
+                load_edges(pending, before_nxt, after_nxt);
+            }
+            const int64_t p = item * IT + (int64_t)j * kWarp + lane;
+            const uint32_t k = k_cur;
+            const bool valid = p < n && k != kSkipKey;
+            const bool loaded = valid && (int64_t)v_cur < nbags;
+            uint32_t prev = __shfl_up_sync(0xffffffffu, k, 1);
+            if (lane == 0) prev = last_key;
+            uint32_t next = __shfl_down_sync(0xffffffffu, k, 1);
+            const uint32_t first_next = __shfl_sync(0xffffffffu, k_nxt, 0);
+            if (lane == kWarp - 1) next = j + 1 < kSubs ? first_next : after;
+            const bool head = valid && prev != k;
+            const bool endq = valid && next != k;
+            const uint32_t hm = __ballot_sync(0xffffffffu, head);
+            const uint32_t em = __ballot_sync(0xffffffffu, endq);
+            const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+            const uint32_t lm = __ballot_sync(0xffffffffu, loaded);
+            const bool stq = (hm & ((2u << lane) - 1u)) != 0 || cs;   // the run through q began inside the item
+            const uint32_t cm = __ballot_sync(0xffffffffu, endq && stq && (int64_t)k < total_rows);
+            const uint32_t leadm = __ballot_sync(0xffffffffu, endq && !stq);
+            const int qmax = vm ? 32 - __clz(vm) : 0;
+            for (int q0 = 0; q0 < qmax; q0 += U) {
+                typename GradRaw<GT>::T g[U][MC];
+                float4 w[U][MC];
+                const uint32_t bl = (lm >> q0) & ((1u << U) - 1u);
+                const uint32_t bc = (cm >> q0) & ((1u << U) - 1u);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const GT* src = grad + (int64_t)__shfl_sync(0xffffffffu, v_cur, (q0 + u) & 31) * D;
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        const int col = lane + m * kWarp;
+                        g[u][m] = typename GradRaw<GT>::T{};
+                        if (((bl >> u) & 1u) && col < c4) g[u][m] = load_grad_raw<GT>(src + 4 * col);
+                    }
+                }
+                if (bc) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const float* trow = tables + (int64_t)__shfl_sync(0xffffffffu, k, (q0 + u) & 31) * D;
+#pragma unroll
+                        for (int m = 0; m < MC; ++m) {
+                            const int col = lane + m * kWarp;
+                            w[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (((bc >> u) & 1u) && col < c4) w[u][m] = ldg_row_early(trow + 4 * col);
+                        }
+                    }
+                }
+                const uint32_t be = (em >> q0) & ((1u << U) - 1u);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) add4(acc[m], widen(g[u][m]));
+                    if ((be >> u) & 1u) {   // a run piece ends at q0 + u
+                        const int q = q0 + u;
+                        if ((bc >> u) & 1u) {   // complete run: w = fmaf(-lr, g, w)
+                            const uint32_t kk = __shfl_sync(0xffffffffu, k, q);
+#pragma unroll
+                            for (int m = 0; m < MC; ++m) {
+                                const int col = lane + m * kWarp;
+                                if (col < c4) {
+                                    float4 x = w[u][m];
+                                    x.x = fmaf(-lr, acc[m].x, x.x);
+                                    x.y = fmaf(-lr, acc[m].y, x.y);
+                                    x.z = fmaf(-lr, acc[m].z, x.z);
+                                    x.w = fmaf(-lr, acc[m].w, x.w);
+                                    *reinterpret_cast<float4*>(tables + (int64_t)kk * D + 4 * col) = x;
+                                }
+                            }
+                        } else if ((leadm >> q) & 1u) {   // leading piece of a run that began in an earlier item
+#pragma unroll
+                            for (int m = 0; m < MC; ++m) {
+                                const int col = lane + m * kWarp;
+                                if (col < c4) reinterpret_cast<float4*>(partials + 2 * item * D)[col] = acc[m];
+                            }
+                        }
+#pragma unroll
+                        for (int m = 0; m < MC; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            }
+            // the run through the last valid position continues past this sub-chunk
+            const int lastq = qmax - 1;
+            const bool cont = vm != 0 && !((em >> lastq) & 1u);
+            const bool st_last = __shfl_sync(0xffffffffu, stq, lastq < 0 ? 0 : lastq);
+            if (cont) {
+                cs = st_last;
+                if (j == kSubs - 1) {   // it continues past the item: a trailing or middle piece
+                    const int64_t slot = st_last ? 2 * item + 1 : 2 * item;
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        const int col = lane + m * kWarp;
+                        if (col < c4) reinterpret_cast<float4*>(partials + slot * D)[col] = acc[m];
+                    }
+                    if (st_last) {   // the run begins in this item: file it with its number of pieces
+                        const uint32_t K = __shfl_sync(0xffffffffu, k, lastq);
+                        const int64_t pieces = run_last_item(keys, n, nitems, IT, item, K, lane) - item + 1;
+                        if (lane == 0) {
+                            const uint64_t e = (uint64_t)item << 32 | (uint64_t)pieces;
+                            if (pieces > kLongPieces)
+                                long_list[atomicAdd(&counters[kCtrLong], 1u)] = e;
+                            else
+                                split_list[atomicAdd(&counters[kCtrSplit], 1u)] = e;
+                        }
+                    }
+                }
+            }
+            last_key = __shfl_sync(0xffffffffu, k, kWarp - 1);
+            k_cur = k_nxt;
+            v_cur = v_nxt;
+        }
+        item = pending;
+        pending = item < nitems ? fetch_item() : nitems;
+        before = before_nxt;
+        after = after_nxt;
+    }
 }
 
 template <int MC, typename GT>
-dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables,
-                            int64_t total_rows, float lr, int64_t nbags, cudaStream_t st)
+dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables, int64_t total_rows,
+                            float lr, int64_t nbags, cudaStream_t st)
 {
-    const int64_t nchunks = (nnz + kChunk - 1) / kChunk;
-    int64_t blocks = (nchunks * kWarp + 255) / 256;
+    constexpr int64_t IT = (int64_t)kWarp * kSubs;
+    const int64_t nitems = (nnz + IT - 1) / IT;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segment_kernel<MC, GT>, 256, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
-    const int64_t resident = (int64_t)num_sms() * per_sm;   // one wave of the grid-stride loop
-    if (blocks > resident) blocks = resident;
+    int64_t blocks = (int64_t)num_sms() * per_sm;   // one resident wave; warps take items from a counter
+    const int64_t need = (nitems + 7) / 8;
+    if (blocks > need) blocks = need;
     dlrm_status s = check_launch_pdl(launch_pdl(segment_kernel<MC, GT>, (int)blocks, 256, 0, st,
-                                                (const uint32_t*)w.keys[0], (const uint32_t*)w.vals[0], nnz, grad, D,
-                                                tables, total_rows, lr, w.partials, w.split_list, w.split_count,
-                                                w.long_list, nchunks, nbags),
+                                                (const uint32_t*)w.keys[0], (const uint32_t*)w.vals[0], nnz, grad,
+                                                D, tables, total_rows, lr, w.partials, w.split_list, w.long_list,
+                                                w.counters, nitems, nbags),
                                      "segment_kernel");
     if (s != DLRM_OK) return s;
-    const size_t smem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(fixup_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e;
+    const size_t fsmem = (size_t)(kFixThreads / kWarp) * D * sizeof(float);
+    if (fsmem > 48 * 1024) {
+        e = cudaFuncSetAttribute(fixup_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
         if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd: %s", cudaGetErrorString(e));
     }
     int64_t fblocks = (int64_t)num_sms() * 4;
-    const int64_t fneed = (nchunks * kWarp + kFixThreads - 1) / kFixThreads;   // one warp per chunk at most
+    const int64_t fneed = (nitems * kWarp + kFixThreads - 1) / kFixThreads;   // one warp per item at most
     if (fblocks > fneed) fblocks = fneed;
-    return check_launch_pdl(launch_pdl(fixup_kernel<MC>, (int)fblocks, kFixThreads, smem, st, (const uint32_t*)w.keys[0],
-                                       (const float*)w.partials, (const uint64_t*)w.split_list,
-                                       (const uint64_t*)w.long_list, (const uint32_t*)w.split_count, D, tables,
-                                       total_rows, lr),
+    return check_launch_pdl(launch_pdl(fixup_kernel<MC>, (int)fblocks, kFixThreads, fsmem, st,
+                                       (const uint32_t*)w.keys[0], (const float*)w.partials,
+                                       (const uint64_t*)w.split_list, (const uint64_t*)w.long_list,
+                                       (const uint32_t*)w.counters, IT, D, tables, total_rows, lr),
                             "fixup_kernel");
 }
 
@@ -651,6 +826,8 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: unknown flag bits 0x%x", flags);
     if (D % 4 != 0 || D > 1024)
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: D must be a multiple of 4, at most 1024");
+    if ((flags & DLRM_FLAG_GRAD_F16) && D % 8 != 0)
+        return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: fp16 gradients need D a multiple of 8");
     if (!aligned16(d_tables) || !aligned16(d_grad_pooled))
         return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd: tables and grad_pooled must be 16-byte aligned");
     if (nnz > 0 && (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
@@ -661,7 +838,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     if (nnz == 0 || B == 0) return DLRM_OK;
 
     cudaStream_t st = as_stream(stream);
-    Ws w = carve(d_workspace, nnz, D);
+    const Ws w = carve(d_workspace, nnz, D);
     const int nbits = key_bits(total_rows);
     const int npasses = (nbits + 7) / 8;
     int cur = npasses & 1;   // the last pass lands in buffer 0
@@ -669,31 +846,34 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     const int64_t nbags = (int64_t)F * B;
     const bool multi = nnz > 2 * nbags;
     const bool hash = (flags & DLRM_FLAG_HASH_INDICES) != 0;
+    const int64_t ntiles = w.ntiles;
+    const int64_t bpb = (nbags + ntiles - 1) / ntiles;   // bags per first-pass tile
     {
-        const int G = multi ? 32 : 1;
-        int64_t blocks = (nbags * G + 255) / 256;
-        const int64_t cap = (int64_t)num_sms() * 8;
-        if (blocks > cap) blocks = cap;
+        const uint32_t mask0 = (1u << (nbits < 8 ? nbits : 8)) - 1u;
         const cudaError_t e =
-            multi ? launch_pdl(keys_kernel<32>, (int)blocks, 256, 0, st, d_row_base, F, B, d_indices, d_offsets, hash,
-                               d_status, w.keys[cur], w.vals[cur], nbags, nnz, w.split_count)
-                  : launch_pdl(keys_kernel<1>, (int)blocks, 256, 0, st, d_row_base, F, B, d_indices, d_offsets, hash,
-                               d_status, w.keys[cur], w.vals[cur], nbags, nnz, w.split_count);
+            multi ? launch_pdl(keys_kernel<32>, (int)ntiles, kSortThreads, 0, st, d_row_base, F, B, d_indices,
+                               d_offsets, hash, d_status, w.keys[cur], w.vals[cur], nbags, nnz, bpb, mask0, w.hist,
+                               ntiles, w.counters)
+                  : launch_pdl(keys_kernel<1>, (int)ntiles, kSortThreads, 0, st, d_row_base, F, B, d_indices,
+                               d_offsets, hash, d_status, w.keys[cur], w.vals[cur], nbags, nnz, bpb, mask0, w.hist,
+                               ntiles, w.counters);
         dlrm_status s = check_launch_pdl(e, "keys_kernel");
         if (s != DLRM_OK) return s;
     }
-    const int64_t ntiles = (nnz + kTile - 1) / kTile;
     for (int pass = 0; pass < npasses; ++pass) {
         const int shift = 8 * pass;
         const int bits = nbits - shift < 8 ? nbits - shift : 8;
         const uint32_t mask = (1u << bits) - 1u;
-        cudaError_t e = launch_pdl(radix_upsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur], nnz,
-                                   shift, mask, w.hist, ntiles);
+        cudaError_t e = cudaSuccess;
+        if (pass > 0)   // the first pass's histogram comes from the key kernel
+            e = launch_pdl(radix_upsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur], nnz, shift,
+                           mask, w.hist, ntiles);
         if (e == cudaSuccess) e = launch_pdl(radix_scan, 256, kSortThreads, 0, st, w.hist, ntiles, w.totals);
         if (e == cudaSuccess)
             e = launch_pdl(radix_downsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur],
                            (const uint32_t*)w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], nnz, shift, mask,
-                           (const uint32_t*)w.hist, (const uint32_t*)w.totals, ntiles);
+                           (const uint32_t*)w.hist, (const uint32_t*)w.totals, ntiles,
+                           pass == 0 ? d_offsets : (const int32_t*)nullptr, bpb, nbags);
         dlrm_status s = check_launch_pdl(e, "radix sort pass");
         if (s != DLRM_OK) return s;
         cur ^= 1;

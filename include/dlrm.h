@@ -207,6 +207,33 @@ dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_dense,
                               void* stream);
 
 /*
+ * dlrm_emb_interact_bwd -- dlrm_interact_bwd for a training step that keeps no
+ * pooled tensor: the rows of Z after the dense row are gathered again from the
+ * tables, exactly as dlrm_emb_fwd pools them, inside the backward kernel.
+ * (The same two operations: "DLRM For PyTorch", §Model architecture -- the
+ *  lookup with sum pooling feeds the dot interaction -- and the gradient of
+ *  the interaction as stated for dlrm_interact_bwd.)
+ *
+ *   pooled[b]      = dlrm_emb_fwd(bags of sample b)    (recomputed, not stored)
+ *   grad_dense[b], grad_pooled[b] = dlrm_interact_bwd(grad_out[b], dense[b], pooled[b])
+ *
+ * Results are bit-identical to dlrm_interact_bwd fed the output of dlrm_emb_fwd
+ * on the same tables and bags.  Arguments as in dlrm_emb_fwd (tables, row_base,
+ * indices, offsets, nnz, flags, d_status) and dlrm_interact_bwd (grad_out,
+ * dense, out_cols, grad_dense, grad_pooled).  Requires fp32 tables, D = 128,
+ * F in {8, 26}, out_cols a multiple of 4 up to 1024 and 16-byte aligned tables,
+ * grad_out, dense, grad_dense and grad_pooled; otherwise DLRM_ERR_UNSUPPORTED
+ * (use dlrm_emb_fwd + dlrm_interact_bwd).  Flags: DLRM_FLAG_HASH_INDICES.
+ * Status bits as in dlrm_emb_fwd, plus DLRM_STATUS_TIMEOUT.
+ */
+dlrm_status dlrm_emb_interact_bwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
+                                  int F, int D, int B, const int32_t* d_indices,
+                                  const int32_t* d_offsets, int64_t nnz, const float* d_grad_out,
+                                  const void* d_dense, int out_cols, float* d_grad_dense,
+                                  float* d_grad_pooled, unsigned flags, uint32_t* d_status,
+                                  void* stream);
+
+/*
  * dlrm_interact_bwd_f16 -- the same gradient for the mixed-precision step
  * ("DLRM For PyTorch", §Mixed precision training: fp16 tensors, static loss
  * scaling, so G and the results carry the loss scale), on the tcgen05 tensor
@@ -242,9 +269,12 @@ size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
  *   tables[r] := fmaf(-lr, g_r, tables[r])
  * Rows not touched are left bit-for-bit unchanged; no dense gradient table is
  * formed.  Deterministic: pairs (row, b*F + t) are stably radix-sorted by
- * row, then each row's gradients are summed in ascending position order in
- * fixed chunks of 32 positions whose partial sums are combined in a fixed
- * order.  Skipped indices (see dlrm_emb_fwd) contribute nothing.
+ * row; the sorted pairs are cut into items of 256 positions, each row's
+ * gradients are summed in ascending position order within an item, and the
+ * sums of a row that spans several items are combined in item order (a row
+ * spanning more than 8 items: 16 contiguous slices of its items, each in
+ * order, then the slices in order).  Skipped indices (see dlrm_emb_fwd)
+ * contribute nothing.
  *
  *   d_tables       fp32 [total_rows][D], updated in place, 16-byte aligned
  *   d_row_base     int64 [F+1] with row_base[F] = total_rows
@@ -257,7 +287,7 @@ size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
  *                  skipped indices, which sort last) and the nnz uint32 that
  *                  start at byte offset dlrm_ws_align(4*nnz) are the matching
  *                  grad_pooled row numbers b*F + t.
- * Requires D % 4 == 0.
+ * Requires D % 4 == 0, at most 1024 (a multiple of 8 with DLRM_FLAG_GRAD_F16).
  */
 dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
                              int F, int D, int B, const int32_t* d_indices,

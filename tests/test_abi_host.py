@@ -80,6 +80,28 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), f"{n} declared but not exported"
 
 
+def _exported():
+    """dlrm_* functions the built library exports (its dynamic symbol table)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", libbuild.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    return {parts[-1] for parts in (line.split() for line in out.splitlines())
+            if len(parts) >= 3 and parts[-2] in ("T", "t") and parts[-1].startswith("dlrm_")}
+
+
+def test_every_exported_symbol_is_declared(L):
+    """The other direction: a C caller can reach every dlrm_* function the library exports,
+    because each one has a prototype in include/*.h."""
+    exported = _exported()
+    assert {"dlrm_emb_fwd", "dlrm_emb_interact_bwd", "dlrm_emb_bwd_sgd"} <= exported
+    missing = sorted(exported - _declared())
+    assert not missing, f"exported but declared in no header: {missing}"
+
+
 def _err(L):
     return L.dlrm_last_error().decode()
 

@@ -53,7 +53,15 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_lib):
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     dl = cuda_lib
     dev = torch.device("cuda:0")
-    nnz = 400_000                  # more than the built-in scratch holds at D = 128
+    # the smallest index count whose workspace exceeds the built-in scratch at D = 128 over 10 rows
+    lo, hi = 1, dl.DLRM_MAX_NNZ
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if dl.load().dlrm_emb_bwd_sgd_workspace_size(mid, 128, 10) > dl.DLRM_NOALLOC_SCRATCH_BYTES:
+            hi = mid
+        else:
+            lo = mid + 1
+    nnz = lo
     tab = torch.zeros(10, 128, device=dev)
     idx = torch.zeros(nnz, dtype=torch.int32, device=dev)
     off = torch.tensor([0, nnz], dtype=torch.int32, device=dev)
