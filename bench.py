@@ -37,6 +37,7 @@ ALPHA_TRAIN = 1.2
 ALPHA_FWD = 1.05
 LR = 0.1
 L2_BYTES = 129 * 2**20
+E2E_MIN_STEPS = 30   # pipelined end-to-end steps at least, whatever --steps is
 WORKLOAD = ("dlrm-default 64K training step: 26 single-hot fp32 tables (rows log-uniform 10..4e6), "
             "D=128, Zipf 1.2, 480 interaction columns, SGD lr 0.1")
 
@@ -157,12 +158,120 @@ def cpu_oracle_step(w, samples: np.ndarray) -> float:
     return time.perf_counter() - t0
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for key in ("Model name:", "Vendor ID:"):
+            for line in out.splitlines():
+                if line.strip().startswith(key):
+                    return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+class ThreadedOracleStep:
+    """The training step on the CPU oracle, split over host threads.
+
+    The oracle's C functions run unchanged, each on a disjoint part of the
+    step: the lookup and the sparse SGD once per table (the tables' rows are
+    disjoint, and a table's positions keep their order, so each row's sum is
+    taken in the same order as in one call), the interaction and its backward
+    once per block of samples.  ctypes releases the interpreter lock during
+    each call, so the parts run in parallel.  ``run(threads)`` returns seconds;
+    ``outputs()`` the results (checked against one oracle call by the tests)."""
+
+    def __init__(self, w, samples: np.ndarray):
+        import ctypes
+
+        import oracle
+        from dlrm_embeddings_dot_gb300.inputs import Compact
+        c = Compact(w, samples)
+        self.L = oracle.lib()
+        self.F, self.D, self.B, self.P, self.lr = c.F, c.D, c.B, w.out_cols, float(w.lr)
+        F, D, B = self.F, self.D, self.B
+        self.tables = np.array(c.tables, dtype=np.float32, order="C")
+        self.parts = []
+        for t in range(F):
+            lo, hi = int(c.offsets[t * B]), int(c.offsets[(t + 1) * B])
+            self.parts.append(dict(off=np.ascontiguousarray(np.asarray(c.offsets[t * B:(t + 1) * B + 1]) - lo,
+                                                            dtype=np.int32),
+                                   idx=np.ascontiguousarray(c.indices[lo:hi], dtype=np.int32),
+                                   rb=np.array([0, int(c.row_base[t + 1] - c.row_base[t])], dtype=np.int64),
+                                   r0=int(c.row_base[t]), r1=int(c.row_base[t + 1]),
+                                   pooled=np.zeros((B, 1, D), np.float32), gp=np.zeros((B, 1, D), np.float32),
+                                   status=np.zeros(1, np.uint32)))
+        self.dense = np.ascontiguousarray(c.dense, dtype=np.float32)
+        self.go = np.ascontiguousarray(c.grad_out, dtype=np.float32)
+        self.pooled = np.zeros((B, F, D), np.float32)
+        self.out = np.zeros((B, self.P), np.float32)
+        self.gd = np.zeros((B, D), np.float32)
+        self.gp = np.zeros((B, F, D), np.float32)
+        self.ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+
+    def run(self, threads: int) -> float:
+        from concurrent.futures import ThreadPoolExecutor
+        L, ptr, F, D, B, P = self.L, self.ptr, self.F, self.D, self.B, self.P
+        blocks = [(int(a[0]), int(a[-1]) + 1) for a in np.array_split(np.arange(B), max(1, threads)) if a.size]
+
+        def lookup(t):
+            q = self.parts[t]
+            if q["r1"] > q["r0"]:
+                L.oracle_emb_fwd(ptr(self.tables[q["r0"]:q["r1"]]), 0, ptr(q["rb"]), 1, D, B, ptr(q["idx"]),
+                                 ptr(q["off"]), q["idx"].size, ptr(q["pooled"]), 0, ptr(q["status"]))
+            self.pooled[:, t, :] = q["pooled"][:, 0, :]
+
+        def interact(blk):
+            b0, b1 = blk
+            L.oracle_interact_fwd(ptr(self.dense[b0:b1]), ptr(self.pooled[b0:b1]), 0, F, D, b1 - b0,
+                                  ptr(self.out[b0:b1]), P)
+
+        def backward(blk):
+            b0, b1 = blk
+            L.oracle_interact_bwd(ptr(self.go[b0:b1]), ptr(self.dense[b0:b1]), ptr(self.pooled[b0:b1]), 0, F, D,
+                                  b1 - b0, P, ptr(self.gd[b0:b1]), ptr(self.gp[b0:b1]))
+
+        def sgd(t):
+            q = self.parts[t]
+            q["gp"][:, 0, :] = self.gp[:, t, :]
+            if q["r1"] > q["r0"]:
+                L.oracle_emb_bwd_sgd(ptr(self.tables[q["r0"]:q["r1"]]), ptr(q["rb"]), 1, D, B, ptr(q["idx"]),
+                                     ptr(q["off"]), q["idx"].size, ptr(q["gp"]), self.lr, 0, ptr(q["status"]),
+                                     None, None)
+
+        with ThreadPoolExecutor(max(1, threads)) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(lookup, range(F)))
+            list(ex.map(interact, blocks))
+            list(ex.map(backward, blocks))
+            list(ex.map(sgd, range(F)))
+            return time.perf_counter() - t0
+
+    def outputs(self):
+        return dict(pooled=self.pooled, out=self.out, gd=self.gd, gp=self.gp, tables=self.tables)
+
+
 def cpu_baseline(w, n_samples: int) -> dict:
+    """The oracle on all host cores (threads over tables and sample blocks) and on one core."""
     samples = np.arange(n_samples)
-    dt = cpu_oracle_step(w, samples)
-    return {"value": n_samples / dt, "unit": "samples/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n_samples} of the {w.B} samples of the same batch (tables compacted to the "
-                      f"rows they touch); single-threaded C oracle, double accumulation; {dt:.2f} s"}
+    cores = host_cores()
+    dt1 = cpu_oracle_step(w, samples)
+    dtn = ThreadedOracleStep(w, samples).run(cores)
+    return {"value": round(n_samples / dtn, 1), "unit": "samples/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "one_core": {"value": round(n_samples / dt1, 1), "unit": "samples/s", "cores": 1, "seconds": round(dt1, 3)},
+            "sample": f"first {n_samples} of the {w.B} samples of the same batch (tables compacted to the rows "
+                      f"they touch); the C oracle, double accumulation, on {cores} threads (lookup and sparse SGD "
+                      f"per table, interaction and its backward per block of samples; {dtn:.2f} s) and in one "
+                      f"call on one core ({dt1:.2f} s)"}
 
 
 # ------------------------------------------------------------- GPU benchmark
@@ -177,6 +286,9 @@ def sgd_kernels(total_rows: int) -> int:
 def kernels_per_step(total_rows: int) -> int:
     # the one-pass training forward, interact_bwd, then the sparse SGD's kernels
     return 2 + sgd_kernels(total_rows)
+
+
+N_BATCHES = 4   # pre-generated index batches the timed loops rotate through
 
 
 def run_ours(args) -> None:
@@ -195,77 +307,82 @@ def run_ours(args) -> None:
     stream = torch.cuda.Stream(device=dev)
     B = args.batch
 
-    # ---- inputs (rank-specific seed: each replica trains on its own batch)
+    # ---- inputs (rank-specific seed: each replica trains on its own batches).  Four batches over
+    # the same tables (the popular rows stay the same) rotate through the timed loops.
     w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, seed=rank, train=True)
+    wb = [w] + [inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, seed=rank, train=True, rows=w.rows,
+                                    batch=k) for k in range(1, N_BATCHES)]
     F, D, P = w.F, w.D, w.out_cols
     with torch.cuda.stream(stream):
         tables = torch.empty(w.total_rows, D, dtype=torch.float32, device=dev)
         dl.dlrm_synth_fill_uniform(tables, w.table_seed, 0, stream=stream)
         row_base = torch.from_numpy(w.row_base).to(dev)
-        idx = torch.from_numpy(w.indices).to(dev)
-        off = torch.from_numpy(w.offsets).to(dev)
-        dense = torch.from_numpy(w.dense).to(dev)
-        grad_out = torch.from_numpy(w.grad_out).to(dev)
-        # The same synthetic batch is replayed every step; with one fixed upstream
-        # gradient the hottest rows would grow geometrically over hundreds of
-        # steps.  Alternating its sign keeps the replayed tables bounded (the
-        # arithmetic is the same either way).
-        grad_out_neg = -grad_out
+        # The upstream gradient of a batch alternates its sign from one round of the four batches to
+        # the next: a replayed batch with one fixed gradient would grow its hottest rows geometrically
+        # over hundreds of steps (the arithmetic is the same either way).
+        dbat = [dict(idx=torch.from_numpy(x.indices).to(dev), off=torch.from_numpy(x.offsets).to(dev),
+                     dense=torch.from_numpy(x.dense).to(dev), go=torch.from_numpy(x.grad_out).to(dev))
+                for x in wb]
+        for d in dbat:
+            d["go_neg"] = -d["go"]
         pooled = torch.empty(B, F, D, device=dev)
         out = torch.empty(B, P, device=dev)
         gd = torch.empty(B, D, device=dev)
         gp = torch.empty(B, F, D, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
+        nnz_max = max(x.nnz for x in wb)
+        ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(nnz_max, D, w.total_rows), dtype=torch.uint8,
                          device=dev)
     torch.cuda.synchronize()
     nnz = w.nnz
 
     ev = {k: [] for k in ("emb_interact_fwd", "interact_bwd", "emb_bwd_sgd")}
-
     nstep = [0]
 
     def step(record=False):
-        go_k = grad_out if nstep[0] % 2 == 0 else grad_out_neg
+        k = nstep[0]
         nstep[0] += 1
+        d = dbat[k % N_BATCHES]
+        go_k = d["go"] if (k // N_BATCHES) % 2 == 0 else d["go_neg"]
         marks = []
         if record:
             marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             marks[0].record(stream)
         # lookup + interaction in one pass; the pooled rows are written for the backward
-        dl.dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, idx, off, dense, pooled, out, P, status=status,
-                                       stream=stream)
+        dl.dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, d["idx"], d["off"], d["dense"], pooled, out, P,
+                                       status=status, stream=stream)
         if record:
             marks[1].record(stream)
-        dl.dlrm_interact_bwd(go_k, dense, pooled, F, D, B, P, gd, gp, stream=stream)
+        dl.dlrm_interact_bwd(go_k, d["dense"], pooled, F, D, B, P, gd, gp, stream=stream)
         if record:
             marks[2].record(stream)
-        dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, idx, off, gp, LR, ws, status=status,
+        dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, d["idx"], d["off"], gp, LR, ws, status=status,
                             stream=stream)
         if record:
             marks[3].record(stream)
-            for k, (a, b) in zip(ev, zip(marks[:-1], marks[1:])):
-                ev[k].append((a, b))
+            for name, (a, b) in zip(ev, zip(marks[:-1], marks[1:])):
+                ev[name].append((a, b))
 
     # ---- warm-up
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, N_BATCHES)):
         step()
     torch.cuda.synchronize()
 
     # ---- per-op durations (events on the launching stream), separate from the timed loop
-    for _ in range(max(5, min(args.steps, 50))):
+    for _ in range(max(8, min(args.steps, 48))):
         step(record=True)
     torch.cuda.synchronize()
     op_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
 
     # ---- the same forward as the two separate calls (context for the one-pass forward)
     two = []
-    for _ in range(max(5, min(args.steps, 50))):
+    for i in range(max(8, min(args.steps, 48))):
+        d = dbat[i % N_BATCHES]
         m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         m[0].record(stream)
-        dl.dlrm_emb_fwd(tables, row_base, F, D, B, idx, off, pooled, status=status, stream=stream)
+        dl.dlrm_emb_fwd(tables, row_base, F, D, B, d["idx"], d["off"], pooled, status=status, stream=stream)
         m[1].record(stream)
-        dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)
+        dl.dlrm_interact_fwd(d["dense"], pooled, F, D, B, out, P, status=status, stream=stream)
         m[2].record(stream)
         two.append(m)
     torch.cuda.synchronize()
@@ -291,30 +408,35 @@ def run_ours(args) -> None:
 
     # ---- forward only, configs' fp16 DLRM-default: Zipf 1.05, tensor-core interaction
     wf = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, seed=rank)
+    wfb = [wf] + [inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, seed=rank, rows=wf.rows, batch=k)
+                  for k in range(1, N_BATCHES)]
     with torch.cuda.stream(stream):
         tab16 = torch.empty(wf.total_rows, D, dtype=torch.float16, device=dev)
         dl.dlrm_synth_fill_uniform(tab16, wf.table_seed, 0, stream=stream)
         rb16 = torch.from_numpy(wf.row_base).to(dev)
-        idx16 = torch.from_numpy(wf.indices).to(dev)
-        off16 = torch.from_numpy(wf.offsets).to(dev)
-        dense16 = torch.from_numpy(wf.dense.astype(np.float16)).to(dev)
+        fbat = [dict(idx=torch.from_numpy(x.indices).to(dev), off=torch.from_numpy(x.offsets).to(dev),
+                     dense=torch.from_numpy(x.dense.astype(np.float16)).to(dev)) for x in wfb]
         pooled16 = torch.empty(B, F, D, dtype=torch.float16, device=dev)
         out16 = torch.empty(B, P, dtype=torch.float16, device=dev)
     torch.cuda.synchronize()
+    fk = [0]
 
     def fstep():
-        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, idx16, off16, pooled16, status=status, stream=stream)
-        dl.dlrm_interact_fwd(dense16, pooled16, F, D, B, out16, P, status=status, stream=stream)
+        d = fbat[fk[0] % N_BATCHES]
+        fk[0] += 1
+        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, d["idx"], d["off"], pooled16, status=status, stream=stream)
+        dl.dlrm_interact_fwd(d["dense"], pooled16, F, D, B, out16, P, status=status, stream=stream)
 
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, N_BATCHES)):
         fstep()
     fev = []
-    for _ in range(max(5, min(args.steps, 50))):
+    for i in range(max(8, min(args.steps, 48))):
+        d = fbat[i % N_BATCHES]
         m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         m[0].record(stream)
-        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, idx16, off16, pooled16, status=status, stream=stream)
+        dl.dlrm_emb_fwd(tab16, rb16, F, D, B, d["idx"], d["off"], pooled16, status=status, stream=stream)
         m[1].record(stream)
-        dl.dlrm_interact_fwd(dense16, pooled16, F, D, B, out16, P, status=status, stream=stream)
+        dl.dlrm_interact_fwd(d["dense"], pooled16, F, D, B, out16, P, status=status, stream=stream)
         m[2].record(stream)
         fev.append(m)
     torch.cuda.synchronize()
@@ -329,12 +451,15 @@ def run_ours(args) -> None:
     f1.record(stream)
     torch.cuda.synchronize()
     fms = reduce_max(f0.elapsed_time(f1), world, dev)
+    uk = [0]
 
     def fused_step():
-        dl.dlrm_emb_interact_fwd(tab16, rb16, F, D, B, idx16, off16, dense16, out16, P, status=status,
+        d = fbat[uk[0] % N_BATCHES]
+        uk[0] += 1
+        dl.dlrm_emb_interact_fwd(tab16, rb16, F, D, B, d["idx"], d["off"], d["dense"], out16, P, status=status,
                                  stream=stream)
 
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, N_BATCHES)):
         fused_step()
     torch.cuda.synchronize()
     barrier(world)
@@ -345,12 +470,12 @@ def run_ours(args) -> None:
     u1.record(stream)
     torch.cuda.synchronize()
     ums = reduce_max(u0.elapsed_time(u1), world, dev)
-    del tab16, pooled16, out16
+    del tab16, pooled16, out16, fbat
 
     # ---- the same training step in mixed precision (the pages' --amp): fp16
     # interaction tensors on tcgen05, fp32 master tables, static loss scale
-    amp_ops = amp_step_ops(dl, w, torch, dev, stream, status, tables)
-    for _ in range(args.warmup):
+    amp_ops = amp_step_ops(dl, wb, torch, dev, stream, status, tables)
+    for _ in range(max(args.warmup, N_BATCHES)):
         for _, fn in amp_ops:
             fn()
     barrier(world)
@@ -373,18 +498,19 @@ def run_ours(args) -> None:
     # step's results are read back on another stream while the next step
     # computes (inputs and outputs double-buffered; the tables are updated in
     # place by every step, so the steps themselves stay in order).
-    h_dense = torch.from_numpy(w.dense).pin_memory()
-    h_idx = torch.from_numpy(w.indices).pin_memory()
-    h_off = torch.from_numpy(w.offsets).pin_memory()
-    h_go = [torch.from_numpy(w.grad_out).pin_memory(), torch.from_numpy(-w.grad_out).pin_memory()]
+    hb = [dict(dense=torch.from_numpy(x.dense).pin_memory(), idx=torch.from_numpy(x.indices).pin_memory(),
+               off=torch.from_numpy(x.offsets).pin_memory(),
+               go=[torch.from_numpy(x.grad_out).pin_memory(), torch.from_numpy(-x.grad_out).pin_memory()])
+          for x in wb]
     h_out = [torch.empty(B, P).pin_memory() for _ in range(2)]
     h_gd = [torch.empty(B, D).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in (h_dense, h_idx, h_off, h_go[0]))
+    h2d = sum(t.numel() * t.element_size() for t in (hb[0]["dense"], hb[0]["idx"], hb[0]["off"], hb[0]["go"][0]))
     d2h = h_out[0].numel() * 4 + h_gd[0].numel() * 4
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        bufs = [dict(dense=torch.empty_like(dense), idx=torch.empty_like(idx), off=torch.empty_like(off),
-                     go=torch.empty_like(grad_out), out=torch.empty_like(out), gd=torch.empty_like(gd))
+        bufs = [dict(dense=torch.empty(B, D, device=dev), idx=torch.empty(nnz_max, dtype=torch.int32, device=dev),
+                     off=torch.empty(F * B + 1, dtype=torch.int32, device=dev), go=torch.empty(B, P, device=dev),
+                     out=torch.empty(B, P, device=dev), gd=torch.empty(B, D, device=dev))
                 for _ in range(2)]
     torch.cuda.synchronize()
 
@@ -394,16 +520,18 @@ def run_ours(args) -> None:
         uploaded = [torch.cuda.Event() for _ in range(2)]
         computed = [torch.cuda.Event() for _ in range(2)]
         read_back = [torch.cuda.Event() for _ in range(2)]
+        nz = [0, 0]
 
         def upload(k):
-            bb = bufs[k % 2]
+            bb, hx = bufs[k % 2], hb[k % N_BATCHES]
             with torch.cuda.stream(up):
                 if k >= 2:
                     up.wait_event(computed[k % 2])     # step k-2 has consumed this input buffer
-                bb["dense"].copy_(h_dense, non_blocking=True)
-                bb["idx"].copy_(h_idx, non_blocking=True)
-                bb["off"].copy_(h_off, non_blocking=True)
-                bb["go"].copy_(h_go[k % 2], non_blocking=True)
+                bb["dense"].copy_(hx["dense"], non_blocking=True)
+                bb["idx"][:hx["idx"].numel()].copy_(hx["idx"], non_blocking=True)
+                bb["off"].copy_(hx["off"], non_blocking=True)
+                bb["go"].copy_(hx["go"][(k // N_BATCHES) % 2], non_blocking=True)
+                nz[k % 2] = hx["idx"].numel()
                 uploaded[k % 2].record(up)
 
         upload(0)
@@ -414,10 +542,11 @@ def run_ours(args) -> None:
             stream.wait_event(uploaded[k % 2])
             if k >= 2:
                 stream.wait_event(read_back[k % 2])    # step k-2's results have left this output buffer
-            dl.dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, bb["idx"], bb["off"], bb["dense"], pooled,
+            idx_k = bb["idx"][:nz[k % 2]]
+            dl.dlrm_emb_interact_fwd_train(tables, row_base, F, D, B, idx_k, bb["off"], bb["dense"], pooled,
                                            bb["out"], P, status=status, stream=stream)
             dl.dlrm_interact_bwd(bb["go"], bb["dense"], pooled, F, D, B, P, bb["gd"], gp, stream=stream)
-            dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, bb["idx"], bb["off"], gp, LR, ws,
+            dl.dlrm_emb_bwd_sgd(tables, row_base, w.total_rows, F, D, B, idx_k, bb["off"], gp, LR, ws,
                                 status=status, stream=stream)
             computed[k % 2].record(stream)
             with torch.cuda.stream(down):
@@ -428,9 +557,9 @@ def run_ours(args) -> None:
         stream.wait_stream(up)
         stream.wait_stream(down)
 
-    e2e_steps(3)
+    e2e_steps(N_BATCHES)
     torch.cuda.synchronize()
-    e_steps = max(3, args.steps // 4)
+    e_steps = max(E2E_MIN_STEPS, args.steps)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -443,20 +572,18 @@ def run_ours(args) -> None:
         if not (torch.equal(h_out[k].view(torch.int32), bufs[k]["out"].cpu().view(torch.int32)) and
                 torch.equal(h_gd[k].view(torch.int32), bufs[k]["gd"].cpu().view(torch.int32))):
             raise RuntimeError("e2e: results read back differ from the device buffers")
+    del bufs, hb
 
     # ---- roofline of the dominant kernel (algorithmic bytes per launch / event time)
     peaks = measured_peaks()
-    unique_rows = None
-    keys = ws[: 4 * nnz].view(torch.int32)
-    k = keys[keys != -1]
-    if k.numel():
-        unique_rows = int(torch.unique_consecutive(k).numel())
+    # touched rows per batch (each step processes one of the rotated batches)
+    unique_rows = statistics.mean(touched_rows(x) for x in wb)
     s = 4  # fp32
     alg = {
         # offsets + index + row read per lookup, pooled row written once; dense read, output written
         "emb_interact_fwd": B * F * (4 + 4 + D * s) + B * F * D * s + B * (D * s + P * s),
         "interact_bwd": B * (P * 4 + D * s + F * D * s + D * 4 + F * D * 4),
-        "emb_bwd_sgd": nnz * (4 + 4 + D * 4) + (unique_rows or 0) * 2 * D * 4,
+        "emb_bwd_sgd": sgd_alg_bytes(nnz, D, unique_rows),
     }
     dom = max(op_ms, key=op_ms.get)
     kernel_names = {"emb_interact_fwd": "emb_interact_regs_kernel", "interact_bwd": "interact_bwd_regs_kernel",
@@ -466,7 +593,8 @@ def run_ours(args) -> None:
             "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": ncu_traffic(dom if dom == "emb_bwd_sgd" else kernel_names[dom]),
-            "algorithmic_bytes_per_launch": alg[dom], "launch_ms": round(op_ms[dom], 4)}
+            "algorithmic_bytes_per_launch": int(alg[dom]), "launch_ms": round(op_ms[dom], 4)}
+    op_frac = {k: round(alg[k] / (v / 1e3) / 1e9 / peaks["hbm_gbs"], 4) for k, v in op_ms.items()}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world,
@@ -475,9 +603,11 @@ def run_ours(args) -> None:
         "data": "synthetic (seeded; Criteo Terabyte not available)",
         "config": {"workload": WORKLOAD, "global_batch": B * world, "per_gpu_batch": B, "tables": F,
                    "embedding_dim": D, "total_rows": w.total_rows, "nnz": nnz, "out_cols": P,
+                   "index_batches": N_BATCHES,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (4.1 GB tables, 0.87 GB pooled/grad tensors per step)"},
         "ops_ms": {k: round(v, 4) for k, v in op_ms.items()},
+        "ops_hbm_frac": op_frac,
         "fwd_two_calls_ms": {k: round(v, 4) for k, v in two_ms.items()},
         "fwd": {"value": round(B * world * args.steps / (fms / 1e3), 1), "unit": "samples/s",
                 "ms_per_step": round(fms / args.steps, 4), "dtype": "f16 storage, f32 accumulate",
@@ -497,7 +627,7 @@ def run_ours(args) -> None:
                                   "to fp16, upstream gradient scaled by the static loss scale 1024, SGD on fp16 "
                                   "gradients with lr/1024"},
         "e2e": {"value": round(B * world * e_steps / (ems / 1e3), 1), "unit": "samples/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                 "pipelining": "next batch uploaded and previous results read back on two copy streams while a "
                               "step computes (double-buffered inputs/outputs)"},
         "gpu_launches": kernels_per_step(w.total_rows) * args.steps,
@@ -506,12 +636,36 @@ def run_ours(args) -> None:
         "device_status": st,
         "finite_output_fraction": round(finite, 6),
     }
+    del tables, dbat, pooled, out, gd, gp, ws
+    torch.cuda.empty_cache()
+    if not args.headline_only:
+        # every other workload of the pages' configurations, each with its own device-timed and
+        # end-to-end figures (rank 0's GPU only: they are context, not the scaled headline)
+        line["configs"] = {}
+        for name in DEFAULT_CONFIGS:
+            line["configs"][name] = measure_config(args, name)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_samples)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def touched_rows(w) -> int:
+    """Distinct global rows a batch's indices touch (the rows the sparse update reads and writes)."""
+    bag = np.repeat(np.arange(w.F * w.B), np.diff(w.offsets.astype(np.int64)))
+    t = bag // w.B
+    n = w.row_base[t + 1] - w.row_base[t]
+    idx = w.indices.astype(np.int64)
+    ok = (idx >= 0) & (idx < n)
+    return int(np.unique(w.row_base[t][ok] + idx[ok]).size)
+
+
+def sgd_alg_bytes(nnz: int, D: int, touched: float, grad_bytes: int = 4) -> float:
+    """Algorithmic bytes of one sparse update: per index its key and value (int32 index and
+    offset read) and its gradient row; per touched row one read and one write of the fp32 row."""
+    return nnz * (4 + 4 + D * grad_bytes) + touched * 2 * D * 4
 
 
 def run_op(args) -> None:
@@ -641,7 +795,54 @@ CONFIGS = {
 }
 
 
-def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> None:
+# the workloads the default run measures besides the headline (which is train-64k)
+DEFAULT_CONFIGS = ["tiny", "tiny-train", "default-fwd", "default-fwd-uniform", "train-64k-amp", "multi-hot",
+                   "multi-hot-uniform", "large-tables", "bottom-mlp"]
+
+
+def _roofline(alg: dict, per: dict, peaks: dict) -> dict:
+    """The op with the largest mean time, its algorithmic bytes over that time against HBM."""
+    dom = max(per, key=per.get)
+    achieved = alg[dom] / (per[dom] / 1e3) / 1e9
+    return {"bound": "hbm", "op": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "bytes": "algorithmic (every lookup counted as a row read: Zipf-hot rows served by L2 count too)"}
+
+
+def _e2e(torch, stream, ops, h2d: list, d2h: list, steps: int, batch: int) -> dict:
+    """The same step through the public API with every per-step input copied up from pinned host
+    memory and every per-step output read back, in stream order (no overlap), inside the timed
+    region.  h2d / d2h: lists of (device tensor, pinned host tensor)."""
+    def once():
+        for dv, hv in h2d:
+            dv.copy_(hv, non_blocking=True)
+        for _, fn in ops:
+            fn()
+        for dv, hv in d2h:
+            hv.copy_(dv, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            once()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            once()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(batch / (ms / 1e3), 1), "unit": "samples/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for _, h in h2d)),
+            "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for _, h in d2h)),
+            "pipelining": "none (copies and kernels in one stream)"}
+
+
+def _pinned(torch, t):
+    return torch.empty(t.shape, dtype=t.dtype).pin_memory()
+
+
+def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> list:
     """The tensor-core bottom MLP alone, then MLP + fused lookup/interaction."""
     B = args.batch
     dims = [13, 512, 256, 128]
@@ -666,7 +867,11 @@ def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> None:
     fused = ("emb_interact_fwd", lambda: dl.dlrm_emb_interact_fwd(tab, rb, w.F, w.D, B, idx, off, dense, out,
                                                                  w.out_cols, status=status, stream=stream))
     per2, ms2 = _time_ops(torch, stream, [mlp, fused], args.steps, args.warmup)
-    print(json.dumps({
+    e2e = _e2e(torch, stream, [mlp, fused],
+               [(xd, torch.from_numpy(x).pin_memory()), (idx, torch.from_numpy(w.indices).pin_memory()),
+                (off, torch.from_numpy(w.offsets).pin_memory())], [(out, _pinned(torch, out))],
+               max(E2E_MIN_STEPS, args.steps), B)
+    return [{
         "config": "bottom-mlp", "workload": CONFIGS["bottom-mlp"], "batch": B, "steps": args.steps,
         "ms_per_step": round(ms, 4), "samples_per_s": round(B / (ms / 1e3), 1),
         "tflops": round(tflops, 1),
@@ -674,141 +879,198 @@ def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> None:
                      "unit": "TFLOP/s", "frac": round(tflops / peak["bf16_tflops"], 4),
                      "peak_note": f"dense bf16 burst ({peak['source']}); fp16 has the same nominal rate"},
         "with_fused_fwd": {"ms_per_step": round(ms2, 4), "samples_per_s": round(B / (ms2 / 1e3), 1),
-                           "ops_ms": {k: round(v, 4) for k, v in per2.items()}},
-        "device_status": int(status.item())}), flush=True)
+                           "ops_ms": {k: round(v, 4) for k, v in per2.items()}, "e2e": e2e},
+        "device_status": int(status.item())}]
 
 
 LOSS_SCALE = 1024.0
 
 
-def amp_step_ops(dl, w, torch, dev, stream, status, tab):
-    """The mixed-precision training step's four calls, on device buffers."""
+def amp_step_ops(dl, wb, torch, dev, stream, status, tab, buffers=None, alternate=True):
+    """The mixed-precision training step's four calls, on device buffers; the calls rotate
+    through the batches of ``wb`` (a workload or a list of workloads over the same tables).
+    ``buffers``, if a dict, receives the first batch's input and output tensors."""
+    wb = wb if isinstance(wb, list) else [wb]
+    w = wb[0]
     F, D, B, P = w.F, w.D, w.B, w.out_cols
-    rb, idx, off = (torch.from_numpy(a).to(dev) for a in (w.row_base, w.indices, w.offsets))
-    dense = torch.from_numpy(w.dense.astype(np.float16)).to(dev)
-    g16 = torch.from_numpy((w.grad_out.astype(np.float64) * LOSS_SCALE).astype(np.float16)).to(dev)
+    rb = torch.from_numpy(w.row_base).to(dev)
+    bat = [dict(idx=torch.from_numpy(x.indices).to(dev), off=torch.from_numpy(x.offsets).to(dev),
+                dense=torch.from_numpy(x.dense.astype(np.float16)).to(dev),
+                g=torch.from_numpy((x.grad_out.astype(np.float64) * LOSS_SCALE).astype(np.float16)).to(dev))
+           for x in wb]
+    for d in bat:
+        d["g_neg"] = -d["g"]
     pooled = torch.empty(B, F, D, dtype=torch.float16, device=dev)
     out = torch.empty(B, P, dtype=torch.float16, device=dev)
     gd = torch.empty(B, D, dtype=torch.float16, device=dev)
     gp = torch.empty(B, F, D, dtype=torch.float16, device=dev)
-    ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8, device=dev)
+    ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(max(x.nnz for x in wb), D, w.total_rows), dtype=torch.uint8,
+                     device=dev)
     lr = float(np.float32(w.lr / LOSS_SCALE))
-    # the replayed batch's upstream gradient alternates its sign (keeps the tables bounded)
-    gs, k = (g16, -g16), [0]
+    if buffers is not None:
+        buffers.update(bat[0], out=out, gd=gd)
+    # step k uses batch k % n; a batch's upstream gradient alternates its sign from one round of the
+    # batches to the next (keeps the replayed tables bounded)
+    k = [0]
+    cur = {}
 
-    def bwd():
-        g = gs[k[0] % 2]
+    def fwd():
+        d = bat[k[0] % len(bat)]
+        cur["d"], cur["g"] = d, d["g"] if not alternate or (k[0] // len(bat)) % 2 == 0 else d["g_neg"]
         k[0] += 1
-        dl.dlrm_interact_bwd_f16(g, dense, pooled, F, D, B, P, gd, gp, status=status, stream=stream)
+        dl.dlrm_emb_fwd(tab, rb, F, D, B, d["idx"], d["off"], pooled, flags=dl.DLRM_FLAG_POOLED_F16, status=status,
+                        stream=stream)
 
     return [
-        ("emb_fwd", lambda: dl.dlrm_emb_fwd(tab, rb, F, D, B, idx, off, pooled, flags=dl.DLRM_FLAG_POOLED_F16,
-                                            status=status, stream=stream)),
-        ("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, B, out, P, status=status, stream=stream)),
-        ("interact_bwd", bwd),
-        ("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, B, idx, off, gp, lr, ws,
-                                                    flags=dl.DLRM_FLAG_GRAD_F16, status=status, stream=stream)),
+        ("emb_fwd", fwd),
+        ("interact_fwd", lambda: dl.dlrm_interact_fwd(cur["d"]["dense"], pooled, F, D, B, out, P, status=status,
+                                                      stream=stream)),
+        ("interact_bwd", lambda: dl.dlrm_interact_bwd_f16(cur["g"], cur["d"]["dense"], pooled, F, D, B, P, gd, gp,
+                                                          status=status, stream=stream)),
+        ("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, B, cur["d"]["idx"],
+                                                    cur["d"]["off"], gp, lr, ws, flags=dl.DLRM_FLAG_GRAD_F16,
+                                                    status=status, stream=stream)),
     ]
 
 
-def run_train_amp(args, dl, inputs, torch, dev, stream, status) -> None:
+def run_train_amp(args, dl, inputs, torch, dev, stream, status) -> list:
     B = args.batch
     w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True)
+    wb = [w] + [inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True, rows=w.rows, batch=k)
+                for k in range(1, N_BATCHES)]
     with torch.cuda.stream(stream):
         tab = torch.empty(w.total_rows, w.D, dtype=torch.float32, device=dev)
         dl.dlrm_synth_fill_uniform(tab, w.table_seed, 0, stream=stream)
     torch.cuda.synchronize()
-    ops = amp_step_ops(dl, w, torch, dev, stream, status, tab)
+    ops = amp_step_ops(dl, wb, torch, dev, stream, status, tab)
     per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
     F, D, P, nnz = w.F, w.D, w.out_cols, w.nnz
+    # end to end on one batch: its indices, offsets, dense rows and scaled gradient up, the
+    # interaction output and the dense gradient back
+    bufs = {}
+    eops = amp_step_ops(dl, [w], torch, dev, stream, status, tab, buffers=bufs, alternate=False)
+    g16 = (w.grad_out.astype(np.float64) * LOSS_SCALE).astype(np.float16)
+    e2e = _e2e(torch, stream, eops,
+               [(bufs["idx"], torch.from_numpy(w.indices).pin_memory()),
+                (bufs["off"], torch.from_numpy(w.offsets).pin_memory()),
+                (bufs["dense"], torch.from_numpy(w.dense.astype(np.float16)).pin_memory()),
+                (bufs["g"], torch.from_numpy(g16).pin_memory())],
+               [(bufs["out"], _pinned(torch, bufs["out"])), (bufs["gd"], _pinned(torch, bufs["gd"]))],
+               max(E2E_MIN_STEPS, args.steps), B)
+    touched = statistics.mean(touched_rows(x) for x in wb)
     alg = {"emb_fwd": nnz * (4 + 4 + D * 4) + B * F * D * 2,
            "interact_fwd": B * (D * 2 + F * D * 2 + P * 2),
            "interact_bwd": B * (P * 2 + D * 2 + F * D * 2 + D * 2 + F * D * 2),
-           "emb_bwd_sgd": nnz * (4 + 4 + D * 2)}
-    print(json.dumps({
+           "emb_bwd_sgd": sgd_alg_bytes(nnz, D, touched, grad_bytes=2)}
+    return [{
         "config": "train-64k-amp", "workload": CONFIGS["train-64k-amp"], "batch": B, "nnz": nnz,
-        "steps": args.steps, "ms_per_step": round(ms, 4), "step_samples_per_s": round(B / (ms / 1e3), 1),
+        "index_batches": N_BATCHES, "steps": args.steps, "ms_per_step": round(ms, 4),
+        "step_samples_per_s": round(B / (ms / 1e3), 1),
         "ops_ms": {k: round(v, 4) for k, v in per.items()},
         "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
-        "device_status": int(status.item())}), flush=True)
+        "roofline": _roofline(alg, per, measured_peaks()), "e2e": e2e,
+        "device_status": int(status.item())}]
 
 
-def run_config(args, name) -> None:
-    """Measure one workload of the pages' configurations and print a JSON line."""
+def measure_config(args, name) -> list:
+    """Measure one workload of the pages' configurations; one result per batch size."""
     import torch
 
     import dlrm_embeddings_dot_gb300 as dl
     from dlrm_embeddings_dot_gb300 import inputs
 
     dl.load()
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     stream = torch.cuda.Stream(device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     if name == "bottom-mlp":
-        run_bottom_mlp(args, dl, inputs, torch, dev, stream, status)
-        return
+        return run_bottom_mlp(args, dl, inputs, torch, dev, stream, status)
     if name == "train-64k-amp":
-        run_train_amp(args, dl, inputs, torch, dev, stream, status)
-        return
+        return run_train_amp(args, dl, inputs, torch, dev, stream, status)
+    peaks = measured_peaks()
 
     def setup(w, tt):
         with torch.cuda.stream(stream):
             tab = torch.empty(w.total_rows, w.D, dtype=tt, device=dev)
             dl.dlrm_synth_fill_uniform(tab, w.table_seed, 0, stream=stream)
-            rb = torch.from_numpy(w.row_base).to(dev)
-            idx = torch.from_numpy(w.indices).to(dev)
-            off = torch.from_numpy(w.offsets).to(dev)
         torch.cuda.synchronize()
-        return tab, rb, idx, off
+        return tab, torch.from_numpy(w.row_base).to(dev)
 
-    batches = [args.batch]
-    if name == "large-tables":
-        batches = [1024, 4096, 16384, 65536, 262144, 1048576]
-    for B in batches:
+    def make(B, batch=0, rows=None):
         if name in ("tiny", "tiny-train"):
-            w = inputs.tiny_slice(seed=0, train=(name == "tiny-train"))
-        elif name in ("default-fwd", "default-fwd-uniform"):
-            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD,
-                                    uniform_indices=name.endswith("-uniform"))
-        elif name == "train-64k":
-            w = inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True)
-        elif name in ("multi-hot", "multi-hot-uniform"):
-            w = inputs.multi_hot(B=B if B != BATCH else 16384, uniform_indices=name.endswith("-uniform"))
-        else:
-            w = inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, rows=inputs.large_tables_rows())
+            return inputs.tiny_slice(seed=batch, train=(name == "tiny-train"))
+        if name in ("default-fwd", "default-fwd-uniform"):
+            return inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, rows=rows, batch=batch,
+                                       uniform_indices=name.endswith("-uniform"))
+        if name == "train-64k":
+            return inputs.dlrm_default(B=B, dtype=inputs.F32, alpha=ALPHA_TRAIN, train=True, rows=rows, batch=batch)
+        if name in ("multi-hot", "multi-hot-uniform"):
+            return inputs.multi_hot(B=16384 if B == BATCH else B, uniform_indices=name.endswith("-uniform"),
+                                    batch=batch)
+        return inputs.dlrm_default(B=B, dtype=inputs.F16, alpha=ALPHA_FWD, rows=inputs.large_tables_rows(),
+                                   batch=batch)
+
+    results = []
+    batches = [args.batch] if name != "large-tables" else [1024, 4096, 16384, 65536, 262144, 1048576]
+    for B in batches:
+        w = make(B)
+        # rotate four index batches over the same tables where they are cheap to draw (up to 4M
+        # indices); the tiny slice draws its other batches with other seeds (its tables are the
+        # same 3 x 1000 rows for every seed)
+        nb = N_BATCHES if w.nnz <= 4_000_000 else 1
+        wb = [w] + [make(B, batch=k, rows=w.rows) for k in range(1, nb)]
         tt = torch.float16 if w.dtype == inputs.F16 else torch.float32
         es = 2 if tt == torch.float16 else 4
         F, D, Bw, P = w.F, w.D, w.B, w.out_cols
-        tab, rb, idx, off = setup(w, tt)
+        tab, rb = setup(w, tt)
+        with torch.cuda.stream(stream):
+            bat = [dict(idx=torch.from_numpy(x.indices).to(dev), off=torch.from_numpy(x.offsets).to(dev),
+                        dense=torch.from_numpy(x.dense.astype(np.float16 if tt == torch.float16 else np.float32))
+                        .to(dev)) for x in wb]
+        torch.cuda.synchronize()
+        cur = {"k": 0, "d": bat[0]}
+
+        def nxt():
+            cur["d"] = bat[cur["k"] % len(bat)]
+            cur["k"] += 1
+
         pooled = torch.empty(Bw, F, D, dtype=tt, device=dev)
-        dense = torch.from_numpy(w.dense.astype(np.float16 if tt == torch.float16 else np.float32)).to(dev)
         out = torch.empty(Bw, P, dtype=tt, device=dev)
-        ops = [("emb_fwd", lambda: dl.dlrm_emb_fwd(tab, rb, F, D, Bw, idx, off, pooled, status=status,
-                                                   stream=stream))]
         multi = name.startswith("multi-hot")
-        if not multi:
-            ops.append(("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, Bw, out, P,
-                                                                     status=status, stream=stream)))
         train = name in ("tiny-train", "train-64k") or multi
+
+        def emb_fwd():
+            nxt()
+            dl.dlrm_emb_fwd(tab, rb, F, D, Bw, cur["d"]["idx"], cur["d"]["off"], pooled, status=status, stream=stream)
+
+        ops = [("emb_fwd", emb_fwd)]
+        if not multi:
+            ops.append(("interact_fwd", lambda: dl.dlrm_interact_fwd(cur["d"]["dense"], pooled, F, D, Bw, out, P,
+                                                                     status=status, stream=stream)))
+        ws = gp = go = gd = None
         if train:
             gp = torch.empty(Bw, F, D, device=dev)
-            ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(w.nnz, D, w.total_rows), dtype=torch.uint8,
-                             device=dev)
+            ws = torch.empty(dl.dlrm_emb_bwd_sgd_workspace_size(max(x.nnz for x in wb), D, w.total_rows),
+                             dtype=torch.uint8, device=dev)
             if multi:
                 gp.normal_(0.0, 1e-2)
             else:
-                go = torch.from_numpy(w.grad_out).to(dev)
+                for d, x in zip(bat, wb):
+                    d["go"] = torch.from_numpy(x.grad_out).to(dev)
                 gd = torch.empty(Bw, D, device=dev)
-                ops.append(("interact_bwd", lambda: dl.dlrm_interact_bwd(go, dense, pooled, F, D, Bw, P, gd, gp,
-                                                                         stream=stream)))
-            ops.append(("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, Bw, idx, off, gp,
-                                                                   w.lr, ws, status=status, stream=stream)))
-        per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
+                ops.append(("interact_bwd", lambda: dl.dlrm_interact_bwd(cur["d"]["go"], cur["d"]["dense"], pooled,
+                                                                         F, D, Bw, P, gd, gp, stream=stream)))
+            ops.append(("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, Bw, cur["d"]["idx"],
+                                                                   cur["d"]["off"], gp, w.lr, ws, status=status,
+                                                                   stream=stream)))
+        per, ms = _time_ops(torch, stream, ops, args.steps, max(args.warmup, len(bat)))
         fused_train = None
         if train and not multi and tt == torch.float32 and F in (8, 26) and D == 128:
-            fops = [("emb_interact_fwd_train",
-                     lambda: dl.dlrm_emb_interact_fwd_train(tab, rb, F, D, Bw, idx, off, dense, pooled, out, P,
-                                                            status=status, stream=stream))] + ops[2:]
+            def fwd_train():
+                nxt()
+                dl.dlrm_emb_interact_fwd_train(tab, rb, F, D, Bw, cur["d"]["idx"], cur["d"]["off"],
+                                               cur["d"]["dense"], pooled, out, P, status=status, stream=stream)
+            fops = [("emb_interact_fwd_train", fwd_train)] + ops[2:]
             fper, fms = _time_ops(torch, stream, fops, args.steps, args.warmup)
             fused_train = {"ms_per_step": round(fms, 4), "step_samples_per_s": round(Bw / (fms / 1e3), 1),
                            "ops_ms": {k: round(v, 4) for k, v in fper.items()}}
@@ -818,63 +1080,100 @@ def run_config(args, name) -> None:
             # than 479, as the one-pass kernel writes whole float4 columns
             P4 = (P + 3) // 4 * 4
             out4 = torch.empty(Bw, P4, dtype=tt, device=dev)
-            two = [ops[0], ("interact_fwd", lambda: dl.dlrm_interact_fwd(dense, pooled, F, D, Bw, out4, P4,
-                                                                         status=status, stream=stream))]
-            one = [("emb_interact_fwd_train",
-                    lambda: dl.dlrm_emb_interact_fwd_train(tab, rb, F, D, Bw, idx, off, dense, pooled, out4, P4,
-                                                           status=status, stream=stream))]
+            two = [ops[0], ("interact_fwd", lambda: dl.dlrm_interact_fwd(cur["d"]["dense"], pooled, F, D, Bw, out4,
+                                                                         P4, status=status, stream=stream))]
+
+            def fwd_train4():
+                nxt()
+                dl.dlrm_emb_interact_fwd_train(tab, rb, F, D, Bw, cur["d"]["idx"], cur["d"]["off"],
+                                               cur["d"]["dense"], pooled, out4, P4, status=status, stream=stream)
             _, two_ms = _time_ops(torch, stream, two, args.steps, args.warmup)
-            _, one_ms = _time_ops(torch, stream, one, args.steps, args.warmup)
+            _, one_ms = _time_ops(torch, stream, [("emb_interact_fwd_train", fwd_train4)], args.steps, args.warmup)
             fused_train = {"fwd_two_calls_ms": round(two_ms, 4), "fwd_train_call_ms": round(one_ms, 4)}
         fused_ms = None
         if tt == torch.float16 and not train:
-            fop = [("emb_interact_fwd", lambda: dl.dlrm_emb_interact_fwd(tab, rb, F, D, Bw, idx, off, dense, out, P,
-                                                                         status=status, stream=stream))]
-            _, fused_ms = _time_ops(torch, stream, fop, args.steps, args.warmup)
+            def fused():
+                nxt()
+                dl.dlrm_emb_interact_fwd(tab, rb, F, D, Bw, cur["d"]["idx"], cur["d"]["off"], cur["d"]["dense"], out,
+                                         P, status=status, stream=stream)
+            _, fused_ms = _time_ops(torch, stream, [("emb_interact_fwd", fused)], args.steps, args.warmup)
         nnz = w.nnz
+        touched = statistics.mean(touched_rows(x) for x in wb) if train else 0
         alg = {"emb_fwd": nnz * (4 + D * es) + Bw * F * (4 + D * es),
                "interact_fwd": Bw * (D * es + F * D * es + P * es),
                "interact_bwd": Bw * (P * 4 + D * es + F * D * es + D * 4 + F * D * 4),
-               "emb_bwd_sgd": nnz * (4 + 4 + D * 4)}
+               "emb_bwd_sgd": sgd_alg_bytes(nnz, D, touched)}
         fwd_ms = per["emb_fwd"] + per.get("interact_fwd", 0.0)
-        line = {"config": name, "workload": CONFIGS[name], "batch": Bw, "nnz": nnz, "steps": args.steps,
-                "ms_per_step": round(ms, 4), "ops_ms": {k: round(v, 4) for k, v in per.items()},
+        # end to end: the step's inputs up from pinned memory, its outputs back (one batch)
+        d0 = bat[0]
+        h2d = [(d0["idx"], torch.from_numpy(wb[0].indices).pin_memory()),
+               (d0["off"], torch.from_numpy(wb[0].offsets).pin_memory())]
+        if not multi:
+            h2d.append((d0["dense"], _pinned(torch, d0["dense"]).copy_(d0["dense"].cpu())))
+        d2h = [(out, _pinned(torch, out))] if not multi else [(pooled, _pinned(torch, pooled))]
+        if train and not multi:
+            h2d.append((d0["go"], torch.from_numpy(wb[0].grad_out).pin_memory()))
+            d2h.append((gd, _pinned(torch, gd)))
+        if multi:
+            h2d.append((gp, _pinned(torch, gp).copy_(gp.cpu())))
+        e_ops = [(n_, f_) for n_, f_ in ops]
+        cur["k"], bat_save = 0, bat
+        bat = [d0]   # the e2e step always computes on the buffers it uploads into
+        e2e = _e2e(torch, stream, e_ops, h2d, d2h, max(E2E_MIN_STEPS, args.steps), Bw)
+        bat = bat_save
+        line = {"config": name, "workload": CONFIGS[name], "batch": Bw, "nnz": nnz, "index_batches": len(wb),
+                "steps": args.steps, "ms_per_step": round(ms, 4), "ops_ms": {k: round(v, 4) for k, v in per.items()},
                 "alg_GBps": {k: round(alg[k] / (v / 1e3) / 1e9, 1) for k, v in per.items()},
                 "fwd_samples_per_s": round(Bw / (fwd_ms / 1e3), 1),
-                "step_samples_per_s": round(Bw / (ms / 1e3), 1), "device_status": int(status.item())}
+                "step_samples_per_s": round(Bw / (ms / 1e3), 1),
+                "roofline": _roofline(alg, per, peaks), "e2e": e2e, "device_status": int(status.item())}
+        if train:
+            line["touched_rows"] = round(touched, 1)
         if fused_train is not None:
             line["one_pass_forward"] = fused_train
         if fused_ms is not None:
             line["fused_fwd"] = {"ms": round(fused_ms, 4), "samples_per_s": round(Bw / (fused_ms / 1e3), 1),
                                  "alg_GBps": round(Bw * (F * (8 + D * 2) + D * 2 + P * 2) / (fused_ms / 1e3) / 1e9,
                                                    1)}
-        print(json.dumps(line), flush=True)
-        del tab, pooled, out, dense
+        results.append(line)
+        del tab, pooled, out, bat, wb, ws, gp, gd
         torch.cuda.empty_cache()
+    return results
+
+
+def run_config(args, name) -> None:
+    for line in measure_config(args, name):
+        print(json.dumps(line), flush=True)
 
 
 def run_reference(args) -> None:
-    """The CPU oracle, timed as it stands, on bounded samples of the same workload."""
+    """The CPU oracle, timed as it stands on all host cores, on bounded samples of the workload:
+    step k runs the oracle on samples [k*n, (k+1)*n) (wrapping) of the 65,536-sample batch."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from dlrm_embeddings_dot_gb300 import inputs
     w = inputs.dlrm_default(B=BATCH, dtype=inputs.F32, alpha=ALPHA_TRAIN, seed=0, train=True)
     n = args.ref_samples
+    cores = host_cores()
+    steps = [ThreadedOracleStep(w, np.arange(n) + (i * n) % (w.B - n)) for i in range(args.warmup + args.steps)]
     for i in range(args.warmup):
-        cpu_oracle_step(w, np.arange(n) + (i * n) % (w.B - n))
+        steps[i].run(cores)
     total = 0.0
     for i in range(args.steps):
-        total += cpu_oracle_step(w, np.arange(n) + ((i + args.warmup) * n) % (w.B - n))
+        total += steps[args.warmup + i].run(cores)
     value = n * args.steps / total
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "samples/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * total / args.steps * (BATCH / n), 2), "higher_is_better": True,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": BATCH, "per_gpu_batch": BATCH},
-        "cpu_baseline": {"value": round(value, 1), "unit": "samples/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} samples of the 65,536-sample batch per step"},
+        "config": {"workload": WORKLOAD, "global_batch": BATCH, "per_gpu_batch": BATCH,
+                   "samples_per_step": n},
+        "cpu_baseline": {"value": round(value, 1), "unit": "samples/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
+                         "sample": f"{n} samples of the 65,536-sample batch per step (ms_per_step is the time of "
+                                   f"that slice, not of the whole batch); the C oracle on {cores} threads"},
         "e2e": {"value": round(value, 1), "unit": "samples/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -889,9 +1188,11 @@ def main(argv=None) -> None:
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--cpu-samples", type=int, default=32768,
                     help="samples of the batch the CPU-oracle baseline runs on (about 10 s of CPU)")
-    ap.add_argument("--ref-samples", type=int, default=512,
+    ap.add_argument("--ref-samples", type=int, default=4096,
                     help="samples per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="the headline line without the other workloads' measurements")
     ap.add_argument("--config", choices=sorted(CONFIGS), action="append",
                     help="measure one of the pages' workloads instead of the headline step (repeatable)")
     ap.add_argument("--op", choices=["emb_fwd", "emb_fwd16", "interact_fwd", "interact_fwd16", "interact_bwd",

@@ -30,6 +30,8 @@
 //   keysA | valsA | keysB | valsB | hist[256][ntiles] | totals[256] | counters |
 //   partials[2 * nitems][D] | split_list[nitems] | long_list[nitems]
 // The sort ends in keysA/valsA, which the caller may read after the call.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -907,26 +909,62 @@ constexpr size_t kStaticScratchBytes = DLRM_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_sgd_scratch[kStaticScratchBytes];
 
+// Identity of the calling thread's current CUDA context (0 if there is none
+// or the driver cannot say): cuCtxGetId numbers every context the process
+// creates, so a context made after a device reset gets a new number.  The two
+// driver calls are looked up through the runtime, so the library does not link
+// the driver library directly.
+unsigned long long current_context_id()
+{
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 // Device address of g_sgd_scratch for the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is queried once
-// per device (with that device current) and cached.
+// array's name is only a host-side stand-in, so the address is queried with
+// the device current (once per device and context) and cached.
 dlrm_status static_scratch(void** out)
 {
+    struct Entry {
+        unsigned long long ctx;
+        void* ptr;
+    };
     static std::mutex mu;
-    static void* cache[64] = {nullptr};
+    static Entry cache[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd_noalloc: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(DLRM_ERR_UNSUPPORTED, "dlrm_emb_bwd_sgd_noalloc: device %d", dev);
     std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!cache[dev].ptr || ctx == 0 || cache[dev].ctx != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_sgd_scratch);
         if (e != cudaSuccess || !p)
             return fail(DLRM_ERR_CUDA, "dlrm_emb_bwd_sgd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        cache[dev] = p;
+        cache[dev].ptr = p;
+        cache[dev].ctx = current_context_id();   // the lookup made the device's primary context current if needed
     }
-    *out = cache[dev];
+    *out = cache[dev].ptr;
     return DLRM_OK;
 }
 
@@ -936,7 +974,7 @@ dlrm_status static_scratch(void** out)
 extern "C" dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
                                                 int F, int D, int B, const int32_t* d_indices,
                                                 const int32_t* d_offsets, int64_t nnz,
-                                                const float* d_grad_pooled, float lr, unsigned flags,
+                                                const void* d_grad_pooled, float lr, unsigned flags,
                                                 uint32_t* d_status, void* stream)
 {
     clear_error();

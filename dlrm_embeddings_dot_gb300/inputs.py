@@ -150,6 +150,18 @@ class BoundedZipf:
         return out
 
 
+def zipf_map(rng: np.random.Generator, n_rows: int, alpha: float, size: int) -> tuple[int, int]:
+    """The (a, c) of the rank -> row map zipf_rows(rng, n_rows, alpha, size) uses."""
+    BoundedZipf(n_rows, alpha).sample(rng, size)
+    if n_rows == 1:
+        return 1, 0
+    while True:
+        a = int(rng.integers(1, n_rows))
+        if math.gcd(a, n_rows) == 1:
+            break
+    return a, int(rng.integers(0, n_rows))
+
+
 def zipf_rows(rng: np.random.Generator, n_rows: int, alpha: float, size: int) -> np.ndarray:
     """Zipf ranks mapped to rows by ``row = (a*(k-1) + c) mod n``, gcd(a, n) = 1."""
     k = BoundedZipf(n_rows, alpha).sample(rng, size)
@@ -225,8 +237,8 @@ class Workload:
         return table_rows(self.table_seed, np.arange(self.total_rows), self.D, self.dtype)
 
 
-def _streams(seed: int, n: int) -> list[np.random.Generator]:
-    return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+def _streams(entropy, n: int) -> list[np.random.Generator]:
+    return [np.random.default_rng(s) for s in np.random.SeedSequence(entropy).spawn(n)]
 
 
 def log_uniform_rows(rng: np.random.Generator, F: int, lo: float, hi: float) -> np.ndarray:
@@ -247,8 +259,11 @@ def make_workload(name: str, B: int, F: int, D: int, dtype: int, rows: np.ndarra
                   alpha: float, dense: np.ndarray, out_cols: int, seed: int,
                   pool: tuple[int, int] = (1, 1), uniform_indices: bool = False,
                   with_grad: bool = False, grad_sigma: float = 1e-2, lr: float = 0.1,
-                  table_seed: int | None = None) -> Workload:
-    r_idx, r_pool, r_grad = _streams(seed + 1000, 3)
+                  table_seed: int | None = None, batch: int = 0) -> Workload:
+    """``batch`` > 0 draws another batch over the same tables: new pooling
+    factors, ranks (or uniform rows) and upstream gradient, with each table's
+    Zipf rank -> row map unchanged, so the popular rows stay the same."""
+    r_idx, r_pool, r_grad = _streams(seed + 1000 if batch == 0 else [seed + 1000, batch], 3)
     rows = np.asarray(rows, dtype=np.int64)
     row_base = np.zeros(F + 1, dtype=np.int64)
     np.cumsum(rows, out=row_base[1:])
@@ -258,13 +273,26 @@ def make_workload(name: str, B: int, F: int, D: int, dtype: int, rows: np.ndarra
         raise ValueError("nnz does not fit int32")
     indices = np.empty(nnz, dtype=np.int32)
     table_rngs = [np.random.default_rng(s) for s in np.random.SeedSequence([seed, 7]).spawn(F)]
+    if batch != 0:   # batch 0's positions per table, to replay its draws of each table's rank -> row map
+        _, offsets0 = _csr(_streams(seed + 1000, 3)[1], F, B, pool[0], pool[1])
     for t in range(F):
         lo, hi = int(offsets[t * B]), int(offsets[(t + 1) * B])
         n = hi - lo
-        if uniform_indices:
-            indices[lo:hi] = table_rngs[t].integers(0, rows[t], size=n)
+        if batch == 0:
+            if uniform_indices:
+                indices[lo:hi] = table_rngs[t].integers(0, rows[t], size=n)
+            else:
+                indices[lo:hi] = zipf_rows(table_rngs[t], int(rows[t]), alpha, n)
         else:
-            indices[lo:hi] = zipf_rows(table_rngs[t], int(rows[t]), alpha, n)
+            rb = np.random.default_rng(np.random.SeedSequence([seed, 7, t, batch]))
+            if uniform_indices:
+                indices[lo:hi] = rb.integers(0, rows[t], size=n)
+            else:
+                # the table's rank -> row map as batch 0 draws it (after batch 0's ranks)
+                n0 = int(offsets0[(t + 1) * B] - offsets0[t * B])
+                a, c = zipf_map(table_rngs[t], int(rows[t]), alpha, n0)
+                k = BoundedZipf(int(rows[t]), alpha).sample(rb, n)
+                indices[lo:hi] = 0 if int(rows[t]) == 1 else (a * (k - 1) + c) % int(rows[t])
     grad = None
     if with_grad:
         grad = r_grad.normal(0.0, grad_sigma, size=(B, out_cols)).astype(np.float32)
@@ -275,8 +303,8 @@ def make_workload(name: str, B: int, F: int, D: int, dtype: int, rows: np.ndarra
                     meta=dict(alpha=alpha, pool=pool, uniform=uniform_indices))
 
 
-def _dense_input(seed: int, B: int, n_features: int, dist: str, mlp: list[int], dtype: int):
-    rng = np.random.default_rng(np.random.SeedSequence([seed, 3]))
+def _dense_input(seed: int, B: int, n_features: int, dist: str, mlp: list[int], dtype: int, batch: int = 0):
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 3] if batch == 0 else [seed, 3, batch]))
     if dist == "normal":
         x = rng.standard_normal((B, n_features)).astype(np.float32)
     else:
@@ -308,28 +336,28 @@ def tiny_slice(seed: int = 0, B: int = 256, train: bool = False) -> Workload:
 
 def dlrm_default(B: int = 65536, dtype: int = F16, alpha: float = 1.05, seed: int = 0,
                  train: bool = False, uniform_indices: bool = False,
-                 rows: np.ndarray | None = None) -> Workload:
+                 rows: np.ndarray | None = None, batch: int = 0) -> Workload:
     """26 single-hot tables, D=128, row counts log-uniform in [10, 4e6]; 13
     lognormal dense features through the 13->512->256->128 bottom MLP; the
     27-vector interaction is 351 + 128 = 479 columns, padded to 480."""
     F, D = 26, 128
     if rows is None:
         rows = log_uniform_rows(np.random.default_rng(np.random.SeedSequence([seed, 11])), F, 10, 4e6)
-    dense = _dense_input(seed, B, 13, "lognormal", [512, 256, 128], dtype)
+    dense = _dense_input(seed, B, 13, "lognormal", [512, 256, 128], dtype, batch)
     return make_workload("dlrm-default", B, F, D, dtype, rows, alpha=alpha, dense=dense,
                          out_cols=480, seed=seed, with_grad=train,
-                         uniform_indices=uniform_indices)
+                         uniform_indices=uniform_indices, batch=batch)
 
 
 def multi_hot(B: int = 16384, rows_per_table: int = 1_000_000, alpha: float = 1.05,
-              seed: int = 0, uniform_indices: bool = False, F: int = 26) -> Workload:
+              seed: int = 0, uniform_indices: bool = False, F: int = 26, batch: int = 0) -> Workload:
     """26 fp32 tables x 1e6 rows x 128, pooling factor uniform in [1, 100]."""
     D = 128
     dense = np.zeros((B, D), dtype=np.float32)
     rows = np.full(F, rows_per_table, dtype=np.int64)
     return make_workload("multi-hot", B, F, D, F32, rows, alpha=alpha, dense=dense,
                          out_cols=interaction_width(F, D), seed=seed, pool=(1, 100),
-                         with_grad=True, uniform_indices=uniform_indices)
+                         with_grad=True, uniform_indices=uniform_indices, batch=batch)
 
 
 def large_tables_rows(seed: int = 0) -> np.ndarray:

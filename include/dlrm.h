@@ -311,24 +311,28 @@ dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t
  * It allocates nothing and calls no allocating routine.
  *
  *  - Sizes whose dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows) exceeds
- *    DLRM_NOALLOC_SCRATCH_BYTES are rejected with DLRM_ERR_UNSUPPORTED (at
- *    D = 128 the limit is 344,960 indices; at D = 16, 813,312).
- *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    DLRM_NOALLOC_SCRATCH_BYTES are rejected with DLRM_ERR_UNSUPPORTED before
+ *    anything is enqueued.  The workspace grows with nnz and D only, so the
+ *    limit is at most 796,416 indices at D = 128 and 955,136 at D = 16.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address in the current CUDA context and caches it; make
+ *    that first call before any stream capture.  A call from another context
+ *    on the device -- for instance after cudaDeviceReset created a new primary
+ *    context -- looks the address up again, so it too should come before any
+ *    capture.
  *  - All calls share the one array, which keeps the previous call's
  *    contents (everything that must start at zero is cleared by each call).
  *    Calls that overlap on the GPU -- on different streams, or from several
  *    host threads -- race on it and must be serialised by the caller.
- * Results are identical to dlrm_emb_bwd_sgd; the sorted keys are not
- * returned.  Flags as for dlrm_emb_bwd_sgd (with DLRM_FLAG_GRAD_F16 the
- * gradient pointer holds fp16).
+ * Results are bit-identical to dlrm_emb_bwd_sgd on the same inputs; the
+ * sorted keys are not returned.  Flags as for dlrm_emb_bwd_sgd (with
+ * DLRM_FLAG_GRAD_F16 the gradient pointer holds fp16).
  */
 #define DLRM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base, int64_t total_rows,
                                      int F, int D, int B, const int32_t* d_indices,
                                      const int32_t* d_offsets, int64_t nnz,
-                                     const float* d_grad_pooled, float lr, unsigned flags,
+                                     const void* d_grad_pooled, float lr, unsigned flags,
                                      uint32_t* d_status, void* stream);
 
 /* Round a byte count up to the workspace sub-buffer alignment (256 bytes). */

@@ -223,3 +223,22 @@ def test_synth_validation(L):
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         dl.load(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("D,limit", [(128, 796_416), (16, 955_136)])
+def test_noalloc_capacity_quoted_in_the_header(L, D, limit):
+    """The most indices dlrm_emb_bwd_sgd_noalloc takes, as include/dlrm.h quotes them: the
+    workspace of `limit` indices fits the built-in scratch and one more does not, whatever
+    the table size."""
+    src = open(os.path.join(ROOT, "include", "dlrm.h")).read()
+    assert f"{limit:,}" in src
+    for rows in (10, 9_056_641, 2**32 - 2):
+        assert L.dlrm_emb_bwd_sgd_workspace_size(limit, D, rows) <= dl.DLRM_NOALLOC_SCRATCH_BYTES
+        assert L.dlrm_emb_bwd_sgd_workspace_size(limit + 1, D, rows) > dl.DLRM_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_rejects_over_capacity_before_any_launch(L):
+    """One index past the capacity is refused on the host (nothing reaches the GPU)."""
+    rc = L.dlrm_emb_bwd_sgd_noalloc(FAKE, FAKE, 10, 1, 128, 796_417, FAKE, FAKE, 796_417, FAKE,
+                                    ctypes.c_float(0.1), 0, None, None)
+    assert rc == dl.DLRM_ERR_UNSUPPORTED and "scratch" in _err(L)
