@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                    ctypes.c_size_t, ctypes.c_uint, _P, _P]
     L.dlrm_emb_bwd_sgd_noalloc.argtypes = [_P, _P, _I64, _I, _I, _I, _P, _P, _I64, _P, ctypes.c_float,
                                            ctypes.c_uint, _P, _P]
+    L.dlrm_set_wait_limit.argtypes = [_I64]
+    L.dlrm_set_wait_limit.restype = _I64
     L.dlrm_ws_align.argtypes = [ctypes.c_size_t]
     L.dlrm_ws_align.restype = ctypes.c_size_t
     L.dlrm_last_error.argtypes = []
@@ -92,6 +94,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     if path is None:
         _lib = L
     return L
+
+
+def dlrm_set_wait_limit(cycles: int) -> int:
+    """Bound of the tensor-core kernels' on-chip waits in SM cycles (negative: the default,
+    about two seconds); returns the previous bound."""
+    return int(load().dlrm_set_wait_limit(int(cycles)))
 
 
 def dlrm_last_error() -> str:

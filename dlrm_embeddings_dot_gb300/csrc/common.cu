@@ -1,5 +1,6 @@
 // common.cu -- error reporting, device queries and the seeded table synthesiser.
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,6 +19,21 @@ void set_error(const char* fmt, ...)
 }
 
 void clear_error() { g_last_error[0] = '\0'; }
+
+static std::atomic<long long> g_wait_limit{-1};   // negative: the default
+
+long long wait_limit_cycles()
+{
+    const long long v = g_wait_limit.load(std::memory_order_relaxed);
+    return v < 0 || v > kDefaultWaitCycles ? kDefaultWaitCycles : v;
+}
+
+long long set_wait_limit_cycles(long long cycles)
+{
+    const long long prev = wait_limit_cycles();
+    g_wait_limit.store(cycles < 0 ? -1 : cycles, std::memory_order_relaxed);
+    return prev;
+}
 
 int num_sms()
 {
@@ -64,6 +80,8 @@ __global__ void synth_uniform_kernel(T* dst, uint64_t seed, int64_t first, int64
 }  // namespace dlrm
 
 using namespace dlrm;
+
+extern "C" int64_t dlrm_set_wait_limit(int64_t cycles) { return set_wait_limit_cycles(cycles); }
 
 extern "C" size_t dlrm_ws_align(size_t bytes) { return (bytes + 255) & ~(size_t)255; }
 

@@ -73,6 +73,12 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 int num_sms();   // SM count of the current device (cached per device)
 
+// Cycles a bounded on-chip wait of the tensor-core kernels lasts before the
+// kernel gives up (dlrm_set_wait_limit; about two seconds by default).
+constexpr long long kDefaultWaitCycles = 4000000000LL;
+long long wait_limit_cycles();
+long long set_wait_limit_cycles(long long cycles);   // negative: the default; returns the previous limit
+
 // -------------------------------------------------------------- device side
 constexpr int kWarp = 32;
 

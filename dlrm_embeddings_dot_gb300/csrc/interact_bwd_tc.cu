@@ -59,7 +59,7 @@ __host__ __device__ inline size_t bwd_smem(int KH, int P, int ns)
 {
     const size_t g_bytes = (size_t)kGroup * 2 * ((P * 2 + 15) / 16 * 16);   // two G rows per builder
     return 1024 + (size_t)ns * ((size_t)KH * kZBlockBytes + kABytes) + kOutStage + kGdScratch + g_bytes +
-           (size_t)(2 * ns + 4) * 8 + 16;
+           (size_t)(3 * ns + 4) * 8 + 16;
 }
 
 __device__ __forceinline__ uint16_t ld_h(const uint16_t* g, int i) { return g[i]; }
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __grid_constant__ CUtensorMap map_dense,
                        const __grid_constant__ CUtensorMap map_gpooled, const __half* __restrict__ grad_out,
                        __half* __restrict__ grad_dense, int F, int D, int B, int P, int KH, int NS,
-                       uint32_t tmem_cols, uint32_t* status)
+                       uint32_t tmem_cols, uint32_t* status, long long wait_cycles)
 {
     pdl_wait_and_release();
     extern __shared__ uint8_t smem_raw[];
@@ -80,8 +80,9 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
     uint8_t* ostage = smem + (size_t)NS * stage_bytes;      // 1 KB aligned
     uint8_t* gdscr = ostage + kOutStage;
     uint8_t* gstage = gdscr + kGdScratch;
-    uint64_t* full = reinterpret_cast<uint64_t*>(gstage + kGroup * 2 * gpitch);
-    uint64_t* empty = full + NS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(gstage + kGroup * 2 * gpitch);   // Z copies landed
+    uint64_t* built = full + NS;                                                    // A tile built
+    uint64_t* empty = built + NS;
     uint64_t* tfull = empty + NS;
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
@@ -93,7 +94,8 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1 + kGroup);   // the TMA producer's arrive.expect_tx + four builders
+            mbar_init(&full[i], 1);        // the TMA producer's arrive.expect_tx
+            mbar_init(&built[i], kGroup);  // the four builders (apart, so an abort can drain the copies alone)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -133,7 +135,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
             int it = 0;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
                 const int stage = it % NS;
-                if (!mbar_wait(&empty[stage], ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag)) break;
+                if (!mbar_wait(&empty[stage], ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, wait_cycles)) break;
                 uint8_t* sb = stages + (size_t)stage * stage_bytes;
                 mbar_expect_tx(&full[stage], (uint32_t)KH * (kM * 128 + kGroup * 128));
                 for (int kb = 0; kb < KH; ++kb) {
@@ -150,9 +152,10 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
             int it = 0;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
                 const int stage = it % NS, buf = it & 1;
-                if (!mbar_wait(&tempty[buf], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag)) break;
+                if (!mbar_wait(&tempty[buf], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, wait_cycles)) break;
                 tc_fence_after();
-                if (!mbar_wait(&full[stage], (uint32_t)(it / NS) & 1u, abort_flag)) break;
+                if (!mbar_wait(&full[stage], (uint32_t)(it / NS) & 1u, abort_flag, wait_cycles)) break;
+                if (!mbar_wait(&built[stage], (uint32_t)(it / NS) & 1u, abort_flag, wait_cycles)) break;
                 tc_fence_after();
                 const uint32_t zb = smem_u32(stages + (size_t)stage * stage_bytes);
                 const uint32_t ab = zb + (uint32_t)z_bytes;
@@ -190,7 +193,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
             const int buf = it & 1;
             const uint4 gcur = gnext;
             gnext = load_gd(tile + gridDim.x);
-            if (!mbar_wait(&tfull[buf], (uint32_t)(it >> 1) & 1u, abort_flag)) break;
+            if (!mbar_wait(&tfull[buf], (uint32_t)(it >> 1) & 1u, abort_flag, wait_cycles)) break;
             if (lane < D / 8) gd_s[lane] = gcur;
             __syncwarp();
             tc_fence_after();
@@ -283,7 +286,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
             const uint16_t* gh = reinterpret_cast<const uint16_t*>(grows + (it & 1) * gpitch);
             __syncwarp();
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(&empty[stage], ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag);
+            if (lane == 0) ok = mbar_wait(&empty[stage], ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, wait_cycles);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             __syncwarp();
             // Z index of this row: p = lane + 1 for embedding rows, 0 for row 31 (dZ_0)
@@ -315,7 +318,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full[stage]);
+            if (lane == 0) mbar_arrive(&built[stage]);
             put_g((it + 1) & 1, rn);
         }
     }
@@ -396,6 +399,6 @@ extern "C" dlrm_status dlrm_interact_bwd_f16(const void* d_grad_out, const void*
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_interact_bwd_f16: %s", cudaGetErrorString(e));
     return check_launch_pdl(launch_pdl(interact_bwd_tc_kernel, grid, kThreads, smem, as_stream(stream), mp, md, mg,
                                        (const __half*)d_grad_out, (__half*)d_grad_dense, F, D, B, out_cols, KH, ns,
-                                       tmem_cols, d_status),
+                                       tmem_cols, d_status, wait_limit_cycles()),
                             "interact_bwd_tc_kernel");
 }

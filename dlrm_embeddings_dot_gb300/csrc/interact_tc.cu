@@ -101,7 +101,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                    const __grid_constant__ CUtensorMap map_dense,
                    const __half* __restrict__ dense,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
-                   uint32_t* status, GatherArgs ga)
+                   uint32_t* status, GatherArgs ga, long long wait_cycles)
 {
     pdl_wait_and_release();
     extern __shared__ uint8_t smem_raw[];
@@ -180,7 +180,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                 for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
                     const int stage = it % NS;
                     const uint32_t ph = (uint32_t)(it / NS) & 1u;
-                    if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) break;
+                    if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, wait_cycles)) break;
                     uint8_t* sb = stages + (size_t)stage * L.stage_bytes;
                     mbar_expect_tx(&full[stage], (uint32_t)KH * (kEBytes + kGroup * 128));
                     for (int kb = 0; kb < KH; ++kb) {
@@ -300,7 +300,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                     }
                     if (k0 == 0) {
                         int w = 1;
-                        if (lane == 0) w = mbar_wait(&empty[stage], ph ^ 1u, abort_flag);
+                        if (lane == 0) w = mbar_wait(&empty[stage], ph ^ 1u, abort_flag, wait_cycles);
                         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
                         if (!ok) break;
                     }
@@ -392,9 +392,9 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                 const uint32_t ph = (uint32_t)(it / NS) & 1u;
                 const int buf = it & 1;
                 const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-                if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag)) break;
+                if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, wait_cycles)) break;
                 tc_fence_after();
-                if (!mbar_wait(&full[stage], ph, abort_flag)) break;
+                if (!mbar_wait(&full[stage], ph, abort_flag, wait_cycles)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * kAccStride);
                 const uint32_t sb = smem_u32(stages + (size_t)stage * L.stage_bytes);
@@ -429,7 +429,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
             const uint32_t bph = (uint32_t)(it >> 1) & 1u;
             const uint4 dcur = dnext;
             dnext = load_dense(tile + gridDim.x);
-            if (!mbar_wait(&tfull[buf], bph, abort_flag)) break;
+            if (!mbar_wait(&tfull[buf], bph, abort_flag, wait_cycles)) break;
             __syncwarp();
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(kSlot * q) << 16) + (uint32_t)(buf * kAccStride);
@@ -511,7 +511,8 @@ dlrm_status launch_kernel(int grid, int threads, const Layout& L, const CUtensor
                                          (int)L.smem);
     if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
     return check_launch_pdl(launch_pdl(interact_tc_kernel<kFused, kCpr>, grid, threads, L.smem, stream, mp, md,
-                                       (const __half*)dense, (__half*)out, F, D, B, P, KH, ns, status, ga),
+                                       (const __half*)dense, (__half*)out, F, D, B, P, KH, ns, status, ga,
+                                       wait_limit_cycles()),
                             "interact_tc_kernel");
 }
 

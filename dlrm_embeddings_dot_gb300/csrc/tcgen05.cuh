@@ -11,7 +11,7 @@
 namespace dlrm {
 namespace tc {
 
-constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
+constexpr long long kWaitCycles = kDefaultWaitCycles;   // about two seconds
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -46,10 +46,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete.  Returns false if the
-// CTA is aborting or the bound is hit (which starts the abort).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
 {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false if the
+// CTA is aborting or the bound is hit (which starts the abort).  A bound
+// shorter than the default (a failure-detection test's) polls without
+// blocking, so a wait that is not already complete gives up once `limit`
+// cycles have passed (at the first poll for limit 0).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit = kWaitCycles)
+{
+    if (limit < kWaitCycles) {
+        const long long t0 = clock64();
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (clock64() - t0 >= limit) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {

@@ -335,6 +335,26 @@ dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* d_row_base,
                                      const void* d_grad_pooled, float lr, unsigned flags,
                                      uint32_t* d_status, void* stream);
 
+/*
+ * dlrm_set_wait_limit -- how long a bounded on-chip wait of the tensor-core
+ * kernels (dlrm_interact_fwd and dlrm_emb_interact_fwd on fp16,
+ * dlrm_interact_bwd_f16) lasts before the kernel gives up, in SM clock cycles.
+ * (The pages have no counterpart: this is the failure detection of the
+ * library itself.)
+ *
+ * Every wait of those kernels on a copy, a tensor-core product or a peer warp
+ * is bounded; when one gives up the kernel lets the copies and products it
+ * already issued finish (each within the default bound), frees its tensor
+ * memory, sets DLRM_STATUS_TIMEOUT in *d_status and returns, so the context
+ * stays usable and the output is incomplete.  The default, about two seconds,
+ * only ends a wait that something has broken; a shorter limit exists to test
+ * that path (0 gives up at the first wait that is not already complete).
+ * cycles < 0 restores the default; larger values are clamped to it.  The limit
+ * is read when a call is made (it is a kernel argument) and is process-wide.
+ * Returns the previous limit.
+ */
+int64_t dlrm_set_wait_limit(int64_t cycles);
+
 /* Round a byte count up to the workspace sub-buffer alignment (256 bytes). */
 size_t dlrm_ws_align(size_t bytes);
 
