@@ -91,6 +91,7 @@ extern "C" dlrm_status dlrm_synth_fill_uniform(void* d_dst, dlrm_dtype dtype, ui
                                                int64_t first_elem, int64_t count, double amplitude,
                                                void* stream)
 {
+    DLRM_API_RANGE("dlrm_synth_fill_uniform");
     clear_error();
     if (!d_dst) return fail(DLRM_ERR_INVALID_ARG, "dlrm_synth_fill_uniform: d_dst is NULL");
     if (count < 0 || first_elem < 0)

@@ -11,6 +11,7 @@
 #include <cstdio>
 
 #include "dlrm.h"
+#include <nvtx3/nvToolsExt.h>
 
 namespace dlrm {
 
@@ -65,6 +66,17 @@ inline dlrm_status check_launch_pdl(cudaError_t e, const char* what)
     }
     return check_launch(what);
 }
+
+// NVTX range around one C-ABI call (the host-side enqueue): profilers that
+// record NVTX show each call by its name over the kernels it launched.
+// Without a tool attached the push and pop cost a few nanoseconds.
+struct ApiRange {
+    explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+    ~ApiRange() { nvtxRangePop(); }
+    ApiRange(const ApiRange&) = delete;
+    ApiRange& operator=(const ApiRange&) = delete;
+};
+#define DLRM_API_RANGE(name) ::dlrm::ApiRange dlrm_api_range_(name)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int dtype_size(dlrm_dtype dt) { return dt == DLRM_F16 ? 2 : 4; }

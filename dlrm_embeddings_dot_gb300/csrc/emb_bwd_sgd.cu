@@ -813,6 +813,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
                                         int64_t nnz, const void* d_grad_pooled, float lr, void* d_workspace,
                                         size_t workspace_bytes, unsigned flags, uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_bwd_sgd");
     clear_error();
     if (F < 1 || D < 1 || B < 0)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_bwd_sgd: need F >= 1, D >= 1, B >= 0");
@@ -977,6 +978,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd_noalloc(float* d_tables, const int64_t* 
                                                 const void* d_grad_pooled, float lr, unsigned flags,
                                                 uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_bwd_sgd_noalloc");
     clear_error();
     const size_t need = dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows);
     if (need == 0 && nnz != 0)

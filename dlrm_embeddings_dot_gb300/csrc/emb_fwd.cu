@@ -412,6 +412,7 @@ extern "C" dlrm_status dlrm_emb_fwd(const void* d_tables, dlrm_dtype dtype,
                                     int64_t nnz, void* d_pooled, unsigned flags,
                                     uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_fwd");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_fwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)

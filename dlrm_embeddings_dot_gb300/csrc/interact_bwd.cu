@@ -421,6 +421,7 @@ extern "C" dlrm_status dlrm_interact_bwd(const float* d_grad_out, const void* d_
                                          dlrm_dtype dtype, int F, int D, int B, int out_cols,
                                          float* d_grad_dense, float* d_grad_pooled, void* stream)
 {
+    DLRM_API_RANGE("dlrm_interact_bwd");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)
@@ -459,6 +460,7 @@ extern "C" dlrm_status dlrm_emb_interact_bwd(const void* d_tables, dlrm_dtype dt
                                             float* d_grad_dense, float* d_grad_pooled, unsigned flags,
                                             uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_interact_bwd");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_bwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)

@@ -343,6 +343,7 @@ extern "C" dlrm_status dlrm_interact_bwd_f16(const void* d_grad_out, const void*
                                              int D, int B, int out_cols, void* d_grad_dense, void* d_grad_pooled,
                                              uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_interact_bwd_f16");
     clear_error();
     if (F < 1 || D < 1 || B < 0)
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_bwd_f16: need F >= 1, D >= 1, B >= 0");

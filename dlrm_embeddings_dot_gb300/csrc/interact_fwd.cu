@@ -600,6 +600,7 @@ extern "C" dlrm_status dlrm_interact_fwd(const void* d_dense, const void* d_pool
                                          int F, int D, int B, void* d_out, int out_cols,
                                          uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_interact_fwd");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_interact_fwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)
@@ -628,6 +629,7 @@ extern "C" dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const vo
                                                    dlrm_dtype dtype, int F, int D, int B,
                                                    void* d_out, int out_cols, void* stream)
 {
+    DLRM_API_RANGE("dlrm_interact_fwd_cuda_core");
     clear_error();
     if (!dtype_ok(dtype) || F < 1 || D < 1 || B < 0 || !d_dense || !d_pooled || !d_out ||
         out_cols < (int64_t)D + (int64_t)F * (F + 1) / 2)
@@ -646,6 +648,7 @@ extern "C" dlrm_status dlrm_emb_interact_fwd_train(const void* d_tables, dlrm_dt
                                                    void* d_pooled, void* d_out, int out_cols, unsigned flags,
                                                    uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_interact_fwd_train");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd_train: bad dtype");
     if (F < 1 || D < 1 || B < 0)

@@ -586,6 +586,7 @@ extern "C" dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dt
                                              void* d_out, int out_cols, unsigned flags, uint32_t* d_status,
                                              void* stream)
 {
+    DLRM_API_RANGE("dlrm_emb_interact_fwd");
     clear_error();
     if (!dtype_ok(dtype)) return fail(DLRM_ERR_INVALID_ARG, "dlrm_emb_interact_fwd: bad dtype");
     if (F < 1 || D < 1 || B < 0)

@@ -320,6 +320,7 @@ extern "C" dlrm_status dlrm_bottom_mlp_fwd(const float* d_x, int B, int n_layers
                                            const void* d_weights, const float* d_biases, void* d_out,
                                            void* d_workspace, size_t ws_bytes, uint32_t* d_status, void* stream)
 {
+    DLRM_API_RANGE("dlrm_bottom_mlp_fwd");
     clear_error();
     if (!mlp_dims_ok(B, n_layers, dims))
         return fail(DLRM_ERR_INVALID_ARG, "dlrm_bottom_mlp_fwd: need B >= 0, 1..64 layers, widths in [1, 65536]");
