@@ -18,14 +18,18 @@
 // Register kernel (fp32, D = 128, F + 1 rows of Z known at compile time): one
 // warp per sample.  Lane l holds features 4l..4l+3 of every row of Z in
 // registers and forms its four-feature partial dot products for all F(F+1)/2
-// pairs (i, j), j < i, in output order, in groups of 32 -- no wasted product.
-// Each group is finished by a transpose through a per-warp 32 x 36 shared
-// scratch: lane l stores its 32 partials as row l (four 16-byte stores, no
-// bank conflict with the 36-float pitch), and lane t adds column t in lane
-// order (32 conflict-free 4-byte reads), which leaves the dot product of the
-// group's pair t in lane t: 32 consecutive output columns, one coalesced
-// store.  (A shuffle transpose-reduce moves half the bytes but serialises a
-// select, a shuffle and an add per step and measured slower.)  A sample
+// pairs (i, j), j < i, in output order, in groups of 32 -- no wasted product
+// (two packed fp32x2 instructions and one add per pair).  Each group is
+// finished by a transpose through a per-warp 32 x 36 shared scratch: lane l
+// stores its 32 partials as row l (four 16-byte stores, no bank conflict with
+// the 36-float pitch), and lane t adds column t (32 conflict-free 4-byte reads
+// into 8 interleaved sums, then a 3-level tree: a dependent chain of 6 adds
+// instead of 31), which leaves the dot product of the group's pair t in lane
+// t: 32 consecutive output columns, one coalesced store.  The kernel is bound
+// by each warp's own latency (its time scales with 1 / resident warps, which
+// registers and shared memory cap at 12 per SM), so shorter chains and fewer
+// instructions pay; moving part of the reduction to shuffles (fewer shared
+// wavefronts, more instructions) measured slower.  A sample
 // arrives in the warp's buffer by two bulk copies (the dense row, then the F
 // pooled rows, contiguous in global memory) completing on the warp's
 // mbarrier; the next sample's copy is issued after the first group, behind a
@@ -258,9 +262,25 @@ constexpr int pair_row(int p)
     return i;
 }
 
+// Four-feature dot product with the packed two-lane fp32 instructions (each
+// lane of mul/fma.rn.f32x2 rounds as the scalar instruction does): features
+// (x, y) and (z, w) side by side, then the two halves added, in half the
+// multiply-add instructions of four scalar ones.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
 __device__ __forceinline__ float dot4(const float4& a, const float4& b)
 {
-    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+    uint64_t p;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(pack2(a.x, a.y)), "l"(pack2(b.x, b.y)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(p) : "l"(pack2(a.z, a.w)), "l"(pack2(b.z, b.w)));
+    float xz, yw;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(xz), "=f"(yw) : "l"(p));
+    return xz + yw;
 }
 
 // Four-feature partial dot product of pair p (zero past the last pair).
@@ -308,9 +328,12 @@ __device__ __forceinline__ void regs_sample(const float4 (&z)[R], float* orow, i
         for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4*>(row + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         __syncwarp();
-        float sum = scratch[lane];
+        float s8[8];
 #pragma unroll
-        for (int r = 1; r < 32; ++r) sum += scratch[r * kPitch + lane];
+        for (int r = 0; r < 8; ++r) s8[r] = scratch[r * kPitch + lane];
+#pragma unroll
+        for (int r = 8; r < 32; ++r) s8[r & 7] += scratch[r * kPitch + lane];
+        const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
         const int col = D + g * 32 + lane;
         if (col < P) orow[col] = sum;
         // orders this group's scratch reads before the next group's writes;
