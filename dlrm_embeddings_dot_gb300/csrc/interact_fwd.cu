@@ -253,6 +253,8 @@ interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pool
 constexpr int kRegWarps = 4;     // warps per CTA, one sample each at a time
 constexpr int kRegD = 128;       // 32 lanes x 4 features
 constexpr int kPitch = 36;       // floats per row of the transpose scratch
+constexpr int kGatherRing = 8;   // staging rows of the one-pass gather (8 x 512 bytes <= the scratch)
+static_assert(kGatherRing * kRegD <= 32 * kPitch, "gather ring larger than the transpose scratch");
 
 // Pair p of the strict lower triangle in row-major order: p = i(i-1)/2 + j.
 constexpr int pair_row(int p)
@@ -404,7 +406,9 @@ interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restric
 // bulk copy on the warp's mbarrier (the tensor-memory-access unit moves the
 // rows, so the gather adds nothing to the shared-memory pipe that bounds the
 // interaction); empty bags (and rejected indices) give zero rows, bags of
-// several indices are summed in fp32 in bag order by the whole warp.
+// several indices are summed in fp32 in bag order by the whole warp, their
+// positions as one list streamed through the transpose scratch (free while
+// the next sample is staged) eight rows at a time.
 // The pooled rows (rows 1..F of the buffer) leave by one bulk store, so the
 // lookup's output is written once and never read back.  Pooled rows and
 // interaction are bit-identical to dlrm_emb_fwd + dlrm_interact_fwd.
@@ -447,7 +451,9 @@ emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, f
     // fill the buffer with sample smp: the bags' rows as rows 1..F, the dense
     // row (lane F's bulk copy) as row 0; lane 0 arrives once all are counted
     auto stage = [&](int64_t smp, uint32_t src_row, int a, int e) {
-        bags.gather(mine, src_row, a, e, bar);
+        // the transpose scratch is free while a sample is staged: it holds the
+        // rows of several-index bags in flight
+        bags.template gather<false, 4, kGatherRing>(mine, src_row, a, e, bar, reinterpret_cast<float4*>(scratch));
         if (lane == F) {
             tc::mbar_expect_tx_only(bar, D * 4);
             tc::bulk_g2s(mine, dense + smp * D, D * 4, bar);
@@ -693,11 +699,12 @@ extern "C" dlrm_status dlrm_emb_interact_fwd_train(const void* d_tables, dlrm_dt
                     "dlrm_emb_fwd + dlrm_interact_fwd otherwise)");
     if (B == 0) return DLRM_OK;
     const int64_t nbags = (int64_t)F * B;
-    if (nnz > nbags + nbags / 8) {
-        // Bags of several indices: one warp per sample sums them one bag after another, while the
-        // lookup spreads the bags over all warps (at 64K samples of 26 bags averaging 1.5 indices,
-        // 0.87 ms in one pass against 0.79 ms as two launches).  The two launches compute the same
-        // bits, so the choice is by speed alone.
+    if (nnz > 3 * nbags) {
+        // Many indices per bag: one warp per sample streams its sample's rows eight at a time, while
+        // the lookup spreads the bags over all warps with more rows in flight (64K samples of 26 bags
+        // over 1e6-row tables: one pass 0.427 against 0.465 ms as two launches at 1.5 indices per
+        // bag, 0.730 against 0.700 at 4).  The two launches compute the same bits, so the choice is
+        // by speed alone.
         dlrm_status s = dlrm_emb_fwd(d_tables, dtype, d_row_base, F, D, B, d_indices, d_offsets, nnz, d_pooled,
                                      flags, d_status, stream);
         if (s != DLRM_OK) return s;

@@ -90,11 +90,13 @@ struct BagLanes {
     // kCopyAsync: every lane copies its 16-byte column of each single-index row
     // with cp.async (completion: cp.async.wait_group by the same lane, which
     // reads only the columns it copied) instead of lane t's bulk copy of row t.
-    // kMultiU: positions of a several-index bag in flight (indices, then rows),
-    // added in bag order; few enough that the caller's live registers are not
-    // spilled
-    template <bool kCopyAsync = false, int kMultiU = 4>
-    __device__ __forceinline__ void gather(float4* buf, uint32_t src_row, int a, int e, uint64_t* bar) const
+    // kMultiU: rows of the several-index bags in flight in registers, few
+    // enough that the caller's live registers are not spilled; kRing > 0: in
+    // flight through kRing rows of shared staging (ring: kRing x 32 float4,
+    // free while gather runs) instead, which costs no registers.
+    template <bool kCopyAsync = false, int kMultiU = 4, int kRing = 0>
+    __device__ __forceinline__ void gather(float4* buf, uint32_t src_row, int a, int e, uint64_t* bar,
+                                           float4* ring = nullptr) const
     {
         if constexpr (kCopyAsync) {
 #pragma unroll
@@ -114,46 +116,123 @@ struct BagLanes {
         }
         for (uint32_t zero = __ballot_sync(0xffffffffu, lane < F && src_row == kRowZero); zero; zero &= zero - 1)
             buf[__ffs(zero) * kWarp + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (uint32_t multi = __ballot_sync(0xffffffffu, src_row == kRowMulti); multi; multi &= multi - 1) {
-            const int t = __ffs(multi) - 1;
-            const int s1 = __shfl_sync(0xffffffffu, a, t), e1 = __shfl_sync(0xffffffffu, e, t);
-            const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p0 = s1; p0 < e1; p0 += kMultiU) {
-                int idx[kMultiU];
+        // Bags of several indices: their positions form one list in bag order
+        // (lane t < F holds bag t's count).  Each lane resolves one of 32
+        // positions at a time (coalesced index loads), then the warp adds the
+        // rows kMultiU at a time, each bag's in position order from zero in
+        // fp32, and stores a bag's sum into its buffer row when the next bag
+        // begins.  A row waits for one index load, not for the bags before it.
+        const int cnt = (lane < F && src_row == kRowMulti) ? e - a : 0;
+        if (!__any_sync(0xffffffffu, cnt > 0)) return;
+        int incl = cnt;
 #pragma unroll
-                for (int u = 0; u < kMultiU; ++u) idx[u] = p0 + u < e1 ? __ldg(ga.indices + p0 + u) : 0;
-                uint32_t row[kMultiU];   // kRowZero: skipped or past the bag
-                float4 r[kMultiU];
-#pragma unroll
-                for (int u = 0; u < kMultiU; ++u) {
-                    int64_t i = idx[u];
-                    row[u] = kRowZero;
-                    if (p0 + u < e1) {
-                        if (ga.hash && n > 0) {
-                            i %= n;
-                            if (i < 0) i += n;
-                            row[u] = (uint32_t)(base + i);
-                        } else if (ga.hash || i < 0 || i >= n) {
-                            set_status(status, DLRM_STATUS_OOB_INDEX);
-                        } else {
-                            row[u] = (uint32_t)(base + i);
-                        }
-                    }
-                    r[u] = row[u] != kRowZero ? u4_as_f4(ldg_nc_l1_v4(ga.tables + (size_t)row[u] * D + 4 * lane))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int u = 0; u < kMultiU; ++u)
-                    if (row[u] != kRowZero) {
-                        acc.x += r[u].x;
-                        acc.y += r[u].y;
-                        acc.z += r[u].z;
-                        acc.w += r[u].w;
-                    }
-            }
-            buf[(t + 1) * kWarp + lane] = acc;
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
+        const int excl = incl - cnt;
+        const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int cur = -1;   // bag being summed (warp-uniform)
+        // position q0 + lane: its bag (the last lane whose list offset is at
+        // most the position) and its table row (kRowZero: skipped or past the list)
+        auto locate = [&](int q0, int& k, uint32_t& row) {
+            const int q = q0 + lane;
+            k = 0;
+#pragma unroll
+            for (int step = kWarp / 2; step > 0; step >>= 1)
+                if (__shfl_sync(0xffffffffu, excl, k + step) <= q) k += step;
+            const int pos = __shfl_sync(0xffffffffu, a, k) + (q - __shfl_sync(0xffffffffu, excl, k));
+            const int64_t base = __shfl_sync(0xffffffffu, tbase, k), n = __shfl_sync(0xffffffffu, tn, k);
+            row = kRowZero;
+            if (q < total) {
+                int64_t i = __ldg(ga.indices + pos);
+                if (ga.hash && n > 0) {
+                    i %= n;
+                    if (i < 0) i += n;
+                    row = (uint32_t)(base + i);
+                } else if (ga.hash || i < 0 || i >= n) {
+                    set_status(status, DLRM_STATUS_OOB_INDEX);
+                } else {
+                    row = (uint32_t)(base + i);
+                }
+            }
+        };
+        auto add = [&](int kj, uint32_t rowj, const float4& v) {
+            if (kj != cur) {
+                if (cur >= 0) buf[(cur + 1) * kWarp + lane] = acc;
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                cur = kj;
+            }
+            if (rowj != kRowZero) {
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        };
+        if constexpr (kRing > 0) {
+            // Rows through a ring of kRing staging rows: lane l copies column l
+            // of position j's row into slot j % kRing, one commit group per
+            // position (empty past the list), so that waiting for all but the
+            // kRing - 1 newest groups completes position j, and reads it back.
+            // The positions stream across chunks of 32: the next chunk's
+            // indices are resolved while this chunk's rows are in flight.
+            static_assert(kRing <= kWarp, "the ring reaches at most one chunk ahead");
+            int kc, kn = 0;
+            uint32_t rc, rn = kRowZero;
+            locate(0, kc, rc);
+            auto issue = [&](int j, int c0) {   // c0: first position of the current chunk
+                const bool next = j >= c0 + kWarp;
+                const uint32_t rowj = __shfl_sync(0xffffffffu, next ? rn : rc, j & (kWarp - 1));
+                if (j < total && rowj != kRowZero) {
+                    const uint32_t d = (uint32_t)__cvta_generic_to_shared(ring + (j % kRing) * kWarp + lane);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
+                                 "l"(ga.tables + (size_t)rowj * D + 4 * lane)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+#pragma unroll
+            for (int j = 0; j < kRing; ++j) issue(j, 0);
+            for (int c0 = 0; c0 < total; c0 += kWarp) {
+                if (c0 + kWarp < total) locate(c0 + kWarp, kn, rn);
+                const int m = total - c0 < kWarp ? total - c0 : kWarp;
+                for (int jj = 0; jj < m; ++jj) {
+                    asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+                    const float4 v = ring[((c0 + jj) % kRing) * kWarp + lane];
+                    add(__shfl_sync(0xffffffffu, kc, jj), __shfl_sync(0xffffffffu, rc, jj), v);
+                    issue(c0 + jj + kRing, c0);
+                }
+                kc = kn;
+                rc = rn;
+            }
+        } else {
+            for (int q0 = 0; q0 < total; q0 += kWarp) {
+                int k;
+                uint32_t row;
+                locate(q0, k, row);
+                const int m = total - q0 < kWarp ? total - q0 : kWarp;
+                for (int j0 = 0; j0 < m; j0 += kMultiU) {
+                    uint32_t rj[kMultiU];
+                    float4 r[kMultiU];
+#pragma unroll
+                    for (int u = 0; u < kMultiU; ++u) {
+                        rj[u] = __shfl_sync(0xffffffffu, row, (j0 + u) & (kWarp - 1));
+                        r[u] = (j0 + u < m && rj[u] != kRowZero)
+                                   ? u4_as_f4(ldg_nc_l1_v4(ga.tables + (size_t)rj[u] * D + 4 * lane))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kMultiU; ++u) {
+                        const int kj = __shfl_sync(0xffffffffu, k, (j0 + u) & (kWarp - 1));
+                        if (j0 + u >= m) break;
+                        add(kj, rj[u], r[u]);
+                    }
+                }
+            }
+        }
+        buf[(cur + 1) * kWarp + lane] = acc;
     }
 };
 

@@ -180,8 +180,8 @@ dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dtype, const 
  * multiple of 4 and at most D + 32 * ceil(F(F+1)/2 / 32) (480 for F = 26),
  * 16-byte aligned tables, dense, pooled and out; otherwise
  * DLRM_ERR_UNSUPPORTED (use the two calls).  Flags: DLRM_FLAG_HASH_INDICES.
- * Status bits as in dlrm_emb_fwd.  When nnz exceeds 1.125 F B (bags of
- * several indices common) the call itself runs the two operations as two
+ * Status bits as in dlrm_emb_fwd.  When nnz exceeds 3 F B (more than three
+ * indices per bag on average) the call itself runs the two operations as two
  * launches, which is faster there and gives the same bits.
  */
 dlrm_status dlrm_emb_interact_fwd_train(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,

@@ -80,9 +80,11 @@ def test_default_shapes_match_two_calls_and_oracle(cuda_lib, B):
     assert_within_abs_sum(o1[samples][:, :W], ro[:, :W], abs_products(c.dense, rp), 1e-5, "fused vs oracle")
 
 
-# bag sizes: "ragged" averages 1.67 indices per bag, so the training forward
-# runs as two launches; "mostly_single" averages 1.06 and stays in one pass
-BAG_MIX = {"ragged": [0, 1, 1, 1, 2, 5], "mostly_single": [1] * 13 + [0, 2, 3]}
+# bag sizes: "heavy" averages 4.2 indices per bag, so the training forward
+# runs as two launches; "ragged" (1.67, with runs of several-index bags longer
+# than one list chunk of 32 positions) and "mostly_single" (1.06) stay in one
+# pass, whose several-index bags go through the staging ring
+BAG_MIX = {"heavy": [0, 1, 2, 5, 9, 8], "ragged": [0, 1, 1, 1, 2, 5], "mostly_single": [1] * 13 + [0, 2, 3]}
 
 
 @pytest.mark.parametrize("F,P", [(26, 480), (8, 164), (8, 192)])
