@@ -324,51 +324,164 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                                  "r"(dv.w)
                                  : "memory");
                 }
-                // bags of several indices (rare): fp32 sum in bag order, one rounding
-                for (uint32_t multi = __ballot_sync(0xffffffffu, row0 == kRowMulti); multi; multi &= multi - 1) {
-                    const int t = __ffs(multi) - 1;
-                    const int s1 = __shfl_sync(0xffffffffu, a0, t), e1 = __shfl_sync(0xffffffffu, z0, t);
-                    const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
-                    const int row = sm * kSlot + t;
-                    for (int c = lane; c < cpr; c += kWarp) {
-                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        constexpr int kMultiU = 4;   // positions in flight, added in bag order
-                        for (int p0 = s1; p0 < e1; p0 += kMultiU) {
-                            int64_t row[kMultiU];
+                // bags of several indices: fp32 sum in bag order, one rounding
+                if constexpr (kCpr == 8 || kCpr == 16 || kCpr == 32) {
+                    // Their positions form one list in bag order (lane t < F holds
+                    // bag t's count); each lane resolves one of 32 positions at a
+                    // time (coalesced index loads), then every lane adds its H
+                    // halves of each row (all 32 lanes busy on one row), kMultiRows
+                    // rows in flight, and a bag's sum is stored when the next begins.
+                    constexpr int H = kCpr / 4;              // halves of a row per lane: 2, 4 or 8
+                    constexpr int kMultiRows = 16;            // 8: 0.327 / 0.824 ms, 24: spills
+                    const int cnt = (lane < F && row0 == kRowMulti) ? z0 - a0 : 0;
+                    if (__any_sync(0xffffffffu, cnt > 0)) {
+                        int incl = cnt;
 #pragma unroll
-                            for (int u = 0; u < kMultiU; ++u) row[u] = p0 + u < e1 ? __ldg(ga.indices + p0 + u) : -1;
-                            uint4 r[kMultiU];
+                        for (int o = 1; o < kWarp; o <<= 1) {
+                            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        const int excl = incl - cnt;
+                        const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+                        float acc[H];
 #pragma unroll
-                            for (int u = 0; u < kMultiU; ++u) {
-                                int64_t i = row[u];
-                                row[u] = -1;
-                                if (p0 + u < e1) {
-                                    if (ga.hash && n > 0) {
-                                        i %= n;
-                                        if (i < 0) i += n;
-                                        row[u] = base + i;
-                                    } else if (ga.hash || i < 0 || i >= n) {
-                                        set_status(status, DLRM_STATUS_OOB_INDEX);
+                        for (int h = 0; h < H; ++h) acc[h] = 0.f;
+                        int cur = -1;   // bag being summed (warp-uniform)
+                        auto flush = [&](int t) {   // lane's H halves of bag t's row, rounded once
+                            const int row = sm * kSlot + t;
+                            const int c = lane * H / 8;
+                            const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 +
+                                                 (((c & 7) ^ (row & 7)) << 4) + (lane * H * 2) % 16;
+                            uint32_t w[H / 2];
+#pragma unroll
+                            for (int h = 0; h < H / 2; ++h) {
+                                const __half2 x = __floats2half2_rn(acc[2 * h], acc[2 * h + 1]);
+                                w[h] = *reinterpret_cast<const uint32_t*>(&x);
+                            }
+                            if constexpr (H == 8)
+                                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w[0]), "r"(w[1]),
+                                             "r"(w[2]), "r"(w[3])
+                                             : "memory");
+                            else if constexpr (H == 4)
+                                asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(dst), "r"(w[0]), "r"(w[1])
+                                             : "memory");
+                            else
+                                asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(w[0]) : "memory");
+#pragma unroll
+                            for (int h = 0; h < H; ++h) acc[h] = 0.f;
+                        };
+                        for (int q0 = 0; q0 < total; q0 += kWarp) {
+                            const int q = q0 + lane;
+                            int k = 0;   // the last lane whose list offset is at most q: its bag holds q
+#pragma unroll
+                            for (int step = kWarp / 2; step > 0; step >>= 1)
+                                if (__shfl_sync(0xffffffffu, excl, k + step) <= q) k += step;
+                            const int pos = __shfl_sync(0xffffffffu, a0, k) + (q - __shfl_sync(0xffffffffu, excl, k));
+                            const int64_t base = __shfl_sync(0xffffffffu, tbase, k);
+                            const int64_t n = __shfl_sync(0xffffffffu, tn, k);
+                            uint32_t rowq = kRowZero;   // skipped, or past the list
+                            if (q < total) {
+                                int64_t i = __ldg(ga.indices + pos);
+                                if (ga.hash && n > 0) {
+                                    i %= n;
+                                    if (i < 0) i += n;
+                                    rowq = (uint32_t)(base + i);
+                                } else if (ga.hash || i < 0 || i >= n) {
+                                    set_status(status, DLRM_STATUS_OOB_INDEX);
+                                } else {
+                                    rowq = (uint32_t)(base + i);
+                                }
+                            }
+                            const int m = total - q0 < kWarp ? total - q0 : kWarp;
+                            for (int j0 = 0; j0 < m; j0 += kMultiRows) {
+                                uint32_t rj[kMultiRows];
+                                uint32_t v[kMultiRows][H / 2];
+#pragma unroll
+                                for (int u = 0; u < kMultiRows; ++u) {
+                                    rj[u] = __shfl_sync(0xffffffffu, rowq, (j0 + u) & (kWarp - 1));
+                                    const bool ld = j0 + u < m && rj[u] != kRowZero;
+                                    const __half* src = ga.tables + (size_t)(ld ? rj[u] : 0) * D + lane * H;
+                                    if constexpr (H == 8) {
+                                        const uint4 x = ld ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
+                                        v[u][0] = x.x;
+                                        v[u][1] = x.y;
+                                        v[u][2] = x.z;
+                                        v[u][3] = x.w;
+                                    } else if constexpr (H == 4) {
+                                        const uint2 x = ld ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0, 0);
+                                        v[u][0] = x.x;
+                                        v[u][1] = x.y;
                                     } else {
-                                        row[u] = base + i;
+                                        v[u][0] = ld ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
                                     }
                                 }
-                                r[u] = row[u] >= 0 ? ldg_nc_v4(ga.tables + row[u] * D + 8 * c) : make_uint4(0, 0, 0, 0);
-                            }
 #pragma unroll
-                            for (int u = 0; u < kMultiU; ++u)
-                                if (row[u] >= 0) {
-                                    float f[8];
-                                    h8_to_f8(r[u], f);
+                                for (int u = 0; u < kMultiRows; ++u) {
+                                    const int kj = __shfl_sync(0xffffffffu, k, (j0 + u) & (kWarp - 1));
+                                    if (j0 + u >= m) break;
+                                    if (kj != cur) {
+                                        if (cur >= 0) flush(cur);
+                                        cur = kj;
+                                    }
+                                    if (rj[u] != kRowZero) {
 #pragma unroll
-                                    for (int v = 0; v < 8; ++v) acc[v] += f[v];
+                                        for (int h = 0; h < H / 2; ++h) {
+                                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v[u][h]));
+                                            acc[2 * h] += f.x;
+                                            acc[2 * h + 1] += f.y;
+                                        }
+                                    }
                                 }
+                            }
                         }
-                        const uint4 w = f8_to_h8(acc);
-                        const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
-                                     "r"(w.w)
-                                     : "memory");
+                        flush(cur);
+                    }
+                } else {
+                    for (uint32_t multi = __ballot_sync(0xffffffffu, row0 == kRowMulti); multi; multi &= multi - 1) {
+                        const int t = __ffs(multi) - 1;
+                        const int s1 = __shfl_sync(0xffffffffu, a0, t), e1 = __shfl_sync(0xffffffffu, z0, t);
+                        const int64_t base = __shfl_sync(0xffffffffu, tbase, t), n = __shfl_sync(0xffffffffu, tn, t);
+                        const int row = sm * kSlot + t;
+                        for (int c = lane; c < cpr; c += kWarp) {
+                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            constexpr int kMultiU = 4;   // positions in flight, added in bag order
+                            for (int p0 = s1; p0 < e1; p0 += kMultiU) {
+                                int64_t row[kMultiU];
+    #pragma unroll
+                                for (int u = 0; u < kMultiU; ++u) row[u] = p0 + u < e1 ? __ldg(ga.indices + p0 + u) : -1;
+                                uint4 r[kMultiU];
+    #pragma unroll
+                                for (int u = 0; u < kMultiU; ++u) {
+                                    int64_t i = row[u];
+                                    row[u] = -1;
+                                    if (p0 + u < e1) {
+                                        if (ga.hash && n > 0) {
+                                            i %= n;
+                                            if (i < 0) i += n;
+                                            row[u] = base + i;
+                                        } else if (ga.hash || i < 0 || i >= n) {
+                                            set_status(status, DLRM_STATUS_OOB_INDEX);
+                                        } else {
+                                            row[u] = base + i;
+                                        }
+                                    }
+                                    r[u] = row[u] >= 0 ? ldg_nc_v4(ga.tables + row[u] * D + 8 * c) : make_uint4(0, 0, 0, 0);
+                                }
+    #pragma unroll
+                                for (int u = 0; u < kMultiU; ++u)
+                                    if (row[u] >= 0) {
+                                        float f[8];
+                                        h8_to_f8(r[u], f);
+    #pragma unroll
+                                        for (int v = 0; v < 8; ++v) acc[v] += f[v];
+                                    }
+                            }
+                            const uint4 w = f8_to_h8(acc);
+                            const uint32_t dst = sbase + (c >> 3) * kKBlockBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                                         "r"(w.w)
+                                         : "memory");
+                        }
                     }
                 }
                 // generic-proxy writes -> visible to the tensor core, then publish this slot

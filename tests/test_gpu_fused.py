@@ -55,14 +55,20 @@ def test_default_shapes_match_two_calls_and_oracle(cuda_lib, B):
     assert_within_abs_sum(b[samples][:, :W], ro[:, :W], abs_products(c.dense, rp), 2e-2, "fused vs oracle")
 
 
+# "heavy" (4.2 indices per bag) puts several chunks of 32 positions in a
+# sample's list of several-index bags
+BAG_MIX = {"ragged": [0, 1, 1, 1, 2, 5], "heavy": [0, 1, 2, 5, 9, 8]}
+
+
+@pytest.mark.parametrize("mix", sorted(BAG_MIX))
 @pytest.mark.parametrize("F,D", [(1, 64), (3, 128), (26, 64), (31, 192), (32, 256), (32, 128)])
-def test_shapes_with_ragged_bags_hashing_and_skips(cuda_lib, F, D):
+def test_shapes_with_ragged_bags_hashing_and_skips(cuda_lib, F, D, mix):
     rng = np.random.default_rng(F * 7 + D)
     B = 37
     rows = rng.integers(1, 50, size=F)
     row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
     tab = to_dev(rng.standard_normal((row_base[-1], D)).astype(np.float16))
-    counts = rng.choice([0, 1, 1, 1, 2, 5], size=F * B)
+    counts = rng.choice(BAG_MIX[mix], size=F * B)
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     idx = rng.integers(-60, 60, size=off[-1]).astype(np.int32)
     dense = to_dev(rng.standard_normal((B, D)).astype(np.float16))
