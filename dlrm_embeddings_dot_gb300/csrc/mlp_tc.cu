@@ -182,12 +182,9 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 #pragma unroll
                 for (int j = 0; j < NC / 4; ++j) {
                     const float4 bb = __ldg(bq + j);
-                    const float a0 = fmaxf(__uint_as_float(v[4 * j]) + bb.x, 0.f);
-                    const float a1 = fmaxf(__uint_as_float(v[4 * j + 1]) + bb.y, 0.f);
-                    const float a2 = fmaxf(__uint_as_float(v[4 * j + 2]) + bb.z, 0.f);
-                    const float a3 = fmaxf(__uint_as_float(v[4 * j + 3]) + bb.w, 0.f);
-                    h[2 * j] = h2_bits(a0, a1);
-                    h[2 * j + 1] = h2_bits(a2, a3);
+                    h[2 * j] = h2_relu_bits(__uint_as_float(v[4 * j]) + bb.x, __uint_as_float(v[4 * j + 1]) + bb.y);
+                    h[2 * j + 1] =
+                        h2_relu_bits(__uint_as_float(v[4 * j + 2]) + bb.z, __uint_as_float(v[4 * j + 3]) + bb.w);
                 }
                 uint8_t* sb = myout + (k & 1) * (32 * 64);
                 if (lane == 0) bulk_wait_read<1>();           // the store that last used this buffer has read it
@@ -226,6 +223,402 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(tmem_cols)
                      : "memory");
+    }
+    if (threadIdx.x == 0 && *abort_flag) set_status(status, DLRM_STATUS_TIMEOUT);
+}
+
+// ----------------------------------------------------------- fused 3 layers
+// The pages' bottom MLP, 16 (13 padded) -> 512 -> 256 -> 128, in one
+// persistent launch: a CTA per SM walks 128-row tiles and keeps each tile's
+// activations on chip, so only x goes in and the 128-wide output comes out.
+//   TMEM (512 columns): layer 1 in two 256-column halves (columns 0..255 and
+//   256..511), layer 2's accumulator in columns 0..255 once the first half is
+//   drained, layer 3's in 256..383 once the second half is.
+//   Shared memory: the x tile and W1 (resident), both as 32-byte rows (one
+//   16-wide K step, 32-byte swizzle); four 16 KB activation slots (one 64-wide
+//   K block of 128 rows each, 128-byte swizzled as the MMA reads them), which
+//   hold layer 1's output blocks 0-3, then 4-7, then layer 2's output blocks
+//   0-3, and last the output staging; a ring of 32 KB weight stages fed by TMA
+//   in the order the MMAs use them (W2's eight K blocks, W3's four); the
+//   biases.
+//   warp 0      producer: builds each x tile from the fp32 input (coalesced
+//               loads of the tile's contiguous rows, rounded to fp16 into the
+//               32-byte-swizzled layout), TMA loads of the weights
+//   warp 1      TMEM allocation and MMA issue
+//   warps 2..17 epilogue: drain TMEM (four warps per lane quarter, each two
+//               of a layer's eight 32-column slices with both loads in
+//               flight), + bias, ReLU, fp16 into the next layer's slots or,
+//               for layer 3 (one slice each), through a staging buffer in the
+//               slots out by TMA store
+// Each slot is filled three times per tile (use u = 0, 1, 2: layer 1 blocks
+// 0-3, 4-7, layer 2 blocks 0-3) by the 8 warps that own its two 32-column
+// slices, each slot published as soon as it is written, so the next layer's
+// MMAs start on block 0 while blocks 1-3 are still being converted; its
+// full/empty barriers alternate phase with every use.  Accumulator columns are
+// reused only after every warp has read them: layer 2 (columns 0..255) waits
+// for all 16 warps' loads of layer 1's first half (lread); layer 3 (256..383)
+// follows layer 2, which needs all of layer 1's second half published; the
+// next tile's layer 1 waits for the drains of layers 2 and 3 (tlo, thi).
+constexpr int kF3K0 = 16, kF3N1 = 512, kF3N2 = 256, kF3N3 = 128;
+constexpr int kF3Epi = 16;                           // epilogue warps, four per TMEM lane quarter
+constexpr int kF3Threads = (2 + kF3Epi) * 32;
+constexpr int kF3Stages = 4;
+constexpr int kF3StageBytes = 256 * 128;             // a {64, 256} fp16 box
+constexpr int kF3SlotBytes = kBM * 128;              // a {64, 128} fp16 box
+constexpr int kF3XOff = 0;                           // x tile: 128 rows x 32 bytes
+constexpr int kF3W1Off = kF3XOff + kBM * 32;         // W1: 512 rows x 32 bytes
+constexpr int kF3SlotOff = kF3W1Off + kF3N1 * 32;
+constexpr int kF3RingOff = kF3SlotOff + 4 * kF3SlotBytes;
+constexpr int kF3BiasOff = kF3RingOff + kF3Stages * kF3StageBytes;   // the three biases, fp32
+constexpr int kF3BarOff = kF3BiasOff + (kF3N1 + kF3N2 + kF3N3) * 4;
+static_assert(kF3Epi * 2 * 32 * 64 <= 4 * kF3SlotBytes, "output staging must fit the slots");
+// barriers: xfull, xempty, w1full, full[S], empty[S], sfull[4], sempty[4], l1a, l1b, l2, l3, tlo, thi,
+// drain, lread, oread
+constexpr int kF3Bars = 3 + 2 * kF3Stages + 8 + 9;
+constexpr size_t kF3Smem = 1024 + kF3BarOff + kF3Bars * 8 + 16;
+
+__global__ void __launch_bounds__(kF3Threads, 1)
+mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ CUtensorMap map_w1,
+                  const __grid_constant__ CUtensorMap map_w2, const __grid_constant__ CUtensorMap map_w3,
+                  const __grid_constant__ CUtensorMap map_out, const float* __restrict__ b1,
+                  const float* __restrict__ b2, const float* __restrict__ b3, int M, uint32_t* status,
+                  long long wait_cycles)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* xs = smem + kF3XOff;
+    uint8_t* w1s = smem + kF3W1Off;
+    uint8_t* slots = smem + kF3SlotOff;
+    uint8_t* ring = smem + kF3RingOff;
+    float* bias_s = reinterpret_cast<float*>(smem + kF3BiasOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF3BarOff);
+    uint64_t* xfull = bars;
+    uint64_t* xempty = bars + 1;
+    uint64_t* w1full = bars + 2;
+    uint64_t* full = bars + 3;
+    uint64_t* empty = full + kF3Stages;
+    uint64_t* sfull = empty + kF3Stages;
+    uint64_t* sempty = sfull + 4;
+    uint64_t* l1a = sempty + 4;
+    uint64_t* l1b = l1a + 1;
+    uint64_t* l2 = l1a + 2;
+    uint64_t* l3 = l1a + 3;
+    uint64_t* tlo = l1a + 4;      // layer-2 accumulator drained: columns 0..255 free
+    uint64_t* thi = l1a + 5;      // layer-3 accumulator drained: columns 256..511 free
+    uint64_t* drain = l1a + 6;    // abort: the MMAs issued so far are complete
+    uint64_t* lread = l1a + 7;    // every warp has loaded its part of layer 1's first half
+    uint64_t* oread = l1a + 8;    // the output stores have read the staging in the slots
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kF3Bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int tiles = (M + kBM - 1) / kBM;
+
+    if (threadIdx.x == 0) {
+        mbar_init(xfull, 1);   // the producer warp's arrival once the tile is built
+        mbar_init(xempty, 1);
+        mbar_init(w1full, 1);
+        for (int i = 0; i < kF3Stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sfull[i], kF3Epi / 2);
+            mbar_init(&sempty[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(&l1a[i], 1);
+        mbar_init(tlo, kF3Epi);
+        mbar_init(thi, kF3Epi);
+        mbar_init(drain, 1);
+        mbar_init(lread, kF3Epi);
+        mbar_init(oread, kF3Epi);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // everything above touches no global memory: it overlaps the previous kernel's tail
+    pdl_wait_and_release();
+    // the biases, read by the epilogue from shared memory (broadcast loads); the
+    // x tile's pad columns stay zero
+    for (int i = threadIdx.x; i < kBM * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(xs)[i] = 0u;
+    for (int i = threadIdx.x; i < kF3N1 + kF3N2 + kF3N3; i += blockDim.x)
+        bias_s[i] = i < kF3N1 ? b1[i] : (i < kF3N1 + kF3N2 ? b2[i - kF3N1] : b3[i - kF3N1 - kF3N2]);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // -------------------------------------------------------------- producer
+        int q = 0, it = 0;   // ring loads, tiles
+        bool ok = true;
+        auto ring_load = [&](const CUtensorMap* map, int c0, int c1, uint32_t bytes) {
+            const int st = q % kF3Stages;
+            if (!mbar_wait(&empty[st], ((uint32_t)(q / kF3Stages) & 1u) ^ 1u, abort_flag, wait_cycles)) return false;
+            mbar_expect_tx(&full[st], bytes);
+            tma_load_2d(ring + (size_t)st * kF3StageBytes, map, c0, c1, &full[st]);
+            ++q;
+            return true;
+        };
+        if (lane == 0 && blockIdx.x < tiles) {   // W1 stays resident
+            mbar_expect_tx(w1full, kF3N1 * 32);
+            tma_load_2d(w1s, &map_w1, 0, 0, w1full);
+            tma_load_2d(w1s + 256 * 32, &map_w1, 0, 256, w1full);
+        }
+        const int64_t xn = (int64_t)M * K0;
+        for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
+            // x tile t: rows m0.. are one contiguous run of fp32; element i of it is
+            // row i / K0, column i % K0, stored as a half at its swizzled place
+            int w = 1;
+            if (lane == 0) w = mbar_wait(xempty, ((uint32_t)it & 1u) ^ 1u, abort_flag, wait_cycles);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            // 128 K0 floats = 32 K0 16-byte words: lane l takes words l + 32 u, u < K0,
+            // eight loads in flight at a time
+            const int64_t base = (int64_t)t * kBM * K0;
+            const float4* x4 = reinterpret_cast<const float4*>(x + base);
+            for (int u0 = 0; u0 < K0; u0 += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t i = base + 4 * (lane + kWarp * (u0 + u));
+                    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (u0 + u < K0) {
+                        if (i + 4 <= xn) {
+                            v[u] = __ldg(x4 + lane + kWarp * (u0 + u));
+                        } else if (i < xn) {   // the input's last, partial word
+                            v[u].x = x[i];
+                            if (i + 1 < xn) v[u].y = x[i + 1];
+                            if (i + 2 < xn) v[u].z = x[i + 2];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (u0 + u >= K0) break;
+                    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * (lane + kWarp * (u0 + u)) + e;
+                        const int r = i / K0, c = i - r * K0;
+                        const uint32_t off = (uint32_t)r * 32 + ((uint32_t)((c >> 3) ^ ((r >> 2) & 1)) << 4) +
+                                             (uint32_t)(c & 7) * 2;
+                        *reinterpret_cast<__half*>(xs + off) = __float2half_rn(f[e]);
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> the MMA
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(xfull);
+                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) ok = ring_load(&map_w2, kb * kKB, 0, kF3StageBytes);
+                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) ok = ring_load(&map_w3, kb * kKB, 0, kF3N3 * 128);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && *abort_flag) {   // the copies already issued must land before the CTA exits
+            for (int j = (q > kF3Stages ? q - kF3Stages : 0); j < q; ++j)
+                mbar_drain(&full[j % kF3Stages], (uint32_t)(j / kF3Stages) & 1u);
+            if (blockIdx.x < tiles) mbar_drain(w1full, 0);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------------------------------------------- MMA issuer
+            int q = 0, it = 0;
+            bool ok = true, issued = false;
+            const uint32_t id256 = idesc_f16(kBM, 256), id128 = idesc_f16(kBM, 128);
+            auto ring_wait = [&]() -> int {
+                const int st = q % kF3Stages;
+                if (!mbar_wait(&full[st], (uint32_t)(q / kF3Stages) & 1u, abort_flag, wait_cycles)) return -1;
+                tc_fence_after();
+                return st;
+            };
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
+                const uint32_t par = (uint32_t)it & 1u;
+                // layer 1, columns 0..255 (after the previous tile's layer 2 is drained)
+                if ((it == 0 && !mbar_wait(w1full, 0, abort_flag, wait_cycles)) ||
+                    !mbar_wait(xfull, par, abort_flag, wait_cycles) || !mbar_wait(tlo, par ^ 1u, abort_flag, wait_cycles))
+                    break;
+                tc_fence_after();
+                const uint64_t xd = sw32_desc(smem_u32(xs));
+                tc_mma_f16(tmem_base, xd, sw32_desc(smem_u32(w1s)), id256, 0);
+                issued = true;
+                tc_commit(l1a);
+                // layer 1, columns 256..511 (after the previous tile's layer 3 is drained)
+                if (!mbar_wait(thi, par ^ 1u, abort_flag, wait_cycles)) break;
+                tc_fence_after();
+                tc_mma_f16(tmem_base + 256, xd, sw32_desc(smem_u32(w1s + 256 * 32)), id256, 0);
+                tc_commit(xempty);
+                tc_commit(l1b);
+                int st;
+                // layer 2: K blocks 0..7 from slots kb % 4 (uses 0 and 1)
+                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) {
+                    const int s = kb & 3;
+                    const uint32_t g = 3u * (uint32_t)it + (uint32_t)(kb >> 2);
+                    if ((kb == 0 && !mbar_wait(lread, par, abort_flag, wait_cycles)) ||
+                        !mbar_wait(&sfull[s], g & 1u, abort_flag, wait_cycles) || (st = ring_wait()) < 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_u32(slots + (size_t)s * kF3SlotBytes);
+                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
+                    for (int kk = 0; kk < kKB / 16; ++kk)
+                        tc_mma_f16(tmem_base, sw128_desc(sa + kk * 32), sw128_desc(wa + kk * 32), id256,
+                                   (kb | kk) != 0);
+                    tc_commit(&empty[st]);
+                    tc_commit(&sempty[s]);
+                    ++q;
+                }
+                if (!ok) break;
+                tc_commit(l2);
+                // layer 3: K blocks 0..3 from slots 0..3 (use 2), accumulator columns 256..383
+                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) {
+                    const uint32_t g = 3u * (uint32_t)it + 2u;
+                    if (!mbar_wait(&sfull[kb], g & 1u, abort_flag, wait_cycles) || (st = ring_wait()) < 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_u32(slots + (size_t)kb * kF3SlotBytes);
+                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
+                    for (int kk = 0; kk < kKB / 16; ++kk)
+                        tc_mma_f16(tmem_base + 256, sw128_desc(sa + kk * 32), sw128_desc(wa + kk * 32), id128,
+                                   (kb | kk) != 0);
+                    tc_commit(&empty[st]);
+                    tc_commit(&sempty[kb]);
+                    ++q;
+                }
+                if (!ok) break;
+                tc_commit(l3);
+            }
+            if (*abort_flag && issued) {   // MMAs already issued must finish before TMEM is freed
+                tc_commit(drain);
+                mbar_drain(drain, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int sub = (warp - 2) / 4;                         // 0..3 among the quarter's warps
+        const int r = 32 * quarter + lane;                       // tile row = TMEM lane
+        const uint32_t trow = tmem_base + ((uint32_t)(32 * quarter) << 16);
+        const int xs64 = (lane >> 1) & 3;                       // 64-byte swizzle of the output staging
+        uint8_t* myout = slots + (size_t)(warp - 2) * (2 * 32 * 64);   // output staging, after layer 3
+        // accumulator v (32 columns) + bias, ReLU -> 16 words of halves
+        auto finish32 = [&](const uint32_t (&v)[32], const float* bias, uint32_t (&h)[16]) {
+            const float4* bq = reinterpret_cast<const float4*>(bias);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 bb = bq[j];
+                h[2 * j] = h2_relu_bits(__uint_as_float(v[4 * j]) + bb.x, __uint_as_float(v[4 * j + 1]) + bb.y);
+                h[2 * j + 1] =
+                    h2_relu_bits(__uint_as_float(v[4 * j + 2]) + bb.z, __uint_as_float(v[4 * j + 3]) + bb.w);
+            }
+        };
+        // 32-column slice j (halves [32 (j & 1), +32) of K block j / 2), row r of slot j / 2
+        auto put_slot = [&](int j, const uint32_t (&h)[16]) {
+            const uint32_t base = smem_u32(slots + (size_t)(j >> 1) * kF3SlotBytes) + (uint32_t)r * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t dst = base + ((uint32_t)((4 * (j & 1) + q) ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[4 * q]), "r"(h[4 * q + 1]),
+                             "r"(h[4 * q + 2]), "r"(h[4 * q + 3])
+                             : "memory");
+            }
+        };
+        // one layer's 256 columns (from TMEM column tcol0) -> slots 0..3 for use g: this
+        // warp's slices sub and sub + 4, both TMEM loads in flight; then publish
+        auto fill_slots = [&](uint32_t tcol0, const float* bias, uint32_t g) {
+            // the first use of a tile reuses the previous tile's output staging
+            if (g % 3u == 0 && !mbar_wait(oread, ((g / 3u) & 1u) ^ 1u, abort_flag, wait_cycles)) return false;
+            const int j0 = sub, j1 = sub + 4;                   // slots sub / 2, then 2 + sub / 2
+            uint32_t v0[32], v1[32];
+            tmem_ld_x32(trow + tcol0 + (uint32_t)(32 * j0), v0);
+            tmem_ld_x32(trow + tcol0 + (uint32_t)(32 * j1), v1);
+            tmem_wait_ld2(v0, v1);
+            if (g % 3u == 0) {   // layer 1's first half read: layer 2 may take its columns
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(lread);
+            }
+            // one slice into its slot, then publish the slot (this warp's share of it)
+            auto put = [&](int j, const uint32_t (&v)[32]) {
+                if (!mbar_wait(&sempty[j >> 1], (g & 1u) ^ 1u, abort_flag, wait_cycles)) return false;
+                uint32_t h[16];
+                finish32(v, bias + 32 * j, h);
+                put_slot(j, h);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> the MMAs
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfull[j >> 1]);
+                return true;
+            };
+            return put(j0, v0) && put(j1, v1);
+        };
+        int it = 0, k = 0;                                      // k: output slices of this warp (buffer k & 1)
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            const uint32_t par = (uint32_t)it & 1u;
+            const int m0 = t * kBM;
+            if (!mbar_wait(l1a, par, abort_flag, wait_cycles)) break;
+            __syncwarp();
+            tc_fence_after();
+            if (!fill_slots(0, bias_s, 3u * it)) break;
+            if (!mbar_wait(l1b, par, abort_flag, wait_cycles)) break;
+            __syncwarp();
+            tc_fence_after();
+            if (!fill_slots(256, bias_s + 256, 3u * it + 1u)) break;
+            if (!mbar_wait(l2, par, abort_flag, wait_cycles)) break;
+            __syncwarp();
+            tc_fence_after();
+            if (!fill_slots(0, bias_s + kF3N1, 3u * it + 2u)) break;
+            tc_fence_before();   // layer 2's columns read: the next tile's layer 1 may take them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tlo);
+            if (!mbar_wait(l3, par, abort_flag, wait_cycles)) break;
+            __syncwarp();
+            tc_fence_after();
+            {
+                const int c0 = 32 * sub;                         // layer 3: one 32-column slice per warp
+                uint32_t v[32], h[16];
+                tmem_ld_x32(trow + 256 + (uint32_t)c0, v);
+                tmem_wait_ld(v);
+                tc_fence_before();   // layer 3's columns read: the next tile's layer 1 may take them
+                __syncwarp();
+                if (lane == 0) mbar_arrive(thi);
+                finish32(v, bias_s + kF3N1 + kF3N2 + c0, h);
+                uint8_t* sb = myout + (k & 1) * (32 * 64);
+                if (lane == 0) bulk_wait_read<1>();           // the store that last used this buffer has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t dst = smem_u32(sb + lane * 64 + ((j ^ xs64) << 4));
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[4 * j]), "r"(h[4 * j + 1]),
+                                 "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {   // rows past M are clipped by the tensor store
+                    tma_store_2d(&map_out, c0, m0 + 32 * quarter, sb);
+                    bulk_commit();
+                    bulk_wait_read<0>();   // the staging may be overwritten by the next tile
+                    mbar_arrive(oread);
+                }
+                ++k;
+            }
+        }
+        if (lane == 0) bulk_wait_all();   // this warp's stores are complete before the CTA exits
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, DLRM_STATUS_TIMEOUT);
 }
@@ -293,6 +686,59 @@ dlrm_status launch_layer(const __half* a, int lda, const __half* w, const float*
                             "mlp_layer_kernel");
 }
 
+// The pages' 13 -> 512 -> 256 -> 128 shape (x padded to 16 columns) runs fused.
+bool fused3_shape(int n_layers, const int* dims)
+{
+    return n_layers == 3 && round_up8(dims[0]) == kF3K0 && dims[1] == kF3N1 && dims[2] == kF3N2 && dims[3] == kF3N3;
+}
+
+dlrm_status launch_fused3(const float* x, int K0, const __half* w, const float* bias, __half* out, int M,
+                          uint32_t* status, cudaStream_t st)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(DLRM_ERR_CUDA, "dlrm_bottom_mlp_fwd: cuTensorMapEncodeTiled unavailable");
+    const cuuint32_t ones[2] = {1, 1};
+    // K-major fp16 operand [rows][cols], {64, box_rows} boxes, 128-byte swizzle
+    auto operand = [&](CUtensorMap* m, const __half* p, int cols, int rows, int box_rows) {
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kKB, (cuuint32_t)box_rows};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p), dims, str, box, ones,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    const __half* w1 = w;
+    const __half* w2 = w1 + (size_t)kF3N1 * kF3K0;
+    const __half* w3 = w2 + (size_t)kF3N2 * kF3N1;
+    // 16-wide K operands: {16, box_rows} boxes of 32-byte rows, 32-byte swizzle
+    auto narrow = [&](CUtensorMap* m, const __half* p, int rows, int box_rows) {
+        const cuuint64_t dims[2] = {(cuuint64_t)kF3K0, (cuuint64_t)rows};
+        const cuuint64_t str[1] = {(cuuint64_t)kF3K0 * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kF3K0, (cuuint32_t)box_rows};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p), dims, str, box, ones,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    CUtensorMap m1, m2, m3, mo;
+    CUresult r = narrow(&m1, w1, kF3N1, 256);
+    if (r == CUDA_SUCCESS) r = operand(&m2, w2, kF3N1, kF3N2, 256);
+    if (r == CUDA_SUCCESS) r = operand(&m3, w3, kF3N2, kF3N3, kF3N3);
+    if (r != CUDA_SUCCESS) return fail(DLRM_ERR_CUDA, "dlrm_bottom_mlp_fwd: operand tensor map (%d)", (int)r);
+    const cuuint64_t odims[2] = {(cuuint64_t)kF3N3, (cuuint64_t)M};
+    const cuuint64_t ostr[1] = {(cuuint64_t)kF3N3 * 2};
+    const cuuint32_t obox[2] = {32, 32};
+    r = enc(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, out, odims, ostr, obox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DLRM_ERR_CUDA, "dlrm_bottom_mlp_fwd: output tensor map (%d)", (int)r);
+    const int tiles = (M + kBM - 1) / kBM;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    cudaError_t e = cudaFuncSetAttribute(mlp3_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kF3Smem);
+    if (e != cudaSuccess) return fail(DLRM_ERR_CUDA, "dlrm_bottom_mlp_fwd: %s", cudaGetErrorString(e));
+    return check_launch_pdl(launch_pdl(mlp3_fused_kernel, grid, kF3Threads, kF3Smem, st, x, K0, m1, m2, m3, mo, bias,
+                                       bias + kF3N1, bias + kF3N1 + kF3N2, M, status, wait_limit_cycles()),
+                            "mlp3_fused_kernel");
+}
+
 // Workspace: x as fp16 [B][round_up8(dims[0])], then each hidden layer's
 // output [B][dims[l+1]], l = 0..n_layers-2, each piece 256-byte aligned.
 bool mlp_dims_ok(int B, int n_layers, const int* dims)
@@ -338,6 +784,9 @@ extern "C" dlrm_status dlrm_bottom_mlp_fwd(const float* d_x, int B, int n_layers
     if (ws_bytes < need)
         return fail(DLRM_ERR_WORKSPACE, "dlrm_bottom_mlp_fwd: workspace %zu bytes < %zu", ws_bytes, need);
     cudaStream_t st = as_stream(stream);
+    if (fused3_shape(n_layers, dims))
+        return launch_fused3(d_x, dims[0], static_cast<const __half*>(d_weights), d_biases,
+                             static_cast<__half*>(d_out), B, d_status, st);
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     const int Kp0 = round_up8(dims[0]);
     __half* x16 = reinterpret_cast<__half*>(ws);

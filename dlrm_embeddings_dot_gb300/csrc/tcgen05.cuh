@@ -211,6 +211,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor: K-major, 32-byte swizzle (rows of 16
+// fp16 elements, one K step), 8-row groups 256 bytes apart.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(256 >> 4) << 32;        // stride byte offset
+    d |= (uint64_t)1 << 46;                 // version
+    d |= (uint64_t)6 << 61;                 // SWIZZLE_32B
+    return d;
+}
+
 // Shared-memory descriptor, 128-byte swizzle, explicit byte offsets.  For an
 // MN-major operand (M or N contiguous) the leading offset is the stride
 // between 64-element blocks along M/N and the stride offset the stride
@@ -295,11 +307,37 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32])
         : "memory");
 }
 
+// tcgen05.wait::ld tied to two sets of 32 loaded registers (two loads in flight).
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r)[32], uint32_t (&u)[32])
+{
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+          "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+          "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
+          "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]), "+r"(u[6]), "+r"(u[7]),
+          "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]), "+r"(u[12]), "+r"(u[13]), "+r"(u[14]), "+r"(u[15]),
+          "+r"(u[16]), "+r"(u[17]), "+r"(u[18]), "+r"(u[19]), "+r"(u[20]), "+r"(u[21]), "+r"(u[22]), "+r"(u[23]),
+          "+r"(u[24]), "+r"(u[25]), "+r"(u[26]), "+r"(u[27]), "+r"(u[28]), "+r"(u[29]), "+r"(u[30]), "+r"(u[31])
+        :
+        : "memory");
+}
+
 // Two floats as one word of round-to-nearest halves (a in the low half).
 __device__ __forceinline__ uint32_t h2_bits(float a, float b)
 {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// relu(a), relu(b) rounded to nearest halves in one conversion (a in the low
+// half); the same bits as rounding fmaxf(x, 0) for every number.
+__device__ __forceinline__ uint32_t h2_relu_bits(float a, float b)
+{
+    uint32_t r;
+    asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
 }
 
 // instruction descriptor, kind::f16: D = f32, A = B = f16, both K-major

@@ -30,7 +30,10 @@ extern "C" {
 
 /* Bytes of device workspace dlrm_bottom_mlp_fwd needs for a batch of B and
  * the host array dims[0..n_layers] (0 for invalid arguments): the fp16 copy
- * of x padded to a multiple of 8 columns plus every hidden activation. */
+ * of x padded to a multiple of 8 columns plus every hidden activation.  The
+ * pages' shape (dims[0] <= 16, then 512, 256, 128) runs as one fused launch
+ * that reads x directly and keeps the hidden activations on chip: there the
+ * workspace is not touched (the size query still counts it). */
 size_t dlrm_bottom_mlp_workspace_size(int B, int n_layers, const int* dims);
 
 /* x: fp32 [B][dims[0]].  d_weights: fp16, the layers one after another,

@@ -68,13 +68,29 @@ def _check(x, dims, W, b, acts, out):
     assert np.all(np.abs(out.astype(np.float64) - ref) <= 2.0**-8 * chain)
 
 
-@pytest.mark.parametrize("B", [1, 300, 4096])
+def _run_layer_by_layer(dl, x, dims, W, b):
+    """The same chain as one call per layer (the per-layer kernel, each layer's
+    fp16 output passed on as fp32, which the next call rounds back exactly)."""
+    h, acts = x, []
+    for l in range(len(W)):
+        a, o = _run(dl, h, [h.shape[1], dims[l + 1]], [W[l]], [b[l]])
+        acts.append(a[0])
+        h = o.astype(np.float32)
+    return acts, o
+
+
+@pytest.mark.parametrize("B", [1, 300, 4096, 4097])
 def test_default_bottom_mlp(cuda_lib, B):
+    """The pages' 13-512-256-128 shape runs as one fused launch whose hidden
+    activations stay on chip: its output equals the layer-by-layer chain bit for
+    bit, and that chain is checked layer by layer against the oracle."""
     dims = [13, 512, 256, 128]
     x = np.random.default_rng(B).lognormal(0.0, 1.0, size=(B, 13)).astype(np.float32)
     W, b = inputs.mlp_layers(dims, seed=0)
-    acts, out = _run(cuda_lib, x, dims, W, b)
-    _check(x, dims, W, b, acts, out)
+    _, out = _run(cuda_lib, x, dims, W, b)
+    lacts, lout = _run_layer_by_layer(cuda_lib, x, dims, W, b)
+    assert np.array_equal(out.view(np.uint16), lout.view(np.uint16)), "fused chain differs from the per-layer one"
+    _check(x, dims, W, b, lacts, lout)
     assert (out > 0).any() and (out == 0).any()
 
 
@@ -96,6 +112,8 @@ def test_full_batch_sampled_rows(cuda_lib):
     x = np.random.default_rng(7).lognormal(0.0, 1.0, size=(B, 13)).astype(np.float32)
     W, b = inputs.mlp_layers(dims, seed=0)
     _, out = _run(cuda_lib, x, dims, W, b)
+    _, lout = _run_layer_by_layer(cuda_lib, x, dims, W, b)
+    assert np.array_equal(out.view(np.uint16), lout.view(np.uint16)), "fused chain differs from the per-layer one"
     rows = np.unique(np.concatenate([np.random.default_rng(8).choice(B, 64, replace=False), [0, B - 1]]))
     ref = oracle.mlp_fwd(x[rows], [w.astype(np.float32) for w in W], b, half_io=True)
     chain = np.abs(x[rows].astype(np.float16).astype(np.float64))
