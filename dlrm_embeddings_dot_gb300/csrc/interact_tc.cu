@@ -26,10 +26,13 @@
 //               into a shared output row, coalesced 16-byte stores.
 // Fused variant (dlrm_emb_interact_fwd, inference): each sample slot of a
 // tile is filled by one gather warp straight from the table, so the pooled
-// tensor never goes to HBM.  Eight gather warps (warp 0 and warps 6..12, in
-// teams of four) fill two tiles at once with 16-byte register loads: a table
-// row is only 256 bytes, and the TMA engine's rate for such small row
-// gathers (tile::gather4) is several times below what the warps reach.
+// tensor never goes to HBM.  Twelve gather warps (warp 0 and warps 6..16, in
+// teams of four) fill three tiles at once with 16-byte register loads, eight
+// in flight per lane: a table row is only 256 bytes, and the TMA engine's
+// rate for such small row gathers (tile::gather4) is several times below
+// what the warps reach.  (At 64K: two teams with 13 loads in flight 0.1169
+// ms, three with 8 0.1102, four with 8 0.1113; 10 or more with three teams
+// spill.)
 // Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 overlap the
 // epilogue of tile i.  Every mbarrier wait is bounded; on timeout the kernel
 // sets DLRM_STATUS_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -55,9 +58,9 @@ constexpr int kKBlockBytes = kEBytes + kDBytes;   // 18 KB (multiple of 1 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;
 constexpr int kThreads = 192;
-constexpr int kTeams = 2;                         // fused: tiles gathered at once, four warps each
+constexpr int kTeams = 3;                         // fused: tiles gathered at once, four warps each
 constexpr int kThreadsFused = (5 + kGroup * kTeams) * 32;   // + gather warps 6.. (warp 0 gathers too)
-constexpr int kGatherU = 13;                      // fused: 16-byte row loads in flight per lane
+constexpr int kGatherU = 8;                       // fused: 16-byte row loads in flight per lane
 constexpr int kMaxStages = 8;
 constexpr int kFusedStages = 4;
 constexpr int kSqRow = 17;                        // words per row of the epilogue's product square

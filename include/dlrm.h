@@ -157,9 +157,10 @@ dlrm_status dlrm_interact_fwd_cuda_core(const void* d_dense, const void* d_poole
  *         D + 32 * ceil(F(F+1)/2 / 32) (480 for F = 26) (CUDA-core kernel);
  * with 16-byte aligned tables, dense and out; otherwise DLRM_ERR_UNSUPPORTED
  * (use the two calls).  Status bits as in dlrm_emb_fwd, plus
- * DLRM_STATUS_TIMEOUT.  One pass is faster than the two calls up to about
- * three indices per bag on average; past that the two calls (which need a
- * pooled buffer) are, with the same bits.
+ * DLRM_STATUS_TIMEOUT.  On 1e6-row tables the fp16 pass beats the two calls
+ * at 1 to 4 indices per bag (measured); the fp32 pass up to about three,
+ * past which the two calls (which need a pooled buffer) are faster, with the
+ * same bits.
  */
 dlrm_status dlrm_emb_interact_fwd(const void* d_tables, dlrm_dtype dtype, const int64_t* d_row_base,
                                   int F, int D, int B, const int32_t* d_indices,
