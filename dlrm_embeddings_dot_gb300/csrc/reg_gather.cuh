@@ -176,8 +176,12 @@ struct BagLanes {
             // of position j's row into slot j % kRing, one commit group per
             // position (empty past the list), so that waiting for all but the
             // kRing - 1 newest groups completes position j, and reads it back.
-            // The positions stream across chunks of 32: the next chunk's
-            // indices are resolved while this chunk's rows are in flight.
+            // Every slot access is by the lane that owns the column, so no
+            // other lane is involved; a slot is refilled only after the lane's
+            // read of it was issued, and the copy writes it only once its
+            // global load returns.  The positions stream across chunks of 32:
+            // the next chunk's indices are resolved while this chunk's rows
+            // are in flight.
             static_assert(kRing <= kWarp, "the ring reaches at most one chunk ahead");
             int kc, kn = 0;
             uint32_t rc, rn = kRowZero;
