@@ -79,13 +79,14 @@ def _run_layer_by_layer(dl, x, dims, W, b):
     return acts, o
 
 
-@pytest.mark.parametrize("B", [1, 300, 4096, 4097])
-def test_default_bottom_mlp(cuda_lib, B):
-    """The pages' 13-512-256-128 shape runs as one fused launch whose hidden
-    activations stay on chip: its output equals the layer-by-layer chain bit for
-    bit, and that chain is checked layer by layer against the oracle."""
-    dims = [13, 512, 256, 128]
-    x = np.random.default_rng(B).lognormal(0.0, 1.0, size=(B, 13)).astype(np.float32)
+@pytest.mark.parametrize("K0,B", [(13, 1), (13, 300), (13, 4096), (13, 4097), (16, 333), (9, 515)])
+def test_default_bottom_mlp(cuda_lib, K0, B):
+    """The pages' 13-512-256-128 shape (and any 9..16 inputs before the same
+    layers) runs as one fused launch whose hidden activations stay on chip: its
+    output equals the layer-by-layer chain bit for bit, and that chain is
+    checked layer by layer against the oracle."""
+    dims = [K0, 512, 256, 128]
+    x = np.random.default_rng(B).lognormal(0.0, 1.0, size=(B, K0)).astype(np.float32)
     W, b = inputs.mlp_layers(dims, seed=0)
     _, out = _run(cuda_lib, x, dims, W, b)
     lacts, lout = _run_layer_by_layer(cuda_lib, x, dims, W, b)
