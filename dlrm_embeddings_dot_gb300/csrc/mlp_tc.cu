@@ -228,53 +228,48 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 }
 
 // ----------------------------------------------------------- fused 3 layers
-// The pages' bottom MLP, 16 (13 padded) -> 512 -> 256 -> 128, in one
-// persistent launch: a CTA per SM walks 128-row tiles and keeps each tile's
-// activations on chip, so only x goes in and the 128-wide output comes out.
-//   TMEM (512 columns): layer 1 in two 256-column halves (columns 0..255 and
-//   256..511), layer 2's accumulator in columns 0..255 once the first half is
-//   drained, layer 3's in 256..383 once the second half is.
+// The pages' bottom MLP, 16 (9..16 padded) -> 512 -> 256 -> 128, in one
+// persistent launch: a CTA per SM walks 128-row tiles, and each tile's
+// activations live in tensor memory, where the next layer's MMA reads them as
+// its A operand, so only x goes in and the 128-wide output comes out.
+//   TMEM (512 columns): an fp32 accumulator in columns 0..255 and the fp16
+//   activations packed two to a column in 256..511.  Layer 1 runs as two
+//   N = 256 halves into 0..255, each converted (bias, ReLU, fp16) into A2 at
+//   256..383 and 384..511; layer 2 (K = 512 from A2) accumulates into 0..255
+//   and is converted into A3 at 256..383; layer 3 (K = 256 from A3) accumulates
+//   into 384..511 and leaves through shared memory by TMA tensor stores.
 //   Shared memory: the x tile and W1 (resident), both as 32-byte rows (one
-//   16-wide K step, 32-byte swizzle); four 16 KB activation slots (one 64-wide
-//   K block of 128 rows each, 128-byte swizzled as the MMA reads them), which
-//   hold layer 1's output blocks 0-3, then 4-7, then layer 2's output blocks
-//   0-3, and last the output staging; a ring of 32 KB weight stages fed by TMA
-//   in the order the MMAs use them (W2's eight K blocks, W3's four); the
-//   biases.
-//   warp 0      producer: builds each x tile from the fp32 input (coalesced
-//               loads of the tile's contiguous rows, rounded to fp16 into the
-//               32-byte-swizzled layout), TMA loads of the weights
+//   16-wide K step, 32-byte swizzle); a 5-stage ring of 32 KB weight boxes fed
+//   by TMA in the order the MMAs use them (W2's eight K blocks, W3's four);
+//   the output staging; the biases.
+//   warp 0      TMA producer of the weight ring (and W1 once)
 //   warp 1      TMEM allocation and MMA issue
-//   warps 2..17 epilogue: drain TMEM (four warps per lane quarter, each two
-//               of a layer's eight 32-column slices with both loads in
-//               flight), + bias, ReLU, fp16 into the next layer's slots or,
-//               for layer 3 (one slice each), through a staging buffer in the
-//               slots out by TMA store
-// Each slot is filled three times per tile (use u = 0, 1, 2: layer 1 blocks
-// 0-3, 4-7, layer 2 blocks 0-3) by the 8 warps that own its two 32-column
-// slices, each slot published as soon as it is written, so the next layer's
-// MMAs start on block 0 while blocks 1-3 are still being converted; its
-// full/empty barriers alternate phase with every use.  Accumulator columns are
-// reused only after every warp has read them: layer 2 (columns 0..255) waits
-// for all 16 warps' loads of layer 1's first half (lread); layer 3 (256..383)
-// follows layer 2, which needs all of layer 1's second half published; the
-// next tile's layer 1 waits for the drains of layers 2 and 3 (tlo, thi).
+//   warps 2..17 conversion: four warps per TMEM lane quarter, each two of a
+//               layer's eight 32-column slices (both loads in flight) into 16
+//               packed columns each; for layer 3 one slice, out by TMA store
+//   warp 18     builds each x tile from the fp32 input (coalesced 16-byte
+//               loads of the tile's contiguous rows, rounded to fp16 at their
+//               swizzled places) as soon as the previous tile's layer 1 has
+//               read the buffer
+// A column range is overwritten only after its last reader: layer 1's second
+// half waits for every warp's conversion of the first (lread), layer 2 for
+// the second (bread), the next tile's layer 1 for layer 2's conversion (a3);
+// A3 replaces A2 once layer 2's MMAs are complete, and the next tile's A2
+// replaces A3 and layer 3's accumulator only after the same warps have
+// drained layer 3 (program order).  Bit-identical to the per-layer kernels.
 constexpr int kF3K0 = 16, kF3N1 = 512, kF3N2 = 256, kF3N3 = 128;
-constexpr int kF3Epi = 16;                           // epilogue warps, four per TMEM lane quarter
-constexpr int kF3Threads = (2 + kF3Epi) * 32;
-constexpr int kF3Stages = 4;
-constexpr int kF3StageBytes = 256 * 128;             // a {64, 256} fp16 box
-constexpr int kF3SlotBytes = kBM * 128;              // a {64, 128} fp16 box
-constexpr int kF3XOff = 0;                           // x tile: 128 rows x 32 bytes
-constexpr int kF3W1Off = kF3XOff + kBM * 32;         // W1: 512 rows x 32 bytes
-constexpr int kF3SlotOff = kF3W1Off + kF3N1 * 32;
-constexpr int kF3RingOff = kF3SlotOff + 4 * kF3SlotBytes;
-constexpr int kF3BiasOff = kF3RingOff + kF3Stages * kF3StageBytes;   // the three biases, fp32
+constexpr int kF3Epi = 16;
+constexpr int kF3Threads = (3 + kF3Epi) * 32;   // producer, MMA, conversion warps, x-tile warp
+constexpr int kF3Stages = 5;
+constexpr int kF3StageBytes = 256 * 128;
+constexpr int kF3XOff = 0;
+constexpr int kF3W1Off = kF3XOff + kBM * 32;
+constexpr int kF3RingOff = kF3W1Off + kF3N1 * 32;
+constexpr int kF3OutOff = kF3RingOff + kF3Stages * kF3StageBytes;
+constexpr int kF3BiasOff = kF3OutOff + kF3Epi * 32 * 64;
 constexpr int kF3BarOff = kF3BiasOff + (kF3N1 + kF3N2 + kF3N3) * 4;
-static_assert(kF3Epi * 2 * 32 * 64 <= 4 * kF3SlotBytes, "output staging must fit the slots");
-// barriers: xfull, xempty, w1full, full[S], empty[S], sfull[4], sempty[4], l1a, l1b, l2, l3, tlo, thi,
-// drain, lread, oread
-constexpr int kF3Bars = 3 + 2 * kF3Stages + 8 + 9;
+// barriers: xfull, xempty, w1full, full[S], empty[S], l1a, l1b, l2, l3, lread, bread, a3, drain
+constexpr int kF3Bars = 3 + 2 * kF3Stages + 8;
 constexpr size_t kF3Smem = 1024 + kF3BarOff + kF3Bars * 8 + 16;
 
 __global__ void __launch_bounds__(kF3Threads, 1)
@@ -288,8 +283,8 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* xs = smem + kF3XOff;
     uint8_t* w1s = smem + kF3W1Off;
-    uint8_t* slots = smem + kF3SlotOff;
     uint8_t* ring = smem + kF3RingOff;
+    uint8_t* stage_out = smem + kF3OutOff;
     float* bias_s = reinterpret_cast<float*>(smem + kF3BiasOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF3BarOff);
     uint64_t* xfull = bars;
@@ -297,17 +292,14 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
     uint64_t* w1full = bars + 2;
     uint64_t* full = bars + 3;
     uint64_t* empty = full + kF3Stages;
-    uint64_t* sfull = empty + kF3Stages;
-    uint64_t* sempty = sfull + 4;
-    uint64_t* l1a = sempty + 4;
+    uint64_t* l1a = empty + kF3Stages;
     uint64_t* l1b = l1a + 1;
     uint64_t* l2 = l1a + 2;
     uint64_t* l3 = l1a + 3;
-    uint64_t* tlo = l1a + 4;      // layer-2 accumulator drained: columns 0..255 free
-    uint64_t* thi = l1a + 5;      // layer-3 accumulator drained: columns 256..511 free
-    uint64_t* drain = l1a + 6;    // abort: the MMAs issued so far are complete
-    uint64_t* lread = l1a + 7;    // every warp has loaded its part of layer 1's first half
-    uint64_t* oread = l1a + 8;    // the output stores have read the staging in the slots
+    uint64_t* lread = l1a + 4;   // layer 1's first half drained into A2 columns 256..383
+    uint64_t* bread = l1a + 5;   // layer 1's second half drained into A2 columns 384..511
+    uint64_t* a3 = l1a + 6;      // layer 2 drained into A3 columns 256..383 (columns 0..255 free)
+    uint64_t* drain = l1a + 7;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kF3Bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -315,23 +307,18 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
     const int tiles = (M + kBM - 1) / kBM;
 
     if (threadIdx.x == 0) {
-        mbar_init(xfull, 1);   // the producer warp's arrival once the tile is built
+        mbar_init(xfull, 1);
         mbar_init(xempty, 1);
         mbar_init(w1full, 1);
         for (int i = 0; i < kF3Stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&sfull[i], kF3Epi / 2);
-            mbar_init(&sempty[i], 1);
-        }
         for (int i = 0; i < 4; ++i) mbar_init(&l1a[i], 1);
-        mbar_init(tlo, kF3Epi);
-        mbar_init(thi, kF3Epi);
-        mbar_init(drain, 1);
         mbar_init(lread, kF3Epi);
-        mbar_init(oread, kF3Epi);
+        mbar_init(bread, kF3Epi);
+        mbar_init(a3, kF3Epi);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -342,10 +329,7 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // everything above touches no global memory: it overlaps the previous kernel's tail
     pdl_wait_and_release();
-    // the biases, read by the epilogue from shared memory (broadcast loads); the
-    // x tile's pad columns stay zero
     for (int i = threadIdx.x; i < kBM * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(xs)[i] = 0u;
     for (int i = threadIdx.x; i < kF3N1 + kF3N2 + kF3N3; i += blockDim.x)
         bias_s[i] = i < kF3N1 ? b1[i] : (i < kF3N1 + kF3N2 ? b2[i - kF3N1] : b3[i - kF3N1 - kF3N2]);
@@ -355,8 +339,8 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        // -------------------------------------------------------------- producer
-        int q = 0, it = 0;   // ring loads, tiles
+        // ------------------------------------------------------- TMA producer
+        int q = 0;   // ring loads issued
         bool ok = true;
         auto ring_load = [&](const CUtensorMap* map, int c0, int c1, uint32_t bytes) {
             const int st = q % kF3Stages;
@@ -366,20 +350,101 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
             ++q;
             return true;
         };
-        if (lane == 0 && blockIdx.x < tiles) {   // W1 stays resident
+        if (lane == 0 && blockIdx.x < tiles) {
             mbar_expect_tx(w1full, kF3N1 * 32);
             tma_load_2d(w1s, &map_w1, 0, 0, w1full);
             tma_load_2d(w1s + 256 * 32, &map_w1, 0, 256, w1full);
         }
+        if (lane == 0)
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) ok = ring_load(&map_w2, kb * kKB, 0, kF3StageBytes);
+                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) ok = ring_load(&map_w3, kb * kKB, 0, kF3N3 * 128);
+            }
+        if (lane == 0 && *abort_flag) {
+            for (int j = (q > kF3Stages ? q - kF3Stages : 0); j < q; ++j)
+                mbar_drain(&full[j % kF3Stages], (uint32_t)(j / kF3Stages) & 1u);
+            if (blockIdx.x < tiles) mbar_drain(w1full, 0);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // --------------------------------------------------- MMA issuer
+            int q = 0, it = 0;
+            bool ok = true, issued = false;
+            const uint32_t id256 = idesc_f16(kBM, 256), id128 = idesc_f16(kBM, 128);
+            auto ring_wait = [&]() -> int {
+                const int st = q % kF3Stages;
+                if (!mbar_wait(&full[st], (uint32_t)(q / kF3Stages) & 1u, abort_flag, wait_cycles)) return -1;
+                tc_fence_after();
+                return st;
+            };
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
+                const uint32_t par = (uint32_t)it & 1u;
+                // layer 1, first half -> columns 0..255 (free once the previous tile's layer 2 is drained)
+                if ((it == 0 && !mbar_wait(w1full, 0, abort_flag, wait_cycles)) ||
+                    !mbar_wait(xfull, par, abort_flag, wait_cycles) || !mbar_wait(a3, par ^ 1u, abort_flag, wait_cycles))
+                    break;
+                tc_fence_after();
+                const uint64_t xd = sw32_desc(smem_u32(xs));
+                tc_mma_f16(tmem_base, xd, sw32_desc(smem_u32(w1s)), id256, 0);
+                issued = true;
+                tc_commit(l1a);
+                // second half -> columns 0..255 again, once the first is drained
+                if (!mbar_wait(lread, par, abort_flag, wait_cycles)) break;
+                tc_fence_after();
+                tc_mma_f16(tmem_base, xd, sw32_desc(smem_u32(w1s + 256 * 32)), id256, 0);
+                tc_commit(xempty);
+                tc_commit(l1b);
+                // layer 2: A = A2 in TMEM columns 256..511, accumulator columns 0..255
+                if (!mbar_wait(bread, par, abort_flag, wait_cycles)) break;
+                tc_fence_after();
+                int st;
+                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) {
+                    if ((st = ring_wait()) < 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
+                    for (int kk = 0; kk < kKB / 16; ++kk)
+                        tc_mma_f16_ts(tmem_base, tmem_base + 256 + (uint32_t)(32 * kb + 8 * kk), sw128_desc(wa + kk * 32),
+                                      id256, (kb | kk) != 0);
+                    tc_commit(&empty[st]);
+                    ++q;
+                }
+                if (!ok) break;
+                tc_commit(l2);
+                // layer 3: A = A3 in TMEM columns 256..383, accumulator columns 384..511
+                if (!mbar_wait(a3, par, abort_flag, wait_cycles)) break;
+                tc_fence_after();
+                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) {
+                    if ((st = ring_wait()) < 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
+                    for (int kk = 0; kk < kKB / 16; ++kk)
+                        tc_mma_f16_ts(tmem_base + 384, tmem_base + 256 + (uint32_t)(32 * kb + 8 * kk),
+                                      sw128_desc(wa + kk * 32), id128, (kb | kk) != 0);
+                    tc_commit(&empty[st]);
+                    ++q;
+                }
+                if (!ok) break;
+                tc_commit(l3);
+            }
+            if (*abort_flag && issued) {
+                tc_commit(drain);
+                mbar_drain(drain, 0);
+            }
+        }
+    } else if (warp == 2 + kF3Epi) {
+        // ----------------------------------------------------------- x tiles
+        // each tile's x rows are one contiguous run of fp32: element i of it is
+        // row i / K0, column i % K0, rounded to fp16 at its swizzled place
         const int64_t xn = (int64_t)M * K0;
-        for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
-            // x tile t: rows m0.. are one contiguous run of fp32; element i of it is
-            // row i / K0, column i % K0, stored as a half at its swizzled place
+        int it = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
             int w = 1;
             if (lane == 0) w = mbar_wait(xempty, ((uint32_t)it & 1u) ^ 1u, abort_flag, wait_cycles);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
-            // 128 K0 floats = 32 K0 16-byte words: lane l takes words l + 32 u, u < K0,
-            // eight loads in flight at a time
             const int64_t base = (int64_t)t * kBM * K0;
             const float4* x4 = reinterpret_cast<const float4*>(x + base);
             for (int u0 = 0; u0 < K0; u0 += 8) {
@@ -391,7 +456,7 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
                     if (u0 + u < K0) {
                         if (i + 4 <= xn) {
                             v[u] = __ldg(x4 + lane + kWarp * (u0 + u));
-                        } else if (i < xn) {   // the input's last, partial word
+                        } else if (i < xn) {
                             v[u].x = x[i];
                             if (i + 1 < xn) v[u].y = x[i + 1];
                             if (i + 2 < xn) v[u].z = x[i + 2];
@@ -414,101 +479,14 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> the MMA
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(xfull);
-                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) ok = ring_load(&map_w2, kb * kKB, 0, kF3StageBytes);
-                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) ok = ring_load(&map_w3, kb * kKB, 0, kF3N3 * 128);
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        }
-        if (lane == 0 && *abort_flag) {   // the copies already issued must land before the CTA exits
-            for (int j = (q > kF3Stages ? q - kF3Stages : 0); j < q; ++j)
-                mbar_drain(&full[j % kF3Stages], (uint32_t)(j / kF3Stages) & 1u);
-            if (blockIdx.x < tiles) mbar_drain(w1full, 0);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------------------------------------------- MMA issuer
-            int q = 0, it = 0;
-            bool ok = true, issued = false;
-            const uint32_t id256 = idesc_f16(kBM, 256), id128 = idesc_f16(kBM, 128);
-            auto ring_wait = [&]() -> int {
-                const int st = q % kF3Stages;
-                if (!mbar_wait(&full[st], (uint32_t)(q / kF3Stages) & 1u, abort_flag, wait_cycles)) return -1;
-                tc_fence_after();
-                return st;
-            };
-            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
-                const uint32_t par = (uint32_t)it & 1u;
-                // layer 1, columns 0..255 (after the previous tile's layer 2 is drained)
-                if ((it == 0 && !mbar_wait(w1full, 0, abort_flag, wait_cycles)) ||
-                    !mbar_wait(xfull, par, abort_flag, wait_cycles) || !mbar_wait(tlo, par ^ 1u, abort_flag, wait_cycles))
-                    break;
-                tc_fence_after();
-                const uint64_t xd = sw32_desc(smem_u32(xs));
-                tc_mma_f16(tmem_base, xd, sw32_desc(smem_u32(w1s)), id256, 0);
-                issued = true;
-                tc_commit(l1a);
-                // layer 1, columns 256..511 (after the previous tile's layer 3 is drained)
-                if (!mbar_wait(thi, par ^ 1u, abort_flag, wait_cycles)) break;
-                tc_fence_after();
-                tc_mma_f16(tmem_base + 256, xd, sw32_desc(smem_u32(w1s + 256 * 32)), id256, 0);
-                tc_commit(xempty);
-                tc_commit(l1b);
-                int st;
-                // layer 2: K blocks 0..7 from slots kb % 4 (uses 0 and 1)
-                for (int kb = 0; ok && kb < kF3N1 / kKB; ++kb) {
-                    const int s = kb & 3;
-                    const uint32_t g = 3u * (uint32_t)it + (uint32_t)(kb >> 2);
-                    if ((kb == 0 && !mbar_wait(lread, par, abort_flag, wait_cycles)) ||
-                        !mbar_wait(&sfull[s], g & 1u, abort_flag, wait_cycles) || (st = ring_wait()) < 0) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sa = smem_u32(slots + (size_t)s * kF3SlotBytes);
-                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
-                    for (int kk = 0; kk < kKB / 16; ++kk)
-                        tc_mma_f16(tmem_base, sw128_desc(sa + kk * 32), sw128_desc(wa + kk * 32), id256,
-                                   (kb | kk) != 0);
-                    tc_commit(&empty[st]);
-                    tc_commit(&sempty[s]);
-                    ++q;
-                }
-                if (!ok) break;
-                tc_commit(l2);
-                // layer 3: K blocks 0..3 from slots 0..3 (use 2), accumulator columns 256..383
-                for (int kb = 0; ok && kb < kF3N2 / kKB; ++kb) {
-                    const uint32_t g = 3u * (uint32_t)it + 2u;
-                    if (!mbar_wait(&sfull[kb], g & 1u, abort_flag, wait_cycles) || (st = ring_wait()) < 0) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sa = smem_u32(slots + (size_t)kb * kF3SlotBytes);
-                    const uint32_t wa = smem_u32(ring + (size_t)st * kF3StageBytes);
-                    for (int kk = 0; kk < kKB / 16; ++kk)
-                        tc_mma_f16(tmem_base + 256, sw128_desc(sa + kk * 32), sw128_desc(wa + kk * 32), id128,
-                                   (kb | kk) != 0);
-                    tc_commit(&empty[st]);
-                    tc_commit(&sempty[kb]);
-                    ++q;
-                }
-                if (!ok) break;
-                tc_commit(l3);
-            }
-            if (*abort_flag && issued) {   // MMAs already issued must finish before TMEM is freed
-                tc_commit(drain);
-                mbar_drain(drain, 0);
-            }
+            if (lane == 0) mbar_arrive(xfull);
         }
     } else {
-        // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
-        const int sub = (warp - 2) / 4;                         // 0..3 among the quarter's warps
-        const int r = 32 * quarter + lane;                       // tile row = TMEM lane
+        const int sub = (warp - 2) / 4;
         const uint32_t trow = tmem_base + ((uint32_t)(32 * quarter) << 16);
-        const int xs64 = (lane >> 1) & 3;                       // 64-byte swizzle of the output staging
-        uint8_t* myout = slots + (size_t)(warp - 2) * (2 * 32 * 64);   // output staging, after layer 3
-        // accumulator v (32 columns) + bias, ReLU -> 16 words of halves
+        const int xs64 = (lane >> 1) & 3;
+        uint8_t* myout = stage_out + (size_t)(warp - 2) * (32 * 64);
         auto finish32 = [&](const uint32_t (&v)[32], const float* bias, uint32_t (&h)[16]) {
             const float4* bq = reinterpret_cast<const float4*>(bias);
 #pragma unroll
@@ -519,98 +497,65 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
                     h2_relu_bits(__uint_as_float(v[4 * j + 2]) + bb.z, __uint_as_float(v[4 * j + 3]) + bb.w);
             }
         };
-        // 32-column slice j (halves [32 (j & 1), +32) of K block j / 2), row r of slot j / 2
-        auto put_slot = [&](int j, const uint32_t (&h)[16]) {
-            const uint32_t base = smem_u32(slots + (size_t)(j >> 1) * kF3SlotBytes) + (uint32_t)r * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t dst = base + ((uint32_t)((4 * (j & 1) + q) ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[4 * q]), "r"(h[4 * q + 1]),
-                             "r"(h[4 * q + 2]), "r"(h[4 * q + 3])
-                             : "memory");
-            }
-        };
-        // one layer's 256 columns (from TMEM column tcol0) -> slots 0..3 for use g: this
-        // warp's slices sub and sub + 4, both TMEM loads in flight; then publish
-        auto fill_slots = [&](uint32_t tcol0, const float* bias, uint32_t g) {
-            // the first use of a tile reuses the previous tile's output staging
-            if (g % 3u == 0 && !mbar_wait(oread, ((g / 3u) & 1u) ^ 1u, abort_flag, wait_cycles)) return false;
-            const int j0 = sub, j1 = sub + 4;                   // slots sub / 2, then 2 + sub / 2
-            uint32_t v0[32], v1[32];
-            tmem_ld_x32(trow + tcol0 + (uint32_t)(32 * j0), v0);
-            tmem_ld_x32(trow + tcol0 + (uint32_t)(32 * j1), v1);
+        // 256 accumulator columns (from 0) -> 128 packed columns from dst0: slices sub and sub + 4
+        auto convert = [&](const float* bias, uint32_t dst0, uint64_t* done) {
+            const int j0 = sub, j1 = sub + 4;
+            uint32_t v0[32], v1[32], h[16];
+            tmem_ld_x32(trow + (uint32_t)(32 * j0), v0);
+            tmem_ld_x32(trow + (uint32_t)(32 * j1), v1);
             tmem_wait_ld2(v0, v1);
-            if (g % 3u == 0) {   // layer 1's first half read: layer 2 may take its columns
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(lread);
-            }
-            // one slice into its slot, then publish the slot (this warp's share of it)
-            auto put = [&](int j, const uint32_t (&v)[32]) {
-                if (!mbar_wait(&sempty[j >> 1], (g & 1u) ^ 1u, abort_flag, wait_cycles)) return false;
-                uint32_t h[16];
-                finish32(v, bias + 32 * j, h);
-                put_slot(j, h);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> the MMAs
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sfull[j >> 1]);
-                return true;
-            };
-            return put(j0, v0) && put(j1, v1);
+            finish32(v0, bias + 32 * j0, h);
+            tmem_st_x16(trow + dst0 + (uint32_t)(16 * j0), h);
+            finish32(v1, bias + 32 * j1, h);
+            tmem_st_x16(trow + dst0 + (uint32_t)(16 * j1), h);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(done);
         };
-        int it = 0, k = 0;                                      // k: output slices of this warp (buffer k & 1)
+        int it = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
             const uint32_t par = (uint32_t)it & 1u;
             const int m0 = t * kBM;
             if (!mbar_wait(l1a, par, abort_flag, wait_cycles)) break;
             __syncwarp();
             tc_fence_after();
-            if (!fill_slots(0, bias_s, 3u * it)) break;
+            convert(bias_s, 256, lread);
             if (!mbar_wait(l1b, par, abort_flag, wait_cycles)) break;
             __syncwarp();
             tc_fence_after();
-            if (!fill_slots(256, bias_s + 256, 3u * it + 1u)) break;
+            convert(bias_s + 256, 384, bread);
             if (!mbar_wait(l2, par, abort_flag, wait_cycles)) break;
             __syncwarp();
             tc_fence_after();
-            if (!fill_slots(0, bias_s + kF3N1, 3u * it + 2u)) break;
-            tc_fence_before();   // layer 2's columns read: the next tile's layer 1 may take them
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tlo);
+            convert(bias_s + kF3N1, 256, a3);
             if (!mbar_wait(l3, par, abort_flag, wait_cycles)) break;
             __syncwarp();
             tc_fence_after();
             {
-                const int c0 = 32 * sub;                         // layer 3: one 32-column slice per warp
+                const int c0 = 32 * sub;
                 uint32_t v[32], h[16];
-                tmem_ld_x32(trow + 256 + (uint32_t)c0, v);
+                tmem_ld_x32(trow + 384 + (uint32_t)c0, v);
                 tmem_wait_ld(v);
-                tc_fence_before();   // layer 3's columns read: the next tile's layer 1 may take them
-                __syncwarp();
-                if (lane == 0) mbar_arrive(thi);
                 finish32(v, bias_s + kF3N1 + kF3N2 + c0, h);
-                uint8_t* sb = myout + (k & 1) * (32 * 64);
-                if (lane == 0) bulk_wait_read<1>();           // the store that last used this buffer has read it
+                if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t dst = smem_u32(sb + lane * 64 + ((j ^ xs64) << 4));
+                    const uint32_t dst = smem_u32(myout + lane * 64 + ((j ^ xs64) << 4));
                     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[4 * j]), "r"(h[4 * j + 1]),
                                  "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
                                  : "memory");
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) {   // rows past M are clipped by the tensor store
-                    tma_store_2d(&map_out, c0, m0 + 32 * quarter, sb);
+                if (lane == 0) {
+                    tma_store_2d(&map_out, c0, m0 + 32 * quarter, myout);
                     bulk_commit();
-                    bulk_wait_read<0>();   // the staging may be overwritten by the next tile
-                    mbar_arrive(oread);
                 }
-                ++k;
             }
         }
-        if (lane == 0) bulk_wait_all();   // this warp's stores are complete before the CTA exits
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
