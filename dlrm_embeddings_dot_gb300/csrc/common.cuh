@@ -37,8 +37,8 @@ inline dlrm_status check_launch(const char* what)
     return DLRM_OK;
 }
 
-// Launch with programmatic stream serialization: the grid may be scheduled
-// while the previous kernel on the stream drains.  Every kernel launched this
+// Launch with programmatic stream serialization: the launch is processed
+// while the previous kernel on the stream runs.  Every kernel launched this
 // way calls pdl_wait() before touching global memory, so it still sees all of
 // the previous kernel's writes and makes none the previous kernel could see.
 template <typename... KArgs, typename... Args>
@@ -99,14 +99,14 @@ constexpr int kWarp = 32;
 // attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ... and let the next grid be scheduled at once (its blocks wait in
-// pdl_wait until this grid completes).  Kernels that need the SM's L1 for
-// themselves leave this out: the next grid is then scheduled as they exit.
-__device__ __forceinline__ void pdl_wait_and_release()
-{
-    pdl_wait();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+// No kernel triggers its dependents early (griddepcontrol.launch_dependents):
+// the next grid is then scheduled only when this one completes, and the
+// attribute still hides its launch processing.  With an early trigger the
+// next grid's blocks took registers and shared memory on SMs as this grid's
+// blocks left, and a one-wave persistent grid that followed (the one-pass
+// forward after the sparse update, the backward after the forward) started
+// with fewer blocks on those SMs: 0.851 ms per 64K fp32 training step with the
+// trigger, 0.808 ms without, 0.839 ms with plain launches.
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit)
 {

@@ -138,7 +138,7 @@ keys_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* _
 {
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
-    pdl_wait_and_release();
+    pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x < kNumCounters) counters[threadIdx.x] = 0;   // counters of the segment pass
     __syncthreads();
     const int lane = threadIdx.x % kWarp;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kSortThreads)
 radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t mask, uint32_t* __restrict__ hist,
               int64_t ntiles)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
     __syncthreads();
@@ -283,7 +283,7 @@ radix_upsweep(const uint32_t* __restrict__ keys, int64_t n, int shift, uint32_t 
 __global__ void __launch_bounds__(kSortThreads)
 radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ totals)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     __shared__ uint32_t warp_sums[kSortThreads / kWarp];
     __shared__ uint32_t chunk_total;
     uint32_t* row = hist + (int64_t)blockIdx.x * ntiles;
@@ -319,7 +319,7 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
                 uint32_t mask, const uint32_t* __restrict__ hist, const uint32_t* __restrict__ totals,
                 int64_t ntiles, const int32_t* __restrict__ offsets, int64_t bpb, int64_t nbags)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     constexpr int kW = kSortThreads / kWarp;
     __shared__ uint32_t wcnt[kW][256];
     __shared__ uint32_t dbase[256];
@@ -486,7 +486,7 @@ fixup_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ partia
              const uint32_t* __restrict__ counters, int64_t IT, int D, float* __restrict__ tables,
              int64_t total_rows, float lr)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     constexpr int kW = kFixThreads / kWarp;
     extern __shared__ __align__(16) float red[];   // [kW][D]
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
@@ -600,7 +600,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
     constexpr int64_t IT = (int64_t)kWarp * kSubs;
     const int lane = threadIdx.x % kWarp;
     const int c4 = D / 4;
-    pdl_wait_and_release();
+    pdl_wait();
 
     auto fetch_item = [&]() -> int64_t {
         uint32_t v = 0;

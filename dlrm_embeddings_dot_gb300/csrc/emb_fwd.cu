@@ -138,6 +138,7 @@ emb_fwd_multi_kernel(const T* __restrict__ tables, const int64_t* __restrict__ r
                      const int32_t* __restrict__ offsets, TO* __restrict__ pooled, bool hash,
                      uint32_t* status, int64_t nbags, int64_t nnz)
 {
+    pdl_wait();
     constexpr int V = Vec<T>::n;
     const int chunks = D / V;
     const int lane = threadIdx.x % G;
@@ -254,6 +255,7 @@ __device__ __forceinline__ void single_hot_body(const T* __restrict__ tables, co
                                                 const int32_t* __restrict__ offsets, TO* __restrict__ pooled,
                                                 bool hash, uint32_t* status, int64_t nbags, int64_t nnz)
 {
+    pdl_wait();
     constexpr int V = Vec<T>::n;
     constexpr int RPI = kWarp / G;                // rows per load instruction
     constexpr int U = 8;                          // load instructions in flight per lane
@@ -370,17 +372,17 @@ void launch(const void* tables, const int64_t* row_base, int F, int D, int B,
     bool launched = false;
     if constexpr (G == kWarp && sizeof(T) == sizeof(TO)) {
         if (single_hot) {
-            emb_fwd_single_row_kernel<T, TO><<<blocks, kThreads, 0, stream>>>(
+            launch_pdl(emb_fwd_single_row_kernel<T, TO>, blocks, kThreads, 0, stream,
                 (const T*)tables, row_base, F, D, B, indices, offsets, (TO*)pooled, hash, status, nbags, nnz);
             launched = true;
         }
     } else if (single_hot && D / Vec<T>::n <= G) {
-        emb_fwd_single_kernel<T, TO, G><<<blocks, kThreads, 0, stream>>>(
+        launch_pdl(emb_fwd_single_kernel<T, TO, G>, blocks, kThreads, 0, stream,
             (const T*)tables, row_base, F, D, B, indices, offsets, (TO*)pooled, hash, status, nbags, nnz);
         launched = true;
     }
     if (!launched)
-        emb_fwd_multi_kernel<T, TO, G><<<(int)grid_for(nbags, G), kThreads, 0, stream>>>(
+        launch_pdl(emb_fwd_multi_kernel<T, TO, G>, (int)grid_for(nbags, G), kThreads, 0, stream,
             (const T*)tables, row_base, F, D, B, indices, offsets, (TO*)pooled, hash, status, nbags, nnz);
 }
 

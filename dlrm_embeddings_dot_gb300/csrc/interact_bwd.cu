@@ -97,7 +97,7 @@ interact_bwd_kernel(const float* __restrict__ grad_out, const T* __restrict__ de
                     const T* __restrict__ pooled, int F, int D, int B, int P,
                     float* __restrict__ grad_dense, float* __restrict__ grad_pooled)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     constexpr int RS = (RMAX + 3) / 4 * 4;       // smem row stride of M (multiple of 4)
     extern __shared__ __align__(16) unsigned char bwd_smem_raw[];
     const int lane = threadIdx.x % kWarp;
@@ -212,7 +212,7 @@ interact_bwd_regs_kernel(const float* __restrict__ grad_out, const float* __rest
                          const float* __restrict__ pooled, RegGather ga, int B, int P, float* __restrict__ grad_dense,
                          float* __restrict__ grad_pooled, uint32_t* __restrict__ status)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     using L = RegBwd<R>;
     constexpr int F = R - 1, D = kRegD, RS = L::RS, NP = L::NP;
     extern __shared__ __align__(16) unsigned char bwd_regs_raw[];

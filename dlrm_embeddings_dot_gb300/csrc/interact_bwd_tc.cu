@@ -70,7 +70,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_pooled, const __g
                        __half* __restrict__ grad_dense, int F, int D, int B, int P, int KH, int NS,
                        uint32_t tmem_cols, uint32_t* status, long long wait_cycles)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int z_bytes = KH * kZBlockBytes;

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 8)
 interact_fwd_ffma_kernel(const T* __restrict__ dense, const T* __restrict__ pooled, int F, int D_rt,
                          int B, T* __restrict__ out, int P)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     extern __shared__ __align__(16) float smem[];
     const int D = DT ? DT : D_rt;
     const FfmaGeom geo = ffma_geom(F, D, P);
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kRegWarps * kWarp, 3)
 interact_fwd_regs_kernel(const float* __restrict__ dense, const float* __restrict__ pooled, int B,
                          float* __restrict__ out, int P, uint32_t* __restrict__ status)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     constexpr int D = kRegD;
     extern __shared__ __align__(16) float4 zbuf[];
     const int lane = threadIdx.x % kWarp;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kRegWarps * kWarp, 3)
 emb_interact_regs_kernel(RegGather ga, const float* __restrict__ dense, int B, float* __restrict__ pooled,
                          float* __restrict__ out, int P, uint32_t* __restrict__ status)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     constexpr int kAfter = kPooled ? (R * (R - 1) / 2 + 31) / 32 / 2 : 0;
     constexpr int F = R - 1;
     constexpr int D = kRegD;

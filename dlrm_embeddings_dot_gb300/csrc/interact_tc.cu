@@ -106,7 +106,7 @@ interact_tc_kernel(const __grid_constant__ CUtensorMap map_pooled,
                    __half* __restrict__ out, int F, int D, int B, int P, int KH, int NS,
                    uint32_t* status, GatherArgs ga, long long wait_cycles)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const Layout L = make_layout(KH, P, NS);

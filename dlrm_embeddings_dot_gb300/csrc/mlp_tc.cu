@@ -54,7 +54,7 @@ mlp_layer_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                  const __grid_constant__ CUtensorMap map_out, const float* __restrict__ bias, int M, int N, int K,
                  int BN, int NS, uint32_t tmem_cols, uint32_t* status)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int a_bytes = kBM * 128, stage_bytes = a_bytes + BN * 128;
@@ -329,7 +329,7 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    pdl_wait_and_release();
+    pdl_wait();
     for (int i = threadIdx.x; i < kBM * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(xs)[i] = 0u;
     for (int i = threadIdx.x; i < kF3N1 + kF3N2 + kF3N3; i += blockDim.x)
         bias_s[i] = i < kF3N1 ? b1[i] : (i < kF3N1 + kF3N2 ? b2[i - kF3N1] : b3[i - kF3N1 - kF3N2]);
@@ -571,7 +571,7 @@ mlp3_fused_kernel(const float* __restrict__ x, int K0, const __grid_constant__ C
 // x (fp32 [M][K]) -> fp16 [M][Kp], pad columns zero.
 __global__ void cast_pad_kernel(const float* __restrict__ x, int64_t M, int K, int Kp, __half* __restrict__ x16)
 {
-    pdl_wait_and_release();
+    pdl_wait();
     const int64_t n = M * Kp;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / Kp;
