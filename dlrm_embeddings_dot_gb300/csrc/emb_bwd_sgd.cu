@@ -11,17 +11,19 @@
 //     8 bits per pass, reduce-then-scan (no inter-block waiting):
 //     per-tile digit histograms -> per-digit scan over tiles -> stable
 //     scatter with warp-level ranking (match.any) in position order.
-//  3. segments: the sorted array is cut into items of kSubs sub-chunks of P
-//     positions (P = 32 for rows of up to 512 bytes).  A warp takes items from a
-//     counter; for each sub-chunk every lane copies its position's gradient row
-//     into shared memory with one bulk copy (so one warp instruction moves 32
-//     rows, and the copies of the next sub-chunk are in flight while this one is
-//     summed).  Each run of equal keys is summed in ascending position order; a
-//     run that starts and ends inside the item updates its row
-//     (w = fmaf(-lr, g, w)) with the table row loaded while the run is summed;
-//     a run crossing an item edge leaves one partial sum per item it touches,
-//     and the item where it starts finds the run's last item and files the run
-//     with its number of pieces.
+//     Up to 8,192 keys one block forms the keys and sorts them in shared
+//     memory instead (the same stable sort in one launch).
+//  3. segments: the sorted array is cut into items of kSubs sub-chunks of 32
+//     positions.  A warp takes items from a counter and walks their
+//     sub-chunks (each position's key and gradient row number in one lane;
+//     the next sub-chunk's loaded meanwhile); the gradient rows of a batch of
+//     positions, and the table rows of the runs that complete among them, are
+//     loaded before any is added.  Each run of equal keys is summed in
+//     ascending position order; a run that starts and ends inside the item
+//     updates its row (w = fmaf(-lr, g, w)); a run crossing an item edge
+//     leaves one partial sum per item it touches, and the item where it
+//     starts finds the run's last item and files the run with its number of
+//     pieces.
 //  4. fixup: each filed run's pieces are added in item order (a block of 16
 //     warps over 16 contiguous slices for runs of many pieces, a warp for the
 //     others) and the row is updated.
@@ -389,6 +391,177 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
     }
 }
 
+
+// ------------------------------------------------ 2'. small batches: one block
+// With few keys the chain of key, count, scan and scatter kernels is all
+// launch and drain latency (about 50 us for a few hundred keys).  Up to
+// kSmallMax keys one block of 32 warps does both steps in shared memory: the
+// keys of every bag (as the key kernel forms them), then the same stable LSD
+// passes -- warp w ranks positions [w * ni * 32, (w + 1) * ni * 32) in order
+// by match.any, the per-digit counts are scanned over the warps and the
+// digit totals over the digits, and each key goes to digit base + earlier
+// warps' count + its rank in the warp -- and writes the sorted pairs where
+// the multi-block sort leaves them.  The result is the same stable sort.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / kWarp;
+constexpr int kSmallItems = 8;                             // keys per thread at most
+constexpr int kSmallMax = kSmallThreads * kSmallItems;    // 8,192 keys
+constexpr int64_t kSmallBags = 4 * (int64_t)kSmallMax;    // bags the block's key loop takes
+
+// keys and values twice (cap each), per-warp digit counts, digit bases, scan carries
+inline size_t small_sort_smem(int cap) { return 16 * (size_t)cap + 4 * (kSmallWarps * 256 + 256 + kSmallWarps); }
+
+__global__ void __launch_bounds__(kSmallThreads, 1)
+small_sort_kernel(const int64_t* __restrict__ row_base, int F, int B, const int32_t* __restrict__ indices,
+                  const int32_t* __restrict__ offsets, bool hash, uint32_t* status, uint32_t* __restrict__ keys_out,
+                  uint32_t* __restrict__ vals_out, int64_t nbags, int nnz, int ni, int nbits,
+                  uint32_t* __restrict__ counters)
+{
+    extern __shared__ __align__(16) uint32_t ssm[];
+    const int cap = ni * kSmallThreads;
+    // buffer c (0 or 1): keys at ssm + 2 * c * cap, values cap further
+    auto kbuf = [&](int c) { return ssm + 2 * c * cap; };
+    auto vbuf = [&](int c) { return ssm + (2 * c + 1) * cap; };
+    uint32_t* wcnt = ssm + 4 * cap;   // [kSmallWarps][256]
+    uint32_t* dbase = wcnt + kSmallWarps * 256;
+    uint32_t* wsum = dbase + 256;
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const uint32_t lt = (1u << lane) - 1u;
+    pdl_wait();
+    if (tid < kNumCounters) counters[tid] = 0;   // counters of the segment pass
+    // positions no bag covers (malformed offsets only) keep the skip key
+    for (int p = tid; p < cap; p += kSmallThreads) {
+        kbuf(0)[p] = kSkipKey;
+        vbuf(0)[p] = 0;
+    }
+    __syncthreads();
+
+    // ---- 1. keys, as the key kernel forms them
+    auto emit = [&](int64_t p, int32_t raw, int64_t base, int64_t n, uint32_t val) {
+        int64_t i = raw;
+        uint32_t key = kSkipKey;
+        if (hash) {
+            if (n > 0) {
+                i %= n;
+                if (i < 0) i += n;
+                key = (uint32_t)(base + i);
+            } else {
+                set_status(status, DLRM_STATUS_OOB_INDEX);
+            }
+        } else if (i >= 0 && i < n) {
+            key = (uint32_t)(base + i);
+        } else {
+            set_status(status, DLRM_STATUS_OOB_INDEX);
+        }
+        kbuf(0)[p] = key;
+        vbuf(0)[p] = val;
+    };
+    auto bag = [&](int64_t g, int64_t& s, int64_t& e, int64_t& base, int64_t& n, uint32_t& val) {
+        const int t = (int)((uint32_t)g / (uint32_t)B);   // F * B < 2^31
+        const int b = (int)g - t * B;
+        base = row_base[t];
+        n = row_base[t + 1] - base;
+        val = (uint32_t)((int64_t)b * F + t);
+        s = offsets[g];
+        e = offsets[g + 1];
+        if (s < 0 || e < s || e > nnz) {   // malformed CSR: clamp, flag, stay in bounds
+            set_status(status, DLRM_STATUS_BAD_OFFSETS);
+            s = s < 0 ? 0 : (s > nnz ? nnz : s);
+            e = e < s ? s : (e > nnz ? nnz : e);
+        }
+    };
+    if (nnz > 2 * nbags) {   // bags of several indices: a warp per bag
+        for (int64_t g = warp; g < nbags; g += kSmallWarps) {
+            int64_t s, e, base, n;
+            uint32_t val;
+            bag(g, s, e, base, n, val);
+            for (int64_t p = s + lane; p < e; p += kWarp) emit(p, indices[p], base, n, val);
+        }
+    } else {
+        for (int64_t g = tid; g < nbags; g += kSmallThreads) {
+            int64_t s, e, base, n;
+            uint32_t val;
+            bag(g, s, e, base, n, val);
+            for (int64_t p = s; p < e; ++p) emit(p, indices[p], base, n, val);
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. stable LSD passes over the bits that can be set
+    int cur = 0;
+    for (int shift = 0; shift < nbits; shift += 8) {
+        const uint32_t mask = (1u << (nbits - shift < 8 ? nbits - shift : 8)) - 1u;
+        const uint32_t* kin = kbuf(cur);
+        const uint32_t* vin = vbuf(cur);
+        for (int x = tid; x < kSmallWarps * 256; x += kSmallThreads) wcnt[x] = 0;
+        __syncthreads();
+        uint32_t key[kSmallItems], val[kSmallItems], local[kSmallItems];
+        const int wbase = warp * ni * kWarp;
+#pragma unroll
+        for (int r = 0; r < kSmallItems; ++r) {
+            if (r < ni) {   // warp-uniform
+                const int p = wbase + r * kWarp + lane;
+                const bool valid = p < nnz;
+                key[r] = valid ? kin[p] : 0;
+                val[r] = valid ? vin[p] : 0;
+                const uint32_t d = (key[r] >> shift) & mask;
+                const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 0x100u);
+                const uint32_t prior = valid ? wcnt[warp * 256 + d] : 0;
+                __syncwarp();
+                if (valid && (peers & lt) == 0) wcnt[warp * 256 + d] = prior + __popc(peers);
+                __syncwarp();
+                local[r] = prior + __popc(peers & lt);
+            }
+        }
+        __syncthreads();
+        // per digit: exclusive scan over the warps, then over the digits
+        uint32_t total = 0;
+        if (tid < 256) {
+            for (int w = 0; w < kSmallWarps; ++w) {
+                const uint32_t c = wcnt[w * 256 + tid];
+                wcnt[w * 256 + tid] = total;
+                total += c;
+            }
+            uint32_t x = total;
+#pragma unroll
+            for (int o = 1; o < kWarp; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == kWarp - 1) wsum[warp] = x;
+            dbase[tid] = x - total;   // exclusive within the warp's 32 digits
+        }
+        __syncthreads();
+        if (tid < 256) {
+            uint32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += wsum[w];
+            dbase[tid] += before;
+        }
+        __syncthreads();
+        uint32_t* kout = kbuf(cur ^ 1);
+        uint32_t* vout = vbuf(cur ^ 1);
+#pragma unroll
+        for (int r = 0; r < kSmallItems; ++r) {
+            if (r < ni) {
+                const int p = wbase + r * kWarp + lane;
+                if (p < nnz) {
+                    const uint32_t d = (key[r] >> shift) & mask;
+                    const uint32_t pos = dbase[d] + wcnt[warp * 256 + d] + local[r];
+                    if (pos < (uint32_t)nnz) {   // always true for consistent counts; guards the write
+                        kout[pos] = key[r];
+                        vout[pos] = val[r];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        cur ^= 1;
+    }
+    for (int p = tid; p < nnz; p += kSmallThreads) {
+        keys_out[p] = kbuf(cur)[p];
+        vals_out[p] = vbuf(cur)[p];
+    }
+}
 
 // ----------------------------------------------------------------- 4. fixup
 constexpr int kFixRegs = 4;   // float4 partial-sum loads a lane keeps in flight
@@ -795,6 +968,24 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
                             "fixup_kernel");
 }
 
+// The segment pass and the fixup for the gradient type and width.
+dlrm_status launch_all_segments(const Ws& w, int64_t nnz, const void* d_grad, unsigned flags, int D, float* tables,
+                                int64_t total_rows, float lr, int64_t nbags, cudaStream_t st)
+{
+    if (flags & DLRM_FLAG_GRAD_F16) {
+        const __half* grad = static_cast<const __half*>(d_grad);
+        if (D <= 128) return launch_segments<1>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+        if (D <= 256) return launch_segments<2>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+        if (D <= 512) return launch_segments<4>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+        return launch_segments<8>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+    }
+    const float* grad = static_cast<const float*>(d_grad);
+    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+    return launch_segments<8>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+}
+
 }  // namespace
 }  // namespace dlrm
 
@@ -847,6 +1038,19 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
     int cur = npasses & 1;   // the last pass lands in buffer 0
 
     const int64_t nbags = (int64_t)F * B;
+    if (nnz <= kSmallMax && nbags <= kSmallBags) {   // one block sorts in shared memory
+        const int ni = (int)((nnz + kSmallThreads - 1) / kSmallThreads);
+        const size_t smem = small_sort_smem(ni * kSmallThreads);
+        cudaError_t e = cudaFuncSetAttribute(small_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)small_sort_smem(kSmallMax));
+        if (e == cudaSuccess)
+            e = launch_pdl(small_sort_kernel, 1, kSmallThreads, smem, st, d_row_base, F, B, d_indices, d_offsets,
+                           (flags & DLRM_FLAG_HASH_INDICES) != 0, d_status, w.keys[0], w.vals[0], nbags, (int)nnz,
+                           ni, nbits, w.counters);
+        dlrm_status s = check_launch_pdl(e, "small_sort_kernel");
+        if (s != DLRM_OK) return s;
+        return launch_all_segments(w, nnz, d_grad_pooled, flags, D, d_tables, total_rows, lr, nbags, st);
+    }
     const bool multi = nnz > 2 * nbags;
     const bool hash = (flags & DLRM_FLAG_HASH_INDICES) != 0;
     const int64_t ntiles = w.ntiles;
@@ -881,18 +1085,7 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
         if (s != DLRM_OK) return s;
         cur ^= 1;
     }
-    if (flags & DLRM_FLAG_GRAD_F16) {
-        const __half* grad = static_cast<const __half*>(d_grad_pooled);
-        if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-        if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-        if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-        return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-    }
-    const float* grad = static_cast<const float*>(d_grad_pooled);
-    if (D <= 128) return launch_segments<1>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-    if (D <= 256) return launch_segments<2>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-    if (D <= 512) return launch_segments<4>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
-    return launch_segments<8>(w, nnz, grad, D, d_tables, total_rows, lr, nbags, st);
+    return launch_all_segments(w, nnz, d_grad_pooled, flags, D, d_tables, total_rows, lr, nbags, st);
 }
 
 // --------------------------------------------------------------------------

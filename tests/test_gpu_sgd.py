@@ -72,10 +72,11 @@ def test_tiny_training_slice(cuda_lib):
     check(cuda_lib, tables, w.row_base, w.F, w.D, w.B, w.indices, w.offsets, gp, w.lr)
 
 
+@pytest.mark.parametrize("B", [50, 400])   # about 3K and 24K indices: the one-block sort and the multi-block one
 @pytest.mark.parametrize("D", [4, 16, 128, 256, 512])
-def test_multi_hot_random(cuda_lib, D):
-    rng = np.random.default_rng(D)
-    F, B = 4, 50
+def test_multi_hot_random(cuda_lib, D, B):
+    rng = np.random.default_rng(D + B)
+    F = 4
     rows = np.array([3, 200, 40, 1])
     row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
     tables = rng.uniform(-0.05, 0.05, size=(row_base[-1], D)).astype(np.float32)
@@ -122,9 +123,10 @@ def test_zipf_default_shapes_and_determinism(cuda_lib):
     assert np.array_equal(tab[torch.from_numpy(c.global_rows).to(dev())].cpu().numpy(), got)
 
 
-def test_hashing_out_of_range_and_lr_zero(cuda_lib):
+@pytest.mark.parametrize("B", [100, 5000])   # 200 and 10,000 indices: both sort paths
+def test_hashing_out_of_range_and_lr_zero(cuda_lib, B):
     rng = np.random.default_rng(9)
-    F, B, D = 2, 100, 16
+    F, D = 2, 16
     row_base = np.array([0, 13, 20], dtype=np.int64)
     tables = rng.uniform(-0.05, 0.05, size=(20, D)).astype(np.float32)
     idx = rng.integers(-30, 30, size=F * B).astype(np.int32)
@@ -136,11 +138,12 @@ def test_hashing_out_of_range_and_lr_zero(cuda_lib):
     assert np.array_equal(tab.cpu().numpy(), tables)
 
 
+@pytest.mark.parametrize("B", [3000, 9000])   # below and above the one-block sort's 8,192 keys
 @pytest.mark.parametrize("total_rows", [1, 255, 256, 257, 70000, 20_000_000])
-def test_key_width_edges(cuda_lib, total_rows):
+def test_key_width_edges(cuda_lib, total_rows, B):
     """The number of radix passes follows the key width; 1 row, byte edges."""
-    rng = np.random.default_rng(total_rows)
-    F, B, D = 1, 3000, 4
+    rng = np.random.default_rng(total_rows + B)
+    F, D = 1, 4
     idx = rng.integers(0, total_rows, size=B).astype(np.int32)
     idx[::5] = total_rows - 1
     uniq = np.unique(idx)
@@ -167,14 +170,19 @@ def test_empty(cuda_lib):
     assert status == 0 and torch.equal(tab, torch.ones(4, 8, device=dev()))
 
 
-def test_malformed_offsets_are_clamped_and_flagged(cuda_lib):
+@pytest.mark.parametrize("reps", [1, 1500])   # 6 and 9,000 indices: both sort paths
+def test_malformed_offsets_are_clamped_and_flagged(cuda_lib, reps):
     """Malformed CSR reaches the sparse update: keys are clamped into [0, nnz],
     grad rows and table rows are range-checked, and the status bit is set."""
-    F, B, D = 2, 4, 16
+    F, B, D = 2, 4 * reps, 16
     tab = torch.zeros(5, D, device=dev())
-    idx = to_dev(np.array([0, 1, 2, 0, 1, 1], dtype=np.int32))
-    bad = to_dev(np.array([0, 2, 9, -3, 4, 3, 6, 100, 6], dtype=np.int32))
-    ws = torch.zeros(cuda_lib.dlrm_emb_bwd_sgd_workspace_size(6, D, 5), dtype=torch.uint8, device=dev())
+    idx_np = np.tile(np.array([0, 1, 2, 0, 1, 1], dtype=np.int32), reps)
+    bad_np = np.arange(F * B + 1, dtype=np.int64) * idx_np.size // (F * B)
+    bad_np[:9] = [0, 2, 9, -3, 4, 3, 6, 100, 6]
+    if reps > 1:
+        bad_np[-1] = idx_np.size + 50
+    idx, bad = to_dev(idx_np), to_dev(bad_np.astype(np.int32))
+    ws = torch.zeros(cuda_lib.dlrm_emb_bwd_sgd_workspace_size(idx_np.size, D, 5), dtype=torch.uint8, device=dev())
     status = torch.zeros(1, dtype=torch.int32, device=dev())
     gp = torch.ones(B, F, D, device=dev())
     cuda_lib.dlrm_emb_bwd_sgd(tab, to_dev(np.array([0, 3, 5], dtype=np.int64)), 5, F, D, B, idx, bad, gp, 0.1,
@@ -182,3 +190,22 @@ def test_malformed_offsets_are_clamped_and_flagged(cuda_lib):
     torch.cuda.synchronize()
     assert int(status.item()) & cuda_lib.DLRM_STATUS_BAD_OFFSETS
     assert torch.isfinite(tab).all()
+
+
+@pytest.mark.parametrize("n,B", [(8192, 8192), (8193, 8193), (100, 40000)])
+def test_one_block_sort_threshold(cuda_lib, n, B):
+    """Batches of up to 8,192 indices over at most 32,768 bags are sorted by one
+    block in shared memory, others by the multi-block passes: both sides of the
+    edge give the stable sort and the oracle's rows (hot rows span many chunks)."""
+    rng = np.random.default_rng(n + B)
+    F, D = 1, 32
+    rows = 70000   # three radix passes
+    tables = rng.uniform(-0.05, 0.05, size=(rows, D)).astype(np.float32)
+    counts = np.zeros(B, np.int64)
+    counts[rng.choice(B, size=min(n, B), replace=False)] = 1
+    np.add.at(counts, rng.integers(0, B, size=n - min(n, B)), 1)
+    off = np.concatenate([[0], np.cumsum(counts)])
+    idx = np.where(rng.random(n) < 0.3, 17, rng.integers(0, rows, size=n)).astype(np.int32)
+    gp = (rng.standard_normal((B, F, D)) * 1e-2).astype(np.float32)
+    check(cuda_lib, tables, np.array([0, rows]), F, D, B, idx, off, gp, 0.1)
+
