@@ -48,6 +48,7 @@ constexpr int kTile = kSortThreads * kItems;   // 1024 keys per tile
 
 // segment pass
 constexpr int kSubs = 8;                 // sub-chunks per item
+constexpr int kSubsSmall = 1;            // ... for batches of the one-block sort (more items in flight)
 constexpr int kFixThreads = 512;
 constexpr int kLongPieces = 8;           // runs of more pieces are summed by a whole block
 
@@ -63,6 +64,12 @@ int key_bits(int64_t total_rows)
     while (b < 32 && ((uint64_t)1 << b) <= (uint64_t)total_rows) ++b;   // 2^b > total_rows
     return b;
 }
+
+constexpr int kSmallMaxKeys = 8192;   // batches up to this many keys take the one-block sort
+
+// Sub-chunks of 32 positions per segment item: a warp walks an item as a
+// chain of dependent loads, so few keys are cut into short items.
+inline int item_subs(int64_t nnz) { return nnz <= kSmallMaxKeys ? kSubsSmall : kSubs; }
 
 struct Ws {
     uint32_t *keys[2], *vals[2];
@@ -80,8 +87,15 @@ Ws carve(void* base, int64_t nnz, int D)
 {
     Ws w;
     w.ntiles = (nnz + kTile - 1) / kTile;
-    const int64_t it = (int64_t)kWarp * kSubs;
+    const int64_t it = (int64_t)kWarp * item_subs(nnz);
     w.nitems = (nnz + it - 1) / it;
+    // item buffers sized so that the workspace never shrinks as nnz grows:
+    // short items stop at kSmallMaxKeys / 32 of them
+    const int64_t it_big = (int64_t)kWarp * kSubs, short_max = kSmallMaxKeys / kWarp / kSubsSmall;
+    const int64_t n_short = (nnz + kWarp * kSubsSmall - 1) / (kWarp * kSubsSmall);
+    const int64_t n_big = (nnz + it_big - 1) / it_big;
+    const int64_t nalloc = n_big > (n_short < short_max ? n_short : short_max) ? n_big
+                                                                              : (n_short < short_max ? n_short : short_max);
     uint8_t* p = static_cast<uint8_t*>(base);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -96,9 +110,9 @@ Ws carve(void* base, int64_t nnz, int D)
     w.hist = (uint32_t*)take(4 * 256 * (size_t)w.ntiles);
     w.totals = (uint32_t*)take(4 * 256);
     w.counters = (uint32_t*)take(4 * kNumCounters);
-    w.partials = (float*)take(4 * 2 * (size_t)w.nitems * D);
-    w.split_list = (uint64_t*)take(8 * (size_t)w.nitems);
-    w.long_list = (uint64_t*)take(8 * (size_t)w.nitems);
+    w.partials = (float*)take(4 * 2 * (size_t)nalloc * D);
+    w.split_list = (uint64_t*)take(8 * (size_t)nalloc);
+    w.long_list = (uint64_t*)take(8 * (size_t)nalloc);
     w.bytes = off;
     return w;
 }
@@ -406,6 +420,7 @@ constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / kWarp;
 constexpr int kSmallItems = 8;                             // keys per thread at most
 constexpr int kSmallMax = kSmallThreads * kSmallItems;    // 8,192 keys
+static_assert(kSmallMax == kSmallMaxKeys, "the one-block sort and the short segment items share the edge");
 constexpr int64_t kSmallBags = 4 * (int64_t)kSmallMax;    // bags the block's key loop takes
 
 // keys and values twice (cap each), per-warp digit counts, digit bases, scan carries
@@ -758,11 +773,11 @@ constexpr int seg_batch()
     return MC >= 8 ? 1 : (sizeof(GT) == 2 ? 8 : 6) / MC > 0 ? (sizeof(GT) == 2 ? 8 : 6) / MC : 1;
 }
 
-// Warps are independent: each takes items of IT = 32 * kSubs positions from a
+// Warps are independent: each takes items of IT = 32 * SUBS positions from a
 // counter and walks their 32-position sub-chunks (lane q holds position q's
 // key and gradient row number; the next sub-chunk's are loaded meanwhile).
 // Rows are added column-wise: lane l holds four-element columns l, l + 32, ...
-template <int MC, typename GT>
+template <int MC, typename GT, int SUBS>
 __global__ void __launch_bounds__(256, MC >= 2 ? 2 : 3)
 segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, int64_t n,
                const GT* __restrict__ grad, int D, float* __restrict__ tables, int64_t total_rows, float lr,
@@ -770,7 +785,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
                uint32_t* __restrict__ counters, int64_t nitems, int64_t nbags)
 {
     constexpr int U = seg_batch<MC, GT>();
-    constexpr int64_t IT = (int64_t)kWarp * kSubs;
+    constexpr int64_t IT = (int64_t)kWarp * SUBS;
     const int lane = threadIdx.x % kWarp;
     const int c4 = D / 4;
     pdl_wait();
@@ -809,9 +824,9 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
         bool cs = false;            // the run continuing into this sub-chunk began inside the item
         uint32_t last_key = before;
         uint32_t k_nxt = kSkipKey, v_nxt = 0, before_nxt = kSkipKey, after_nxt = kSkipKey;
-        for (int j = 0; j < kSubs; ++j) {
+        for (int j = 0; j < SUBS; ++j) {
             // next sub-chunk (or the next item's first) in flight while this one is summed
-            if (j + 1 < kSubs) {
+            if (j + 1 < SUBS) {
                 load_sub(item, j + 1, k_nxt, v_nxt);
             } else {
                 load_sub(pending, 0, k_nxt, v_nxt);
@@ -825,7 +840,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
             if (lane == 0) prev = last_key;
             uint32_t next = __shfl_down_sync(0xffffffffu, k, 1);
             const uint32_t first_next = __shfl_sync(0xffffffffu, k_nxt, 0);
-            if (lane == kWarp - 1) next = j + 1 < kSubs ? first_next : after;
+            if (lane == kWarp - 1) next = j + 1 < SUBS ? first_next : after;
             const bool head = valid && prev != k;
             const bool endq = valid && next != k;
             const uint32_t hm = __ballot_sync(0xffffffffu, head);
@@ -902,7 +917,7 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
             const bool st_last = __shfl_sync(0xffffffffu, stq, lastq < 0 ? 0 : lastq);
             if (cont) {
                 cs = st_last;
-                if (j == kSubs - 1) {   // it continues past the item: a trailing or middle piece
+                if (j == SUBS - 1) {   // it continues past the item: a trailing or middle piece
                     const int64_t slot = st_last ? 2 * item + 1 : 2 * item;
 #pragma unroll
                     for (int m = 0; m < MC; ++m) {
@@ -933,20 +948,20 @@ segment_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ v
     }
 }
 
-template <int MC, typename GT>
-dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables, int64_t total_rows,
+template <int MC, typename GT, int SUBS>
+dlrm_status launch_segments_subs(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables, int64_t total_rows,
                             float lr, int64_t nbags, cudaStream_t st)
 {
-    constexpr int64_t IT = (int64_t)kWarp * kSubs;
+    constexpr int64_t IT = (int64_t)kWarp * SUBS;
     const int64_t nitems = (nnz + IT - 1) / IT;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segment_kernel<MC, GT>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segment_kernel<MC, GT, SUBS>, 256, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     int64_t blocks = (int64_t)num_sms() * per_sm;   // one resident wave; warps take items from a counter
     const int64_t need = (nitems + 7) / 8;
     if (blocks > need) blocks = need;
-    dlrm_status s = check_launch_pdl(launch_pdl(segment_kernel<MC, GT>, (int)blocks, 256, 0, st,
+    dlrm_status s = check_launch_pdl(launch_pdl(segment_kernel<MC, GT, SUBS>, (int)blocks, 256, 0, st,
                                                 (const uint32_t*)w.keys[0], (const uint32_t*)w.vals[0], nnz, grad,
                                                 D, tables, total_rows, lr, w.partials, w.split_list, w.long_list,
                                                 w.counters, nitems, nbags),
@@ -966,6 +981,15 @@ dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, flo
                                        (const uint64_t*)w.split_list, (const uint64_t*)w.long_list,
                                        (const uint32_t*)w.counters, IT, D, tables, total_rows, lr),
                             "fixup_kernel");
+}
+
+template <int MC, typename GT>
+dlrm_status launch_segments(const Ws& w, int64_t nnz, const GT* grad, int D, float* tables, int64_t total_rows,
+                            float lr, int64_t nbags, cudaStream_t st)
+{
+    if (item_subs(nnz) == kSubsSmall)
+        return launch_segments_subs<MC, GT, kSubsSmall>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
+    return launch_segments_subs<MC, GT, kSubs>(w, nnz, grad, D, tables, total_rows, lr, nbags, st);
 }
 
 // The segment pass and the fixup for the gradient type and width.

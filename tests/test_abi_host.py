@@ -188,6 +188,16 @@ def test_gathering_backward_validation(L):
     assert f(FAKE, 0, FAKE, 26, 128, 0, None, FAKE, 0, FAKE, FAKE, 480, FAKE, FAKE, 0, None, None) == dl.DLRM_OK
 
 
+def test_sgd_workspace_grows_with_nnz(L):
+    """Callers size one workspace for their largest batch: the size never drops as
+    nnz grows, across the edge where short segment items stop (8,192 indices)."""
+    ns = list(range(8000, 8400)) + [8192 * 8 - 1, 8192 * 8, 8192 * 8 + 1, 10**6]
+    for D in (4, 128, 1024):
+        sizes = [L.dlrm_emb_bwd_sgd_workspace_size(n, D, 5000) for n in [1, 31, 32, 33, 256, 257] + ns]
+        assert all(x > 0 for x in sizes)
+        assert all(a <= b for a, b in zip(sizes, sizes[1:]))
+
+
 def test_sgd_workspace_and_validation(L):
     ws = L.dlrm_emb_bwd_sgd_workspace_size
     assert ws(-1, 128, 10) == 0 and ws(10, 3, 10) == 0 and ws(10, 128, 0) == 0
