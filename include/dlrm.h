@@ -316,7 +316,7 @@ dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_base, int64_t
  *  - Sizes whose dlrm_emb_bwd_sgd_workspace_size(nnz, D, total_rows) exceeds
  *    DLRM_NOALLOC_SCRATCH_BYTES are rejected with DLRM_ERR_UNSUPPORTED before
  *    anything is enqueued.  The workspace grows with nnz and D only, so the
- *    limit is at most 796,416 indices at D = 128 and 955,136 at D = 16.
+ *    limit is at most 809,216 indices at D = 128 and 973,632 at D = 16.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address in the current CUDA context and caches it; make
  *    that first call before any stream capture.  A call from another context

@@ -235,7 +235,7 @@ def test_binding_refuses_missing_library(tmp_path):
         dl.load(str(tmp_path / "nope.so"))
 
 
-@pytest.mark.parametrize("D,limit", [(128, 796_416), (16, 955_136)])
+@pytest.mark.parametrize("D,limit", [(128, 809_216), (16, 973_632)])
 def test_noalloc_capacity_quoted_in_the_header(L, D, limit):
     """The most indices dlrm_emb_bwd_sgd_noalloc takes, as include/dlrm.h quotes them: the
     workspace of `limit` indices fits the built-in scratch and one more does not, whatever
@@ -249,6 +249,6 @@ def test_noalloc_capacity_quoted_in_the_header(L, D, limit):
 
 def test_noalloc_rejects_over_capacity_before_any_launch(L):
     """One index past the capacity is refused on the host (nothing reaches the GPU)."""
-    rc = L.dlrm_emb_bwd_sgd_noalloc(FAKE, FAKE, 10, 1, 128, 796_417, FAKE, FAKE, 796_417, FAKE,
+    rc = L.dlrm_emb_bwd_sgd_noalloc(FAKE, FAKE, 10, 1, 128, 809_217, FAKE, FAKE, 809_217, FAKE,
                                     ctypes.c_float(0.1), 0, None, None)
     assert rc == dl.DLRM_ERR_UNSUPPORTED and "scratch" in _err(L)
