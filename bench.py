@@ -1025,10 +1025,11 @@ def run_bottom_mlp(args, dl, inputs, torch, dev, stream, status) -> list:
 LOSS_SCALE = 1024.0
 
 
-def amp_step_ops(dl, wb, torch, dev, stream, status, tab, buffers=None, alternate=True):
+def amp_step_ops(dl, wb, torch, dev, stream, status, tab, buffers=None, alternate=True, io=None):
     """The mixed-precision training step's four calls, on device buffers; the calls rotate
     through the batches of ``wb`` (a workload or a list of workloads over the same tables).
-    ``buffers``, if a dict, receives the first batch's input and output tensors."""
+    ``buffers``, if a dict, receives the first batch's input and output tensors; ``io``, if a
+    dict, is read at each call instead: its "in" (idx, off, dense, g), "out" and "gd" tensors."""
     wb = wb if isinstance(wb, list) else [wb]
     w = wb[0]
     F, D, B, P = w.F, w.D, w.B, w.out_cols
@@ -1054,18 +1055,24 @@ def amp_step_ops(dl, wb, torch, dev, stream, status, tab, buffers=None, alternat
     cur = {}
 
     def fwd():
-        d = bat[k[0] % len(bat)]
-        cur["d"], cur["g"] = d, d["g"] if not alternate or (k[0] // len(bat)) % 2 == 0 else d["g_neg"]
+        if io is not None:
+            d = io["in"]
+            cur["d"], cur["g"] = d, d["g"]
+        else:
+            d = bat[k[0] % len(bat)]
+            cur["d"], cur["g"] = d, d["g"] if not alternate or (k[0] // len(bat)) % 2 == 0 else d["g_neg"]
         k[0] += 1
         dl.dlrm_emb_fwd(tab, rb, F, D, B, d["idx"], d["off"], pooled, flags=dl.DLRM_FLAG_POOLED_F16, status=status,
                         stream=stream)
 
     return [
         ("emb_fwd", fwd),
-        ("interact_fwd", lambda: dl.dlrm_interact_fwd(cur["d"]["dense"], pooled, F, D, B, out, P, status=status,
+        ("interact_fwd", lambda: dl.dlrm_interact_fwd(cur["d"]["dense"], pooled, F, D, B,
+                                                      out if io is None else io["out"], P, status=status,
                                                       stream=stream)),
-        ("interact_bwd", lambda: dl.dlrm_interact_bwd_f16(cur["g"], cur["d"]["dense"], pooled, F, D, B, P, gd, gp,
-                                                          status=status, stream=stream)),
+        ("interact_bwd", lambda: dl.dlrm_interact_bwd_f16(cur["g"], cur["d"]["dense"], pooled, F, D, B, P,
+                                                          gd if io is None else io["gd"], gp, status=status,
+                                                          stream=stream)),
         ("emb_bwd_sgd", lambda: dl.dlrm_emb_bwd_sgd(tab, rb, w.total_rows, F, D, B, cur["d"]["idx"],
                                                     cur["d"]["off"], gp, lr, ws, flags=dl.DLRM_FLAG_GRAD_F16,
                                                     status=status, stream=stream)),
@@ -1085,17 +1092,25 @@ def run_train_amp(args, dl, inputs, torch, dev, stream, status) -> list:
     per, ms = _time_ops(torch, stream, ops, args.steps, args.warmup)
     F, D, P, nnz = w.F, w.D, w.out_cols, w.nnz
     # end to end on one batch: its indices, offsets, dense rows and scaled gradient up, the
-    # interaction output and the dense gradient back
+    # interaction output and the dense gradient back, every step (both schedules, as the configs)
     bufs = {}
-    eops = amp_step_ops(dl, [w], torch, dev, stream, status, tab, buffers=bufs, alternate=False)
-    g16 = (w.grad_out.astype(np.float64) * LOSS_SCALE).astype(np.float16)
-    e2e = _e2e(torch, stream, eops,
-               [(bufs["idx"], torch.from_numpy(w.indices).pin_memory()),
-                (bufs["off"], torch.from_numpy(w.offsets).pin_memory()),
-                (bufs["dense"], torch.from_numpy(w.dense.astype(np.float16)).pin_memory()),
-                (bufs["g"], torch.from_numpy(g16).pin_memory())],
-               [(bufs["out"], _pinned(torch, bufs["out"])), (bufs["gd"], _pinned(torch, bufs["gd"]))],
-               max(E2E_MIN_STEPS, args.steps), B)
+    amp_step_ops(dl, [w], torch, dev, stream, status, tab, buffers=bufs, alternate=False)
+    in_parts = [(n_, bufs[n_]) for n_ in ("idx", "off", "dense", "g")]
+    out_parts = [("out", bufs["out"]), ("gd", bufs["gd"])]
+    h_in = _pack_host(torch, in_parts)
+    slots_in = [_packed_views(torch, dev, in_parts) for _ in range(2)]
+    slots_out = [_packed_views(torch, dev, out_parts) for _ in range(2)]
+    io = {}
+    eops = amp_step_ops(dl, [w], torch, dev, stream, status, tab, alternate=False, io=io)
+
+    def bind(slot):
+        io["in"] = slots_in[slot][1]
+        io["out"] = slots_out[slot][1]["out"]
+        io["gd"] = slots_out[slot][1]["gd"]
+
+    e2e = _e2e_pipelined(torch, stream, eops, bind, [x[0] for x in slots_in], h_in, [x[0] for x in slots_out],
+                         max(E2E_MIN_STEPS, args.steps), B)
+    del slots_in, slots_out, bufs
     touched = statistics.mean(touched_rows(x) for x in wb)
     alg = {"emb_fwd": nnz * (4 + 4 + D * 4) + B * F * D * 2,
            "interact_fwd": B * (D * 2 + F * D * 2 + P * 2),
