@@ -329,6 +329,7 @@ radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ t
 // positions offsets[b * bpb] .. offsets[(b + 1) * bpb] (clamped), taken in
 // sub-tiles of kTile keys, each digit's output offset advancing by the
 // sub-tile's count; later passes' tiles are fixed ranges of kTile positions.
+template <bool kReorder>
 __global__ void __launch_bounds__(kSortThreads)
 radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
                 uint32_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out, int64_t n, int shift,
@@ -340,6 +341,8 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
     __shared__ uint32_t wcnt[kW][256];
     __shared__ uint32_t dbase[256];
     __shared__ uint32_t warp_sums[kW];
+    __shared__ uint32_t tstart[kReorder ? 256 : 1];       // first place of each digit in the sub-tile
+    __shared__ uint32_t skey[kReorder ? kTile : 1], sval[kReorder ? kTile : 1];
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     const uint32_t lt = (1u << lane) - 1u;
     int64_t lo, hi;
@@ -387,16 +390,46 @@ radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict
             wcnt[w][threadIdx.x] = subtotal;
             subtotal += c;
         }
-        __syncthreads();
+        if constexpr (kReorder) {
+            // the sub-tile ordered by digit in shared memory first, then written out in that
+            // order: consecutive threads write consecutive places of a digit's range
+            tstart[threadIdx.x] = block_excl_scan(subtotal, warp_sums, nullptr);
+            __syncthreads();
 #pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            const int64_t p = wbase + r * kWarp + lane;
-            if (p < hi) {
-                const uint32_t d = (key[r] >> shift) & mask;
-                const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
-                if (pos < n) {   // always true for consistent histograms; guards the write
-                    keys_out[pos] = key[r];
-                    vals_out[pos] = val[r];
+            for (int r = 0; r < kItems; ++r) {
+                const int64_t p = wbase + r * kWarp + lane;
+                if (p < hi) {
+                    const uint32_t d = (key[r] >> shift) & mask;
+                    const uint32_t lp = tstart[d] + wcnt[warp][d] + local[r];
+                    if (lp < (uint32_t)kTile) {   // always true for consistent counts; guards the write
+                        skey[lp] = key[r];
+                        sval[lp] = val[r];
+                    }
+                }
+            }
+            __syncthreads();
+            const int cnt = (int)(hi - sub < kTile ? hi - sub : kTile);
+            for (int i = threadIdx.x; i < cnt; i += kSortThreads) {
+                const uint32_t k2 = skey[i];
+                const uint32_t d = (k2 >> shift) & mask;
+                const uint32_t pos = dbase[d] + ((uint32_t)i - tstart[d]);
+                if (pos < n) {
+                    keys_out[pos] = k2;
+                    vals_out[pos] = sval[i];
+                }
+            }
+        } else {
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < kItems; ++r) {
+                const int64_t p = wbase + r * kWarp + lane;
+                if (p < hi) {
+                    const uint32_t d = (key[r] >> shift) & mask;
+                    const uint32_t pos = dbase[d] + wcnt[warp][d] + local[r];
+                    if (pos < n) {   // always true for consistent histograms; guards the write
+                        keys_out[pos] = key[r];
+                        vals_out[pos] = val[r];
+                    }
                 }
             }
         }
@@ -1101,7 +1134,8 @@ extern "C" dlrm_status dlrm_emb_bwd_sgd(float* d_tables, const int64_t* d_row_ba
                            mask, w.hist, ntiles);
         if (e == cudaSuccess) e = launch_pdl(radix_scan, 256, kSortThreads, 0, st, w.hist, ntiles, w.totals);
         if (e == cudaSuccess)
-            e = launch_pdl(radix_downsweep, (int)ntiles, kSortThreads, 0, st, (const uint32_t*)w.keys[cur],
+            e = launch_pdl(pass == 0 ? radix_downsweep<true> : radix_downsweep<false>, (int)ntiles, kSortThreads, 0,
+                           st, (const uint32_t*)w.keys[cur],
                            (const uint32_t*)w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], nnz, shift, mask,
                            (const uint32_t*)w.hist, (const uint32_t*)w.totals, ntiles,
                            pass == 0 ? d_offsets : (const int32_t*)nullptr, bpb, nbags);
