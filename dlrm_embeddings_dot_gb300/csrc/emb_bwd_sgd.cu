@@ -329,6 +329,11 @@ radix_scan(uint32_t* __restrict__ hist, int64_t ntiles, uint32_t* __restrict__ t
 // positions offsets[b * bpb] .. offsets[(b + 1) * bpb] (clamped), taken in
 // sub-tiles of kTile keys, each digit's output offset advancing by the
 // sub-tile's count; later passes' tiles are fixed ranges of kTile positions.
+// kReorder (the first pass, whose input is in position order): each sub-tile
+// is placed in shared memory by digit before it is written out, so that
+// neighbouring threads write neighbouring places of a digit's output range
+// (Zipf-hot keys spread over a warp otherwise make every write its own
+// request); later passes read keys already grouped by their lower digits.
 template <bool kReorder>
 __global__ void __launch_bounds__(kSortThreads)
 radix_downsweep(const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
