@@ -71,3 +71,25 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
     assert capsys.readouterr().out == ""   # the other ranks exit without work
+
+
+def test_packed_e2e_buffers_alias_their_parts():
+    """The end-to-end loops copy one packed buffer per direction: every part sits at a 256-byte
+    aligned offset, in order, and the views the calls take alias exactly its bytes."""
+    import torch
+
+    import bench
+
+    offs, tot = bench._pack_layout([5, 256, 257, 0, 12])
+    assert offs == [0, 256, 512, 1024, 1024] and tot == 1280
+    parts = [("a", torch.arange(7, dtype=torch.int32)), ("b", torch.ones(3, 5, dtype=torch.float16)),
+             ("c", torch.full((2, 2), 2.5, dtype=torch.float32))]
+    buf, views = bench._packed_views(torch, torch.device("cpu"), parts)
+    offs, tot = bench._pack_layout([t.numel() * t.element_size() for _, t in parts])
+    assert buf.numel() == tot and buf.dtype == torch.uint8
+    for (name, t), o in zip(parts, offs):
+        v = views[name]
+        assert v.shape == t.shape and v.dtype == t.dtype
+        v.copy_(t)
+        n = t.numel() * t.element_size()
+        assert torch.equal(buf[o:o + n], t.contiguous().view(-1).view(torch.uint8))
