@@ -275,10 +275,9 @@ size_t dlrm_emb_bwd_sgd_workspace_size(int64_t nnz, int D, int64_t total_rows);
  * row; the sorted pairs are cut into items of 256 positions (32 when nnz is
  * at most 8,192), each row's gradients are summed in ascending position order
  * within an item, and the sums of a row that spans several items are
- * combined in item order (a row
- * spanning more than 8 items: 16 contiguous slices of its items, each in
- * order, then the slices in order).  Skipped indices (see dlrm_emb_fwd)
- * contribute nothing.
+ * combined in item order (a row spanning more than 8 items: 16 contiguous
+ * slices of its items, each in order, then the slices in order).  Skipped
+ * indices (see dlrm_emb_fwd) contribute nothing.
  *
  *   d_tables       fp32 [total_rows][D], updated in place, 16-byte aligned
  *   d_row_base     int64 [F+1] with row_base[F] = total_rows
