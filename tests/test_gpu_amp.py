@@ -173,3 +173,28 @@ def test_amp_training_step_64k_sampled(cuda_lib):
     sd, sp = abs_bwd(g16[samples].astype(np.float64), dense16[samples], rp)
     _close16(gd[sel].cpu().numpy(), rgd, sd, "grad_dense (sampled)")
     _close16(gp[sel].cpu().numpy(), rgp, sp, "grad_pooled (sampled)")
+
+
+@pytest.mark.parametrize("B", [3000, 5000])   # 6,000 and 10,000 indices: both sort paths, D = 128
+def test_sgd_with_fp16_gradients_both_sort_paths(cuda_lib, B):
+    """fp16 gradients of 128-wide rows below and above the one-block sort's 8,192 indices:
+    bit-identical to the same gradients widened to fp32, and within the oracle's bar."""
+    dl = cuda_lib
+    rng = np.random.default_rng(B)
+    F, D = 2, 128
+    rows = np.array([1500, 700])
+    row_base = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    tables = rng.uniform(-0.05, 0.05, size=(row_base[-1], D)).astype(np.float32)
+    idx = np.concatenate([np.where(rng.random(B) < 0.4, 3, rng.integers(0, n, size=B)) for n in rows]).astype(np.int32)
+    off = np.arange(F * B + 1)
+    g16 = (rng.normal(0.0, 1e-2, size=(B, F, D)) * S).astype(np.float16)
+    lr = np.float32(0.1 / S)
+    t16, st16, k16, v16 = run_sgd(dl, tables, row_base, F, D, B, idx, off, g16, lr, flags=dl.DLRM_FLAG_GRAD_F16)
+    t32, st32, k32, v32 = run_sgd(dl, tables, row_base, F, D, B, idx, off, g16.astype(np.float32), lr)
+    assert st16 == st32 == 0 and np.array_equal(k16, k32) and np.array_equal(v16, v32)
+    assert np.array_equal(t16.cpu().numpy(), t32.cpu().numpy()), "fp16 gradients widen exactly"
+    ref, _, rk, _ = oracle.emb_bwd_sgd(tables, row_base, F, D, B, idx, off, g16.astype(np.float32), float(lr))
+    assert np.array_equal(k16, rk)
+    assert_within_abs_sum(t16.cpu().numpy(), ref,
+                          abs_scale(tables, row_base, F, B, D, idx, off, g16.astype(np.float32), float(lr)), 1e-5,
+                          "tables")
