@@ -132,16 +132,21 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+def ncu_traffic(kernel: str, batch: int = None):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source.  A
+    capture on a smaller batch (the recipe's size rule) is scaled to `batch` by the samples
+    processed, the kernel's traffic growing in proportion to them; returns (bytes, note)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
-        return None
+        return None, None
     with open(p) as f:
         e = json.load(f).get(kernel)
     if not e or e.get("source_digest") != source_digest(e.get("source_files", [])):
-        return None
-    return e.get("dram_bytes_per_launch")
+        return None, None
+    dram, cb = e.get("dram_bytes_per_launch"), e.get("captured_batch")
+    if batch and cb and cb != batch:
+        return int(round(dram * batch / cb)), f"ncu capture at batch {cb} ({dram} B) scaled by {batch}/{cb} samples"
+    return dram, f"ncu capture at batch {cb}" if cb else None
 
 
 # ------------------------------------------------------------ oracle (CPU)
@@ -614,10 +619,11 @@ def run_ours(args) -> None:
     kernel_names = {"emb_interact_fwd": "emb_interact_regs_kernel", "interact_bwd": "interact_bwd_regs_kernel",
                     "emb_bwd_sgd": f"emb_bwd_sgd ({sgd_kernels(w.total_rows)} kernels)"}
     achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
+    traffic, traffic_note = ncu_traffic(dom if dom == "emb_bwd_sgd" else kernel_names[dom], batch=B)
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": ncu_traffic(dom if dom == "emb_bwd_sgd" else kernel_names[dom]),
+            "traffic": traffic, "traffic_note": traffic_note,
             "algorithmic_bytes_per_launch": int(alg[dom]), "launch_ms": round(op_ms[dom], 4)}
     op_frac = {k: round(alg[k] / (v / 1e3) / 1e9 / peaks["hbm_gbs"], 4) for k, v in op_ms.items()}
 
